@@ -1,0 +1,124 @@
+/*
+ * decode_body.h -- the oracle's decode read, written once and included by
+ * np_oracle.c for each working precision (NPO_REAL = double or float).
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE (see np_oracle.c).
+ *
+ * For each row r, kv head kh, query head h of that kv head's group and
+ * split s:
+ *   1. gather: for t < context_lens[r], K_t and V_t are the [head_dim]
+ *      vectors at pool slot block_tables[r][t / bs] * bs + t % bs, kv head
+ *      kh ("Day 17: paging under the sampling path", Diagram: a block table
+ *      maps tokens to blocks; "Day 25: the fused read dispatches to the
+ *      kernel backend", What I added today: SDPA over the assembled slots);
+ *   2. scores: s_t = scale * sum_d q[r, h, d] * K_t[d], over the split's
+ *      tokens t in [s * split_len, min((s + 1) * split_len, c));
+ *   3. exact two-pass softmax by index: m = max_t s_t,
+ *      p_t = exp(s_t - m), Z = sum_t p_t ("Day 25", What I learned 1);
+ *   4. out = sum_t p_t V_t / Z and lse = m + log Z.
+ * An empty split (no tokens) gives out = 0 and lse = -inf.  With
+ * num_splits = 1 and split_len >= the context this is the whole read.
+ *
+ * Layouts (all dense, row-major):
+ *   q            [rows, q_heads, head_dim]           storage dtype
+ *   k/v_pool     [num_blocks, block_size, kv_heads, head_dim]
+ *   block_tables [rows, max_blocks_per_row] int32 (entries past the row's
+ *                last needed block are never read)
+ *   context_lens [rows] int32
+ *   out          [rows, q_heads, num_splits, head_dim]  NPO_REAL
+ *   lse          [rows, q_heads, num_splits]            NPO_REAL
+ */
+
+int NPO_NAME(npo_paged_decode)(
+    NPO_REAL* out, NPO_REAL* lse, const void* q, const void* k_pool,
+    const void* v_pool, int dtype, int64_t num_blocks, int32_t block_size,
+    int32_t kv_heads, int32_t head_dim, const int32_t* block_tables,
+    int32_t max_blocks_per_row, const int32_t* context_lens, int32_t rows,
+    int32_t q_heads, double scale, int64_t split_len, int32_t num_splits) {
+  if (npo_elem_size(dtype) == 0 || num_blocks <= 0 || block_size <= 0 ||
+      kv_heads <= 0 || head_dim <= 0 || max_blocks_per_row < 0 || rows < 0 ||
+      q_heads <= 0 || q_heads % kv_heads != 0 || split_len <= 0 ||
+      num_splits <= 0)
+    return NPO_BAD_ARG;
+  const int32_t group = q_heads / kv_heads;
+  const NPO_REAL sc = (NPO_REAL)scale;
+  const int64_t capacity = (int64_t)max_blocks_per_row * block_size;
+
+  for (int32_t r = 0; r < rows; ++r) {
+    const int64_t c = context_lens[r];
+    if (c < 0 || c > capacity) return NPO_BAD_CONTEXT;
+    if (c > split_len * (int64_t)num_splits) return NPO_BAD_ARG;
+
+    for (int32_t kh = 0; kh < kv_heads; ++kh) {
+      /* 1. gather this row's history for kv head kh into contiguous arrays */
+      size_t n = (size_t)(c > 0 ? c : 1);
+      NPO_REAL* hk = (NPO_REAL*)malloc(n * (size_t)head_dim * sizeof(NPO_REAL));
+      NPO_REAL* hv = (NPO_REAL*)malloc(n * (size_t)head_dim * sizeof(NPO_REAL));
+      NPO_REAL* sco = (NPO_REAL*)malloc(n * sizeof(NPO_REAL));
+      if (!hk || !hv || !sco) {
+        free(hk);
+        free(hv);
+        free(sco);
+        return NPO_NO_MEMORY;
+      }
+      for (int64_t t = 0; t < c; ++t) {
+        int64_t block = block_tables[(int64_t)r * max_blocks_per_row + t / block_size];
+        if (block < 0 || block >= num_blocks) {
+          free(hk);
+          free(hv);
+          free(sco);
+          return NPO_BAD_BLOCK;
+        }
+        int64_t slot = block * block_size + t % block_size;
+        for (int32_t d = 0; d < head_dim; ++d) {
+          int64_t idx = (slot * kv_heads + kh) * head_dim + d;
+          hk[t * head_dim + d] = (NPO_REAL)npo_load(k_pool, dtype, idx);
+          hv[t * head_dim + d] = (NPO_REAL)npo_load(v_pool, dtype, idx);
+        }
+      }
+
+      for (int32_t h = kh * group; h < (kh + 1) * group; ++h) {
+        for (int32_t s = 0; s < num_splits; ++s) {
+          int64_t rhs = ((int64_t)r * q_heads + h) * num_splits + s;
+          NPO_REAL* o = out + rhs * head_dim;
+          int64_t tb = (int64_t)s * split_len;
+          int64_t te = tb + split_len < c ? tb + split_len : c;
+          for (int32_t d = 0; d < head_dim; ++d) o[d] = 0;
+          if (tb >= te) {
+            lse[rhs] = -INFINITY;
+            continue;
+          }
+          /* 2. scores */
+          for (int64_t t = tb; t < te; ++t) {
+            NPO_REAL dot = 0;
+            for (int32_t d = 0; d < head_dim; ++d) {
+              NPO_REAL qd = (NPO_REAL)npo_load(
+                  q, dtype, ((int64_t)r * q_heads + h) * head_dim + d);
+              dot += qd * hk[t * head_dim + d];
+            }
+            sco[t] = sc * dot;
+          }
+          /* 3. exact softmax: max, exponentials, their sum */
+          NPO_REAL m = sco[tb];
+          for (int64_t t = tb + 1; t < te; ++t)
+            if (sco[t] > m) m = sco[t];
+          NPO_REAL z = 0;
+          for (int64_t t = tb; t < te; ++t) {
+            sco[t] = NPO_EXP(sco[t] - m);
+            z += sco[t];
+          }
+          /* 4. probability-weighted sum of V, and the log-sum-exp */
+          for (int64_t t = tb; t < te; ++t)
+            for (int32_t d = 0; d < head_dim; ++d)
+              o[d] += sco[t] * hv[t * head_dim + d];
+          for (int32_t d = 0; d < head_dim; ++d) o[d] /= z;
+          lse[rhs] = m + NPO_LOG(z);
+        }
+      }
+      free(hk);
+      free(hv);
+      free(sco);
+    }
+  }
+  return NPO_OK;
+}
