@@ -1,0 +1,452 @@
+#!/usr/bin/env python3
+"""Benchmark of one decode step of the paged read: append + read (+ reduce).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+Prints ONE JSON line.  ``value`` is KV GB/s: the K and V bytes of every row's
+history (sum_r c_r * 2 * kv_heads * head_dim * elem_size) read by one step,
+divided by the device time of the step (CUDA events, K steps between a
+barrier + synchronize on both sides, max over ranks), aggregated over ranks.
+Inputs are resident in HBM before timing.  ``e2e`` is the same metric when
+every step also copies its per-step inputs (q, new K/V, slot mapping, block
+tables, context lengths) from pinned host memory and reads the output back.
+``--impl reference`` times the CPU oracle instead, on a bounded sample.
+
+Multi-GPU (torchrun): rows are independent, so each rank runs its own
+replica of the workload (its own pool and batch) with no collective on the
+data path ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+DEFAULT_WORKLOAD = "bf16-long"
+METRIC = "paged decode read: KV GB/s and % of GB300 HBM peak; µs per decode step"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2**20
+
+
+# ------------------------------------------------------------ accounting ---
+def algorithmic_bytes(w: wl.Workload, md: wl.Metadata) -> dict:
+    """Bytes one step must move at minimum, by kernel.
+
+    decode: every history token's K and V rows once, q once, out once, the
+    table entries the walk needs once, the context lengths once (the split
+    partials are not algorithmic: they are this implementation's overhead).
+    append: the new tokens' K/V read once and written once, plus slots.
+    """
+    cl = md.context_lens.to(torch.int64)
+    es = w.elem_size
+    kv = int(cl.sum()) * 2 * w.kv_heads * w.head_dim * es
+    qo = 2 * w.rows * w.q_heads * w.head_dim * es
+    tab = int(((cl + w.block_size - 1) // w.block_size).sum()) * 4 + 4 * w.rows
+    app = 2 * 2 * w.rows * w.kv_heads * w.head_dim * es + 8 * w.rows
+    return {"kv": kv, "decode": kv + qo + tab, "append": app}
+
+
+def measured_peak() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_np_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str) -> float | None:
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"kernel_sources_sha256:\s*([0-9a-f]+)", txt)
+    t = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m or not t or m.group(1) != kernel_sources_hash():
+        return None
+    return float(t.group(1))
+
+
+# ---------------------------------------------------------------- clocks ---
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: torch.device):
+        self.gpu = None
+        try:  # nvidia-smi wants the PCI bus id of the device torch is using
+            pr = torch.cuda.get_device_properties(device)
+            self.gpu = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+        except Exception:
+            pass
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *([f"--id={self.gpu}"] if self.gpu else []),
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=5)
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ distributed --
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        return dist, rank, world, local
+    return None, 0, 1, 0
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle ---
+def oracle_sample(inp: wl.Inputs, budget_s: float, seed: int = 0) -> dict:
+    """Time the oracle (single-threaded C, as it stands) on rows of the step
+    until ``budget_s`` seconds of work are done.  Host copies are made first."""
+    import oracle
+
+    w = inp.w
+    g = torch.Generator().manual_seed(seed)
+    order = torch.randperm(w.rows, generator=g).tolist()
+    done_rows, kv_bytes, elapsed = [], 0, 0.0
+    per_token = 2 * w.kv_heads * w.head_dim * w.elem_size
+    for r in order:
+        host = wl.row_subproblem(inp, [r])
+        kp, vp = host["k_pool"].copy(), host["v_pool"].copy()
+        t0 = time.perf_counter()
+        oracle.kv_append(kp, vp, host["k_new"], host["v_new"], host["slot_mapping"])
+        oracle.paged_decode(host["q"], kp, vp, host["block_tables"], host["context_lens"],
+                            w.softmax_scale)
+        elapsed += time.perf_counter() - t0
+        done_rows.append(r)
+        kv_bytes += int(host["context_lens"][0]) * per_token
+        if elapsed >= budget_s:
+            break
+    return {"rows": done_rows, "kv_bytes": kv_bytes, "seconds": elapsed,
+            "gbs": kv_bytes / elapsed / 1e9 if elapsed > 0 else None}
+
+
+# ---------------------------------------------------------------- arms ----
+def run_reference(args, w: wl.Workload, dist, rank):
+    """The oracle arm: each step is the oracle on a bounded sample of rows."""
+    if rank != 0:
+        return None
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = wl.make_inputs(w, device=dev, poison=False)
+    step_budget = args.ref_step_seconds
+    for i in range(args.warmup):
+        oracle_sample(inp, step_budget, seed=1000 + i)
+    times, kvb, rows = [], 0, []
+    for i in range(args.steps):
+        s = oracle_sample(inp, step_budget, seed=i)
+        times.append(s["seconds"])
+        kvb += s["kv_bytes"]
+        rows.append(len(s["rows"]))
+    total = sum(times)
+    value = kvb / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step: the single-threaded C oracle (fp64) on "
+                                   f"randomly chosen rows of the {w.name} step until "
+                                   f"{step_budget:g} s of work ({statistics.mean(rows):.1f} "
+                                   f"rows per step on average)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def run_ours(args, w: wl.Workload, dist, rank, world, local):
+    import paged_kv_decode_np_gb300 as npg
+
+    npg.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = wl.make_inputs(w, device=dev, poison=False)
+    md = inp.md
+    bt, cl, sm = (t.to(dev) for t in (md.block_tables, md.context_lens, md.slot_mapping))
+    S = npg.np_paged_decode_plan(w.rows, w.q_heads, w.kv_heads, w.head_dim, w.block_size,
+                                 bt.shape[1], w.torch_dtype)
+    ws = npg.workspace(w.rows, w.q_heads, w.head_dim, S, device=dev)
+    out = torch.empty_like(inp.q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    nbytes = algorithmic_bytes(w, md)
+    # inputs larger than L2 need no flush; otherwise write a 2xL2 buffer
+    # between timed steps, outside the timed kernels
+    flush = None
+    if nbytes["kv"] < 4 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(rec=None):
+        launches = 0
+        npg.np_kv_append(inp.k_pool, inp.v_pool, inp.k_new, inp.v_new, sm, err, stream)
+        launches += 1
+        if rec is not None:
+            rec[0].record(stream)
+        npg.np_paged_decode(out if S == 1 else None, inp.q, inp.k_pool, inp.v_pool, bt, cl,
+                            w.softmax_scale, S, ws, err, stream)
+        if rec is not None:
+            rec[1].record(stream)
+        launches += 1
+        if S > 1:
+            npg.np_paged_decode_reduce(out, ws, S, stream)
+            launches += 1
+        return launches
+
+    # CPU baseline first (host copies of the sampled rows before any kernel)
+    cpu = oracle_sample(inp, args.cpu_seconds) if (rank == 0 and world == 1) else None
+
+    for _ in range(args.warmup):
+        step()
+        if flush is not None:
+            flush.zero_()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    st_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    launches = 0
+    with ClockSampler(dev) as clk:
+        barrier(dist)
+        torch.cuda.synchronize()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            st_ev[i][0].record(stream)
+            launches += step(ev[i])
+            st_ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+    if flush is None:
+        elapsed_ms = t_start.elapsed_time(t_end)
+    else:  # exclude the L2 flushes between steps
+        elapsed_ms = sum(a.elapsed_time(b) for a, b in st_ev)
+    decode_ms = [a.elapsed_time(b) for a, b in ev]
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error flags {int(err.item()):#x}")
+
+    # end-to-end through the C ABI with host buffers
+    pin = {k: t.to("cpu").pin_memory() for k, t in
+           dict(q=inp.q, k_new=inp.k_new, v_new=inp.v_new, sm=sm, bt=bt, cl=cl).items()}
+    dbuf = {k: torch.empty_like(t, device=dev) for k, t in pin.items()}
+    out_host = torch.empty_like(out, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for k in pin:
+            dbuf[k].copy_(pin[k], non_blocking=True)
+        npg.np_kv_append(inp.k_pool, inp.v_pool, dbuf["k_new"], dbuf["v_new"], dbuf["sm"], err,
+                         stream)
+        npg.np_paged_decode(out if S == 1 else None, dbuf["q"], inp.k_pool, inp.v_pool,
+                            dbuf["bt"], dbuf["cl"], w.softmax_scale, S, ws, err, stream)
+        if S > 1:
+            npg.np_paged_decode_reduce(out, ws, S, stream)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_st = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        e_st[i][0].record(stream)
+        e2e_step()
+        e_st[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e_st)
+
+    # aggregate over ranks: max time, summed bytes
+    elapsed_ms = max_over_ranks(dist, elapsed_ms)
+    e2e_ms = max_over_ranks(dist, e2e_ms)
+    kv_total = sum_over_ranks(dist, float(nbytes["kv"])) * args.steps
+    if rank != 0:
+        return None
+    value = kv_total / (elapsed_ms / 1e3) / 1e9
+    e2e_value = kv_total / (e2e_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+    dec_avg_ms = statistics.mean(decode_ms)
+    achieved = nbytes["decode"] / (dec_avg_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "us_per_step": 1e3 * elapsed_ms / args.steps,
+        "frac_of_hbm_peak": value / world / peak,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) q/K/V, shuffled free-list block tables)",
+        "config": {
+            "workload": w.name, "description": w.description, "rows": w.rows,
+            "q_heads": w.q_heads, "kv_heads": w.kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "max_blocks_per_row": bt.shape[1],
+            "num_blocks": md.num_blocks, "num_splits": S,
+            "split_len": npg.np_paged_decode_split_len(w.block_size, bt.shape[1], S),
+            "mean_context": float(md.context_lens.double().mean()),
+            "kv_bytes_per_step": nbytes["kv"],
+            "l2": ("inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2"
+                   % (nbytes["kv"] / 1e9)) if flush is None else
+                  "L2 flushed (2x L2 buffer written) between timed steps, flush excluded",
+            "parallelism": f"replicas x{world} (rows independent, no collective)",
+        },
+        "roofline": {
+            "bound": "hbm", "kernel": "paged_decode_kernel", "achieved": achieved,
+            "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+            if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "unit": "GB/s", "frac": achieved / peak,
+            "traffic": profiled_traffic(w.name),
+            "algorithmic_bytes_per_launch": nbytes["decode"],
+            "avg_launch_ms": dec_avg_ms,
+        },
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = {
+            "value": cpu["gbs"], "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"rows {cpu['rows']} of this step ({cpu['kv_bytes'] / 1e9:.3f} GB of K/V,"
+                      f" {cpu['seconds']:.1f} s), single-threaded C oracle in fp64, "
+                      f"append + read"}
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=2.0)
+    args = ap.parse_args(argv)
+    if args.impl == "ours" and args.warmup < 3:
+        args.warmup = 3  # timing rule: at least 3 untimed warm-up steps
+    w = wl.WORKLOADS[args.workload]
+    dist, rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line = run_reference(args, w, dist, rank)
+    else:
+        line = run_ours(args, w, dist, rank, world, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,201 @@
+/*
+ * np_paged.h -- C ABI of the GB300 (sm_103a) batched paged-attention decode
+ * library, libnp_paged.so.
+ *
+ * The operation (one decode step of an inference engine's paged KV cache):
+ *
+ *   1. np_kv_append: each new token's K and V rows are written into a shared
+ *      pool of fixed-size blocks at the flat slot given by a slot mapping,
+ *      slot = physical_block * block_size + offset ("Day 25: the fused read
+ *      dispatches to the kernel backend", What I added today: the read gets
+ *      the layer's K/V pools and the slot mapping for the whole history;
+ *      What I learned 1: scatter and gather are exact copies).
+ *
+ *   2. np_paged_decode: each row's single query token attends over that
+ *      row's whole history, which is scattered over the pool and addressed
+ *      through the row's block table ("Day 17: paging under the sampling
+ *      path", Post angle and Diagram: a pool of fixed KV blocks and a block
+ *      table mapping tokens to blocks).  The result equals scaled-dot-product
+ *      attention over the gathered history ("Day 25", What I added today),
+ *      computed as a streamed (online) softmax that never materialises the
+ *      [rows, heads, 1, ctx] score rectangle ("Day 60: the read becomes a
+ *      choice", What I added today and Post angle).  Query heads share kv
+ *      heads in groups (GQA): q head h reads kv head h / (q_heads/kv_heads).
+ *
+ *   3. np_paged_decode_reduce: when the read is split along the context
+ *      (flash-decoding: each split of a row's history is read by its own
+ *      thread block), the per-split partial outputs are merged by their
+ *      log-sum-exp.  The pages do not describe this split; it is how this
+ *      library spreads long and ragged histories over the GPU.
+ *
+ * Conventions shared by every call:
+ *   - Every data pointer is CALLER-OWNED DEVICE memory on the current CUDA
+ *     device, dense and row-major in the layout stated for it, 16-byte
+ *     aligned.  The library never allocates, frees, or synchronises; it never
+ *     reads device memory back to the host, so a step can be captured in a
+ *     CUDA graph (after the first call on a device, which sets kernel
+ *     attributes).
+ *   - Work is enqueued on `stream` (NULL = the legacy default stream) and
+ *     runs asynchronously; the return value covers argument validation and
+ *     the launch only.  Validation failures return before anything is
+ *     enqueued.
+ *   - Device-side problems never trap or fault: the affected token/block is
+ *     skipped or clamped and a bit is OR-ed into *err_word (a device int32
+ *     the caller zeroes and reads when convenient; NULL = not reported).
+ *   - Pools: k_pool and v_pool are separate arrays, each
+ *     [num_blocks, block_size, kv_heads, head_dim] of `dtype`.
+ *   - Supported: dtype NP_F32 or NP_BF16; head_dim in {16, 32, 64, 128, 256};
+ *     group q_heads/kv_heads in {1, 2, 4, 5, 8}; any block_size >= 1; any
+ *     kv_heads >= 1.  Arithmetic is fp32 in every case (bf16 is widened
+ *     exactly); q and out have the pool dtype.
+ */
+#ifndef NP_PAGED_H
+#define NP_PAGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NP_ABI_VERSION 1
+
+/* Same type as cudaStream_t / CUstream, without pulling in CUDA headers. */
+typedef struct CUstream_st* np_stream_t;
+
+typedef enum np_status {
+  NP_OK = 0,
+  NP_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape or value */
+  NP_ERR_UNSUPPORTED = 2,  /* head_dim, group or dtype outside the set above */
+  NP_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+  NP_ERR_OUT_OF_RANGE = 4, /* a size whose byte count overflows int64 */
+  NP_ERR_CUDA = 5          /* a CUDA runtime call or launch failed */
+} np_status;
+
+typedef enum np_dtype { NP_F32 = 0, NP_BF16 = 1 } np_dtype;
+
+/* Bits OR-ed into *err_word by the kernels. */
+#define NP_FLAG_BLOCK_ID 0x1 /* a block-table entry the walk needed was outside
+                                [0, num_blocks); block 0 was read instead */
+#define NP_FLAG_CONTEXT 0x2  /* context_lens[r] < 0 or > max_blocks_per_row *
+                                block_size; clamped into that range */
+#define NP_FLAG_SLOT 0x4     /* an append slot >= num_blocks * block_size;
+                                that token was not written */
+#define NP_FLAG_TIMEOUT 0x8  /* an internal pipeline wait gave up (never
+                                expected; the output of that block is wrong) */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* np_status_string(np_status status);
+
+/* NP_ABI_VERSION of the loaded library. */
+int32_t np_abi_version(void);
+
+/*
+ * np_kv_append -- scatter this step's new K/V into the pools.
+ *   k_pool, v_pool  [num_blocks, block_size, kv_heads, head_dim] dtype (written)
+ *   k_new, v_new    [num_tokens, kv_heads, head_dim] dtype
+ *   slot_mapping    [num_tokens] int64: token i goes to pool slot
+ *                   slot_mapping[i] (element offset slot*kv_heads*head_dim);
+ *                   a negative slot means "padding, skip"; a slot
+ *                   >= num_blocks*block_size is skipped and flagged
+ *                   (NP_FLAG_SLOT).
+ * Bit-exact copy.  Two tokens with the same slot: one of them wins
+ * (unspecified which).  num_tokens == 0 is a no-op.
+ */
+np_status np_kv_append(void* k_pool, void* v_pool, np_dtype dtype,
+                       int64_t num_blocks, int32_t block_size,
+                       int32_t kv_heads, int32_t head_dim, const void* k_new,
+                       const void* v_new, const int64_t* slot_mapping,
+                       int32_t num_tokens, int32_t* err_word,
+                       np_stream_t stream);
+
+/*
+ * np_paged_decode_plan -- how many context splits the library recommends.
+ * Pure host arithmetic on STATIC shapes only (never on context_lens, so the
+ * choice needs no device read and a step stays graph-capturable).
+ * num_sms <= 0 queries the current device's SM count.
+ * Writes the split count (>= 1) to *num_splits.
+ */
+np_status np_paged_decode_plan(int32_t rows, int32_t q_heads, int32_t kv_heads,
+                               int32_t head_dim, int32_t block_size,
+                               int32_t max_blocks_per_row, np_dtype dtype,
+                               int32_t num_sms, int32_t* num_splits);
+
+/*
+ * np_paged_decode_split_len -- tokens per split for a given split count:
+ * ceil(max_blocks_per_row*block_size / num_splits) rounded up to a multiple
+ * of 64 tokens (and of block_size when block_size > 64).  Split s covers
+ * history tokens [s*split_len, (s+1)*split_len).  Returns -1 on bad input.
+ */
+int64_t np_paged_decode_split_len(int32_t block_size,
+                                  int32_t max_blocks_per_row,
+                                  int32_t num_splits);
+
+/*
+ * np_paged_decode_workspace_bytes -- workspace a split read needs:
+ *   partial outputs  [rows, q_heads, num_splits, head_dim] fp32 at offset 0,
+ *   partial lse      [rows, q_heads, num_splits] fp32 at the next 256-byte
+ *                    boundary (natural log; -inf for an empty split).
+ * 0 when num_splits <= 1.
+ */
+size_t np_paged_decode_workspace_bytes(int32_t rows, int32_t q_heads,
+                                       int32_t head_dim, int32_t num_splits);
+
+/*
+ * np_paged_decode -- the decode read.
+ *   out            [rows, q_heads, head_dim] dtype; written when
+ *                  num_splits == 1 (may be NULL otherwise)
+ *   q              [rows, q_heads, head_dim] dtype
+ *   k_pool, v_pool [num_blocks, block_size, kv_heads, head_dim] dtype
+ *   block_tables   [rows, max_blocks_per_row] int32: logical block j of row
+ *                  r is physical block block_tables[r*max_blocks_per_row+j];
+ *                  entries at j >= ceil(context_lens[r]/block_size) are
+ *                  never read
+ *   context_lens   [rows] int32: history length of each row (including any
+ *                  token appended this step); 0 gives an all-zero output
+ *   scale          softmax scale applied to q.k (finite)
+ *   num_splits     >= 1.  1: out is written directly.  > 1: split s of row r
+ *                  (tokens [s*split_len, (s+1)*split_len), see
+ *                  np_paged_decode_split_len) writes its normalised partial
+ *                  output and lse into `workspace`; call
+ *                  np_paged_decode_reduce next to produce out.
+ *   workspace      device buffer of >= np_paged_decode_workspace_bytes(...)
+ *                  bytes (may be NULL when num_splits == 1)
+ *   err_word       device int32 or NULL (NP_FLAG_BLOCK_ID, NP_FLAG_CONTEXT,
+ *                  NP_FLAG_TIMEOUT)
+ * Memory traffic: each history token's K and V rows are read once from HBM;
+ * q, block tables and context lengths once; out (or the partials) written
+ * once.
+ */
+np_status np_paged_decode(void* out, const void* q, const void* k_pool,
+                          const void* v_pool, np_dtype dtype,
+                          int64_t num_blocks, int32_t block_size,
+                          int32_t kv_heads, int32_t head_dim,
+                          const int32_t* block_tables,
+                          int32_t max_blocks_per_row,
+                          const int32_t* context_lens, int32_t rows,
+                          int32_t q_heads, float scale, int32_t num_splits,
+                          void* workspace, size_t workspace_bytes,
+                          int32_t* err_word, np_stream_t stream);
+
+/*
+ * np_paged_decode_reduce -- merge split partials into out.
+ *   out        [rows, q_heads, head_dim] of out_dtype
+ *   workspace  as written by np_paged_decode with the same rows, q_heads,
+ *              head_dim and num_splits
+ * For each (row, head): L = max_s lse_s; out = sum_s e^(lse_s - L) o_s /
+ * sum_s e^(lse_s - L), skipping splits whose lse is -inf; all splits empty
+ * gives zeros.
+ */
+np_status np_paged_decode_reduce(void* out, np_dtype out_dtype,
+                                 const void* workspace, size_t workspace_bytes,
+                                 int32_t rows, int32_t q_heads,
+                                 int32_t head_dim, int32_t num_splits,
+                                 np_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NP_PAGED_H */

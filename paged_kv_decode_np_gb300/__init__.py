@@ -1,0 +1,248 @@
+"""paged_kv_decode_np_gb300 -- GB300 (sm_103a) batched paged-attention decode.
+
+A thin ctypes binding over ``libnp_paged.so`` (C ABI in
+``include/np_paged.h``).  The functions keep the C names and only marshal
+arguments: every step of the append, the read and the reduce runs in the
+library's CUDA kernels.  torch supplies device memory and streams.  There is
+no CPU fallback: if the library is missing, or a tensor is not on a CUDA
+device, the call raises.
+
+Typical decode step::
+
+    import paged_kv_decode_np_gb300 as npg
+    S = npg.np_paged_decode_plan(rows, q_heads, kv_heads, head_dim, block_size,
+                                 max_blocks_per_row, torch.bfloat16)
+    ws = npg.workspace(rows, q_heads, head_dim, S, device="cuda")
+    npg.np_kv_append(k_pool, v_pool, k_new, v_new, slot_mapping)
+    npg.np_paged_decode(out, q, k_pool, v_pool, block_tables, context_lens,
+                        scale, num_splits=S, workspace=ws)
+    if S > 1:
+        npg.np_paged_decode_reduce(out, ws, num_splits=S)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+__all__ = [
+    "load", "NPError", "np_abi_version", "np_status_string", "np_kv_append",
+    "np_paged_decode_plan", "np_paged_decode_split_len",
+    "np_paged_decode_workspace_bytes", "np_paged_decode", "np_paged_decode_reduce",
+    "workspace", "decode_step", "NP_OK", "NP_ERR_INVALID_ARG", "NP_ERR_UNSUPPORTED",
+    "NP_ERR_WORKSPACE", "NP_ERR_OUT_OF_RANGE", "NP_ERR_CUDA", "NP_F32", "NP_BF16",
+    "NP_FLAG_BLOCK_ID", "NP_FLAG_CONTEXT", "NP_FLAG_SLOT", "NP_FLAG_TIMEOUT",
+]
+
+NP_OK = 0
+NP_ERR_INVALID_ARG = 1
+NP_ERR_UNSUPPORTED = 2
+NP_ERR_WORKSPACE = 3
+NP_ERR_OUT_OF_RANGE = 4
+NP_ERR_CUDA = 5
+
+NP_F32 = 0
+NP_BF16 = 1
+
+NP_FLAG_BLOCK_ID = 0x1
+NP_FLAG_CONTEXT = 0x2
+NP_FLAG_SLOT = 0x4
+NP_FLAG_TIMEOUT = 0x8
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libnp_paged.so")
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_LIB: ctypes.CDLL | None = None
+
+
+class NPError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        name = load().np_status_string(status).decode() if _LIB else str(status)
+        super().__init__(f"{call} returned {name}")
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libnp_paged.so (built by ``__graft_entry__.build()``)."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is not built; run `python -c 'import __graft_entry__ as g; "
+                           "g.build()'` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(p)
+    lib.np_status_string.restype = ctypes.c_char_p
+    lib.np_status_string.argtypes = [ctypes.c_int]
+    lib.np_abi_version.restype = _I32
+    lib.np_abi_version.argtypes = []
+    lib.np_kv_append.restype = ctypes.c_int
+    lib.np_kv_append.argtypes = [_P, _P, ctypes.c_int, _I64, _I32, _I32, _I32, _P, _P, _P,
+                                 _I32, _P, _P]
+    lib.np_paged_decode_plan.restype = ctypes.c_int
+    lib.np_paged_decode_plan.argtypes = [_I32, _I32, _I32, _I32, _I32, _I32, ctypes.c_int,
+                                         _I32, ctypes.POINTER(_I32)]
+    lib.np_paged_decode_split_len.restype = _I64
+    lib.np_paged_decode_split_len.argtypes = [_I32, _I32, _I32]
+    lib.np_paged_decode_workspace_bytes.restype = ctypes.c_size_t
+    lib.np_paged_decode_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32]
+    lib.np_paged_decode.restype = ctypes.c_int
+    lib.np_paged_decode.argtypes = [_P, _P, _P, _P, ctypes.c_int, _I64, _I32, _I32, _I32, _P,
+                                    _I32, _P, _I32, _I32, ctypes.c_float, _I32, _P,
+                                    ctypes.c_size_t, _P, _P]
+    lib.np_paged_decode_reduce.restype = ctypes.c_int
+    lib.np_paged_decode_reduce.argtypes = [_P, ctypes.c_int, _P, ctypes.c_size_t, _I32, _I32,
+                                           _I32, _I32, _P]
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def _check(status: int, call: str) -> None:
+    if status != NP_OK:
+        raise NPError(status, call)
+
+
+def _dtype_code(dt) -> int:
+    if dt in (torch.float32, "f32", NP_F32):
+        return NP_F32
+    if dt in (torch.bfloat16, "bf16", NP_BF16):
+        return NP_BF16
+    raise TypeError(f"unsupported dtype {dt}; the library stores float32 or bfloat16")
+
+
+def _dev(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be on a CUDA device (no CPU path exists)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _opt(t: torch.Tensor | None, name: str) -> int | None:
+    return None if t is None else _dev(t, name)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def np_abi_version() -> int:
+    return load().np_abi_version()
+
+
+def np_status_string(status: int) -> str:
+    return load().np_status_string(status).decode()
+
+
+def np_kv_append(k_pool, v_pool, k_new, v_new, slot_mapping, err_word=None, stream=None):
+    """Scatter [T, Hk, D] new K/V rows into the pools at ``slot_mapping`` (int64)."""
+    nb, bs, hk, d = k_pool.shape
+    if v_pool.shape != k_pool.shape or k_new.shape != v_new.shape or \
+            k_new.shape[1:] != (hk, d) or k_new.dtype != k_pool.dtype or \
+            v_new.dtype != k_pool.dtype or v_pool.dtype != k_pool.dtype:
+        raise ValueError("np_kv_append: shape/dtype mismatch")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.shape != (k_new.shape[0],):
+        raise ValueError("np_kv_append: slot_mapping must be int64 [num_tokens]")
+    st = load().np_kv_append(
+        _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), _dtype_code(k_pool.dtype), nb, bs, hk,
+        d, _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(slot_mapping, "slot_mapping"),
+        k_new.shape[0], _opt(err_word, "err_word"), _stream(stream))
+    _check(st, "np_kv_append")
+
+
+def np_paged_decode_plan(rows, q_heads, kv_heads, head_dim, block_size, max_blocks_per_row,
+                         dtype, num_sms: int = 0) -> int:
+    out = _I32(0)
+    st = load().np_paged_decode_plan(rows, q_heads, kv_heads, head_dim, block_size,
+                                     max_blocks_per_row, _dtype_code(dtype), num_sms,
+                                     ctypes.byref(out))
+    _check(st, "np_paged_decode_plan")
+    return out.value
+
+
+def np_paged_decode_split_len(block_size, max_blocks_per_row, num_splits) -> int:
+    return load().np_paged_decode_split_len(block_size, max_blocks_per_row, num_splits)
+
+
+def np_paged_decode_workspace_bytes(rows, q_heads, head_dim, num_splits) -> int:
+    return load().np_paged_decode_workspace_bytes(rows, q_heads, head_dim, num_splits)
+
+
+def workspace(rows, q_heads, head_dim, num_splits, device="cuda") -> torch.Tensor | None:
+    """A torch-allocated workspace of the size the library asks for (None if unsplit)."""
+    n = np_paged_decode_workspace_bytes(rows, q_heads, head_dim, num_splits)
+    if n == 0:
+        return None
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def np_paged_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale,
+                    num_splits: int = 1, workspace=None, err_word=None, stream=None):
+    """The decode read (see np_paged.h).  Writes ``out`` when num_splits == 1."""
+    rows, q_heads, d = q.shape
+    nb, bs, hk, d2 = k_pool.shape
+    if d2 != d or v_pool.shape != k_pool.shape or q.dtype != k_pool.dtype or \
+            v_pool.dtype != k_pool.dtype:
+        raise ValueError("np_paged_decode: q/pool shape or dtype mismatch")
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or \
+            block_tables.shape[0] != rows:
+        raise ValueError("np_paged_decode: block_tables must be int32 [rows, max_blocks]")
+    if context_lens.dtype != torch.int32 or context_lens.shape != (rows,):
+        raise ValueError("np_paged_decode: context_lens must be int32 [rows]")
+    if out is not None and (out.shape != q.shape or out.dtype != q.dtype):
+        raise ValueError("np_paged_decode: out must match q")
+    ws_ptr = _opt(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().np_paged_decode(
+        _opt(out, "out"), _dev(q, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+        _dtype_code(q.dtype), nb, bs, hk, d, _dev(block_tables, "block_tables"),
+        block_tables.shape[1], _dev(context_lens, "context_lens"), rows, q_heads,
+        float(scale), num_splits, ws_ptr, ws_bytes, _opt(err_word, "err_word"),
+        _stream(stream))
+    _check(st, "np_paged_decode")
+
+
+def np_paged_decode_reduce(out, workspace, num_splits: int, stream=None):
+    """Merge split partials in ``workspace`` into ``out`` [rows, q_heads, head_dim]."""
+    rows, q_heads, d = out.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = load().np_paged_decode_reduce(
+        _dev(out, "out"), _dtype_code(out.dtype), _dev(workspace, "workspace"), ws_bytes, rows,
+        q_heads, d, num_splits, _stream(stream))
+    _check(st, "np_paged_decode_reduce")
+
+
+def decode_step(out, q, k_pool, v_pool, block_tables, context_lens, scale, *, k_new=None,
+                v_new=None, slot_mapping=None, num_splits: int = 1, workspace=None,
+                err_word=None, stream=None) -> int:
+    """One decode step: append (if new K/V given), read, reduce (if split).
+
+    Returns the number of library kernels launched.
+    """
+    launches = 0
+    if k_new is not None:
+        np_kv_append(k_pool, v_pool, k_new, v_new, slot_mapping, err_word, stream)
+        launches += 1 if k_new.shape[0] > 0 else 0
+    np_paged_decode(out if num_splits == 1 else None, q, k_pool, v_pool, block_tables,
+                    context_lens, scale, num_splits, workspace, err_word, stream)
+    launches += 1 if q.shape[0] > 0 else 0
+    if num_splits > 1:
+        np_paged_decode_reduce(out, workspace, num_splits, stream)
+        launches += 1 if q.shape[0] > 0 else 0
+    return launches
+
+
+def default_scale(head_dim: int) -> float:
+    return 1.0 / math.sqrt(head_dim)

@@ -1,0 +1,292 @@
+// api.cu -- the C ABI of libnp_paged.so (declared in include/np_paged.h):
+// argument validation, split planning from static shapes, and launches.
+// Nothing here allocates, synchronises or reads device memory.
+#include <limits.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "decode_kernel.cuh"
+#include "decode_launch.h"
+#include "np_paged.h"
+
+#ifndef NPK_SMEM_BUDGET
+#define NPK_SMEM_BUDGET 0  // 0: the device's opt-in maximum per block
+#endif
+
+namespace {
+
+using npk::DecodeLaunch;
+using npk::DecodeParams;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int elem_size(np_dtype d) { return d == NP_F32 ? 4 : (d == NP_BF16 ? 2 : 0); }
+
+bool head_dim_supported(int32_t d) {
+  return d == 16 || d == 32 || d == 64 || d == 128 || d == 256;
+}
+
+bool group_supported(int32_t g) { return g == 1 || g == 2 || g == 4 || g == 5 || g == 8; }
+
+// a*b*... without int64 overflow; false on overflow or negative input
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+  if (a < 0 || b < 0) return false;
+  if (a != 0 && b > INT64_MAX / a) return false;
+  *out = a * b;
+  return true;
+}
+
+// kv heads per CTA: the largest divisor of kv_heads that is <= 8
+int head_group_of(int32_t kv_heads) {
+  for (int hg = 8; hg >= 1; --hg)
+    if (kv_heads % hg == 0) return hg;
+  return 1;
+}
+
+struct DeviceInfo {
+  std::atomic<int> sms{0};
+  std::atomic<int> smem_optin{0};
+};
+DeviceInfo g_dev[64];
+
+np_status device_info(int* sms, int* smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NP_ERR_CUDA;
+  DeviceInfo* di = dev < 64 ? &g_dev[dev] : nullptr;
+  int s = di ? di->sms.load() : 0, m = di ? di->smem_optin.load() : 0;
+  if (s == 0 || m == 0) {
+    if (cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&m, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return NP_ERR_CUDA;
+    if (di) {
+      di->sms.store(s);
+      di->smem_optin.store(m);
+    }
+  }
+  *sms = s;
+  *smem = m;
+  return NP_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+npk::DecodeLauncher launcher_for(np_dtype dt, int32_t d) {
+  if (dt == NP_F32) {
+    switch (d) {
+      case 16: return npk::decode_f32_d16;
+      case 32: return npk::decode_f32_d32;
+      case 64: return npk::decode_f32_d64;
+      case 128: return npk::decode_f32_d128;
+      case 256: return npk::decode_f32_d256;
+    }
+  } else if (dt == NP_BF16) {
+    switch (d) {
+      case 16: return npk::decode_bf16_d16;
+      case 32: return npk::decode_bf16_d32;
+      case 64: return npk::decode_bf16_d64;
+      case 128: return npk::decode_bf16_d128;
+      case 256: return npk::decode_bf16_d256;
+    }
+  }
+  return nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* np_status_string(np_status s) {
+  switch (s) {
+    case NP_OK: return "NP_OK";
+    case NP_ERR_INVALID_ARG: return "NP_ERR_INVALID_ARG";
+    case NP_ERR_UNSUPPORTED: return "NP_ERR_UNSUPPORTED";
+    case NP_ERR_WORKSPACE: return "NP_ERR_WORKSPACE";
+    case NP_ERR_OUT_OF_RANGE: return "NP_ERR_OUT_OF_RANGE";
+    case NP_ERR_CUDA: return "NP_ERR_CUDA";
+  }
+  return "NP_ERR_UNKNOWN";
+}
+
+int32_t np_abi_version(void) { return NP_ABI_VERSION; }
+
+np_status np_kv_append(void* k_pool, void* v_pool, np_dtype dtype, int64_t num_blocks,
+                       int32_t block_size, int32_t kv_heads, int32_t head_dim,
+                       const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                       int32_t num_tokens, int32_t* err_word, np_stream_t stream) {
+  const int es = elem_size(dtype);
+  if (es == 0) return NP_ERR_UNSUPPORTED;
+  if (num_blocks <= 0 || block_size <= 0 || kv_heads <= 0 || head_dim <= 0 || num_tokens < 0)
+    return NP_ERR_INVALID_ARG;
+  int64_t row_bytes = 0, slots = 0, pool_bytes = 0;
+  if (!mul_ok((int64_t)kv_heads * es, head_dim, &row_bytes) ||
+      !mul_ok(num_blocks, block_size, &slots) || !mul_ok(slots, row_bytes, &pool_bytes))
+    return NP_ERR_OUT_OF_RANGE;
+  if (row_bytes % 16 != 0) return NP_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return NP_OK;
+  if (!k_pool || !v_pool || !k_new || !v_new || !slot_mapping) return NP_ERR_INVALID_ARG;
+  if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(k_new, 16) ||
+      !aligned(v_new, 16) || !aligned(slot_mapping, 8) || (err_word && !aligned(err_word, 4)))
+    return NP_ERR_INVALID_ARG;
+  return npk::launch_append(k_pool, v_pool, slots, row_bytes, k_new, v_new, slot_mapping,
+                            num_tokens, err_word, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int64_t np_paged_decode_split_len(int32_t block_size, int32_t max_blocks_per_row,
+                                  int32_t num_splits) {
+  if (block_size <= 0 || max_blocks_per_row <= 0 || num_splits <= 0) return -1;
+  const int64_t cap = (int64_t)max_blocks_per_row * block_size;
+  const int64_t align = block_size > 64 ? block_size : 64;
+  int64_t sl = (cap + num_splits - 1) / num_splits;
+  sl = (sl + align - 1) / align * align;
+  return sl;
+}
+
+np_status np_paged_decode_plan(int32_t rows, int32_t q_heads, int32_t kv_heads,
+                               int32_t head_dim, int32_t block_size,
+                               int32_t max_blocks_per_row, np_dtype dtype, int32_t num_sms,
+                               int32_t* num_splits) {
+  const int es = elem_size(dtype);
+  if (!num_splits) return NP_ERR_INVALID_ARG;
+  if (es == 0) return NP_ERR_UNSUPPORTED;
+  if (rows < 0 || q_heads <= 0 || kv_heads <= 0 || q_heads % kv_heads != 0 || head_dim <= 0 ||
+      block_size <= 0 || max_blocks_per_row <= 0)
+    return NP_ERR_INVALID_ARG;
+  if (num_sms <= 0) {
+    int smem = 0;
+    np_status st = device_info(&num_sms, &smem);
+    if (st != NP_OK) return st;
+  }
+  const int g = q_heads / kv_heads;
+  const int hg = head_group_of(kv_heads);
+  const int64_t units = (int64_t)rows * (kv_heads / hg);
+  const int64_t cap = (int64_t)max_blocks_per_row * block_size;
+  // Tokens per split: about 2 MB of K+V per CTA, and at least 128x the
+  // partial result it writes (so partials + reduce stay ~1% of the traffic).
+  const int64_t tok_bytes = 2ll * hg * head_dim * es;
+  int64_t sl = (2ll << 20) / tok_bytes;
+  const int64_t sl_partial = 256ll * g / es;
+  if (sl < sl_partial) sl = sl_partial;
+  sl = (sl + 63) / 64 * 64;
+  int64_t s = (cap + sl - 1) / sl;
+  // Few, short rows: split finer so at least ~2 CTAs per SM exist.
+  while (units * s < 2ll * num_sms && sl > 64) {
+    sl = (sl / 2 + 63) / 64 * 64;
+    s = (cap + sl - 1) / sl;
+  }
+  if (s < 1) s = 1;
+  if (s > 65535) s = 65535;
+  *num_splits = (int32_t)s;
+  return NP_OK;
+}
+
+size_t np_paged_decode_workspace_bytes(int32_t rows, int32_t q_heads, int32_t head_dim,
+                                       int32_t num_splits) {
+  if (num_splits <= 1 || rows <= 0 || q_heads <= 0 || head_dim <= 0) return 0;
+  const size_t units = (size_t)rows * q_heads * num_splits;
+  return round_up(units * head_dim * sizeof(float), 256) + round_up(units * sizeof(float), 256);
+}
+
+np_status np_paged_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                          np_dtype dtype, int64_t num_blocks, int32_t block_size,
+                          int32_t kv_heads, int32_t head_dim, const int32_t* block_tables,
+                          int32_t max_blocks_per_row, const int32_t* context_lens, int32_t rows,
+                          int32_t q_heads, float scale, int32_t num_splits, void* workspace,
+                          size_t workspace_bytes, int32_t* err_word, np_stream_t stream) {
+  const int es = elem_size(dtype);
+  if (es == 0) return NP_ERR_UNSUPPORTED;
+  if (rows < 0 || q_heads <= 0 || kv_heads <= 0 || q_heads % kv_heads != 0 ||
+      num_blocks <= 0 || block_size <= 0 || max_blocks_per_row <= 0 || num_splits <= 0 ||
+      num_splits > 65535 || !isfinite(scale))
+    return NP_ERR_INVALID_ARG;
+  if (!head_dim_supported(head_dim) || !group_supported(q_heads / kv_heads))
+    return NP_ERR_UNSUPPORTED;
+  int64_t slots = 0, pool_elems = 0, pool_bytes = 0, tab = 0;
+  if (!mul_ok(num_blocks, block_size, &slots) ||
+      !mul_ok(slots, (int64_t)kv_heads * head_dim, &pool_elems) ||
+      !mul_ok(pool_elems, es, &pool_bytes) || !mul_ok(rows, max_blocks_per_row, &tab) ||
+      !mul_ok(max_blocks_per_row, block_size, &tab))
+    return NP_ERR_OUT_OF_RANGE;
+  if (rows > 65535) return NP_ERR_UNSUPPORTED;  // grid.y
+  if (rows == 0) return NP_OK;
+  if (!q || !k_pool || !v_pool || !block_tables || !context_lens) return NP_ERR_INVALID_ARG;
+  if (num_splits == 1 && !out) return NP_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+      (out && !aligned(out, 16)) || !aligned(block_tables, 4) || !aligned(context_lens, 4) ||
+      (err_word && !aligned(err_word, 4)))
+    return NP_ERR_INVALID_ARG;
+  float* ws_o = nullptr;
+  float* ws_lse = nullptr;
+  if (num_splits > 1) {
+    const size_t need = np_paged_decode_workspace_bytes(rows, q_heads, head_dim, num_splits);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return NP_ERR_WORKSPACE;
+    ws_o = static_cast<float*>(workspace);
+    ws_lse = reinterpret_cast<float*>(
+        static_cast<char*>(workspace) +
+        round_up((size_t)rows * q_heads * num_splits * head_dim * sizeof(float), 256));
+  }
+  int sms = 0, smem_optin = 0;
+  np_status st = device_info(&sms, &smem_optin);
+  if (st != NP_OK) return st;
+
+  const int hg = head_group_of(kv_heads);
+  DecodeParams p{};
+  p.out = out;
+  p.ws_o = ws_o;
+  p.ws_lse = ws_lse;
+  p.q = q;
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.err = err_word;
+  p.num_blocks = num_blocks;
+  p.split_len = np_paged_decode_split_len(block_size, max_blocks_per_row, num_splits);
+  p.block_size = block_size;
+  p.kv_heads = kv_heads;
+  p.head_group = hg;
+  p.token_warps = npk::kMaxConsumerWarps / hg;
+  p.max_blocks_per_row = max_blocks_per_row;
+  p.q_heads = q_heads;
+  p.num_splits = num_splits;
+  p.stages = 0;
+  p.qscale = scale * 1.4426950408889634f;  // log2(e)
+
+  DecodeLaunch L{};
+  L.params = &p;
+  L.group = q_heads / kv_heads;
+  L.head_group = hg;
+  L.token_warps = p.token_warps;
+  L.rows = rows;
+  L.splits = num_splits;
+  L.head_groups = kv_heads / hg;
+  L.smem_budget = NPK_SMEM_BUDGET > 0 && NPK_SMEM_BUDGET < smem_optin ? NPK_SMEM_BUDGET
+                                                                      : (size_t)smem_optin;
+  L.stream = reinterpret_cast<cudaStream_t>(stream);
+  npk::DecodeLauncher fn = launcher_for(dtype, head_dim);
+  if (!fn) return NP_ERR_UNSUPPORTED;
+  return fn(L, p);
+}
+
+np_status np_paged_decode_reduce(void* out, np_dtype out_dtype, const void* workspace,
+                                 size_t workspace_bytes, int32_t rows, int32_t q_heads,
+                                 int32_t head_dim, int32_t num_splits, np_stream_t stream) {
+  if (elem_size(out_dtype) == 0) return NP_ERR_UNSUPPORTED;
+  if (rows < 0 || q_heads <= 0 || num_splits <= 0 || num_splits > 65535)
+    return NP_ERR_INVALID_ARG;
+  if (!head_dim_supported(head_dim)) return NP_ERR_UNSUPPORTED;
+  if (rows == 0) return NP_OK;
+  if (!out || !aligned(out, 16)) return NP_ERR_INVALID_ARG;
+  if (num_splits == 1) return NP_ERR_INVALID_ARG;  // nothing to merge: decode wrote out
+  const size_t need = np_paged_decode_workspace_bytes(rows, q_heads, head_dim, num_splits);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return NP_ERR_WORKSPACE;
+  const float* ws_o = static_cast<const float*>(workspace);
+  const float* ws_lse = reinterpret_cast<const float*>(
+      static_cast<const char*>(workspace) +
+      round_up((size_t)rows * q_heads * num_splits * head_dim * sizeof(float), 256));
+  return npk::launch_reduce(out, out_dtype, ws_o, ws_lse, rows, q_heads, head_dim, num_splits,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// decode_inst.cu -- instantiates the decode kernel for one storage type and
+// head_dim (chosen at compile time: -DNPK_BF16=0/1 -DNPK_D=<head_dim>) and
+// for every supported GQA group, behind one launcher function.
+#include "decode_kernel.cuh"
+#include "decode_launch.h"
+
+#ifndef NPK_BF16
+#error "define NPK_BF16"
+#endif
+#ifndef NPK_D
+#error "define NPK_D"
+#endif
+
+#if NPK_BF16
+using StorageT = __nv_bfloat16;
+#define NPK_TNAME bf16
+#else
+using StorageT = float;
+#define NPK_TNAME f32
+#endif
+
+#define NPK_CAT3(a, b, c) a##b##c
+#define NPK_NAME3(a, b, c) NPK_CAT3(a, b, c)
+#define NPK_LAUNCHER NPK_NAME3(decode_, NPK_TNAME, NPK_NAME3(_d, NPK_D, ))
+
+namespace npk {
+namespace {
+
+template <int G>
+np_status launch_one(DecodeLaunch& L, DecodeParams& p) {
+  using SM = DecodeSmem<StorageT, NPK_D, G>;
+  const int warps = L.head_group * L.token_warps;
+  const size_t fixed = SM::ptile_bytes(warps) + 16 + 128;
+  const size_t sb = SM::stage_bytes(L.head_group);
+  if (L.smem_budget <= fixed) return NP_ERR_UNSUPPORTED;
+  size_t stages = (L.smem_budget - fixed) / (sb + 16);
+  if (stages > 8) stages = 8;
+  if (stages < 2) return NP_ERR_UNSUPPORTED;
+  while (stages > 2 && SM::total(L.head_group, (int)stages, warps) > L.smem_budget) --stages;
+  const size_t smem = SM::total(L.head_group, (int)stages, warps);
+  if (smem > L.smem_budget) return NP_ERR_UNSUPPORTED;
+  p.stages = (int)stages;
+  L.stages = (int)stages;
+  L.smem_bytes = smem;
+
+  auto kern = paged_decode_kernel<StorageT, NPK_D, G>;
+  // The opt-in shared-memory limit is a per-device function attribute.
+  static unsigned long long configured = 0;  // bit d: done on device d
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NP_ERR_CUDA;
+  if (dev < 64 && !((__atomic_load_n(&configured, __ATOMIC_ACQUIRE) >> dev) & 1ull)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)L.smem_budget) != cudaSuccess)
+      return NP_ERR_CUDA;
+    __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
+  } else if (dev >= 64) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)L.smem_budget) != cudaSuccess)
+      return NP_ERR_CUDA;
+  }
+  dim3 grid(L.splits, L.rows, L.head_groups);
+  kern<<<grid, 32 * (warps + 1), smem, L.stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? NP_OK : NP_ERR_CUDA;
+}
+
+}  // namespace
+
+np_status NPK_LAUNCHER(DecodeLaunch& L, DecodeParams& p) {
+  switch (L.group) {
+    case 1: return launch_one<1>(L, p);
+    case 2: return launch_one<2>(L, p);
+    case 4: return launch_one<4>(L, p);
+    case 5: return launch_one<5>(L, p);
+    case 8: return launch_one<8>(L, p);
+    default: return NP_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace npk

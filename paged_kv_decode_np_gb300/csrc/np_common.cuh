@@ -1,0 +1,203 @@
+// np_common.cuh -- device helpers shared by the kernels of libnp_paged.so:
+// mbarrier and bulk-copy (TMA) inline PTX, bounded waits, storage-type
+// widening, error flags.  sm_103a only.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "np_paged.h"
+
+namespace npk {
+
+// ---------------------------------------------------------------- errors --
+__device__ __forceinline__ void set_flag(int32_t* err, int32_t bit) {
+  if (err != nullptr) atomicOr(err, bit);
+}
+
+// ----------------------------------------------------------------- time ---
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// A pipeline wait gives up after this long (nothing legitimate takes more
+// than microseconds; this bounds a wait that could otherwise never end).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+// ------------------------------------------------------------- mbarrier ---
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count)
+               : "memory");
+}
+
+// Makes barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Waits until the phase with the given parity has completed.  Bounded: gives
+// up (returns false) when *abort becomes non-zero or after kWaitLimitNs, in
+// which case it sets *abort itself so every other waiter in the block stops.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------- bulk copy (TMA) ----
+// L2 policy for streamed K/V: read once, evict first.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing `bytes`
+// transactions on `bar`.  src, dst 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                        uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// ----------------------------------------------------------- arithmetic ---
+// 2^x (PTX ex2.approx, flush-to-zero); ex2(-inf) = +0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------- storage types ----
+// Widening of 16-byte / 8-byte vectors of the storage type to fp32.
+// bf16 is the top half of an fp32, so widening is a shift or a mask.
+template <typename T>
+struct Storage;
+
+template <>
+struct Storage<float> {
+  static constexpr int kBytes = 4;
+  static constexpr np_dtype kDtype = NP_F32;
+  // n elements (4 or 2) from a 16- or 8-byte aligned address
+  template <int N>
+  __device__ __forceinline__ static void load(const float* p, float* x) {
+    if constexpr (N == 4) {
+      float4 v = *reinterpret_cast<const float4*>(p);
+      x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    } else if constexpr (N == 2) {
+      float2 v = *reinterpret_cast<const float2*>(p);
+      x[0] = v.x; x[1] = v.y;
+    } else {
+      static_assert(N == 1, "vector width");
+      x[0] = *p;
+    }
+  }
+  template <int N>
+  __device__ __forceinline__ static void store(float* p, const float* x) {
+    if constexpr (N == 4) {
+      *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    } else if constexpr (N == 2) {
+      *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
+    } else {
+      static_assert(N == 1, "vector width");
+      *p = x[0];
+    }
+  }
+};
+
+__device__ __forceinline__ void widen_bf16x2(uint32_t w, float& lo, float& hi) {
+  lo = __uint_as_float(w << 16);
+  hi = __uint_as_float(w & 0xffff0000u);
+}
+
+template <>
+struct Storage<__nv_bfloat16> {
+  static constexpr int kBytes = 2;
+  static constexpr np_dtype kDtype = NP_BF16;
+  template <int N>
+  __device__ __forceinline__ static void load(const __nv_bfloat16* p, float* x) {
+    if constexpr (N == 8) {
+      uint4 v = *reinterpret_cast<const uint4*>(p);
+      widen_bf16x2(v.x, x[0], x[1]);
+      widen_bf16x2(v.y, x[2], x[3]);
+      widen_bf16x2(v.z, x[4], x[5]);
+      widen_bf16x2(v.w, x[6], x[7]);
+    } else if constexpr (N == 4) {
+      uint2 v = *reinterpret_cast<const uint2*>(p);
+      widen_bf16x2(v.x, x[0], x[1]);
+      widen_bf16x2(v.y, x[2], x[3]);
+    } else if constexpr (N == 2) {
+      uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+      widen_bf16x2(v, x[0], x[1]);
+    } else {
+      static_assert(N == 1, "vector width");
+      x[0] = __bfloat162float(*p);
+    }
+  }
+  // fp32 -> bf16 round-to-nearest-even
+  template <int N>
+  __device__ __forceinline__ static void store(__nv_bfloat16* p, const float* x) {
+    if constexpr (N >= 2) {
+      static_assert(N % 2 == 0 && N <= 8, "vector width");
+      uint32_t w[N / 2];
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t*>(&h);
+      }
+      if constexpr (N == 8) {
+        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+      } else if constexpr (N == 4) {
+        *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+      } else {
+        *reinterpret_cast<uint32_t*>(p) = w[0];
+      }
+    } else {
+      *p = __float2bfloat16_rn(x[0]);
+    }
+  }
+};
+
+}  // namespace npk

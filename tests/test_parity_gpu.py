@@ -1,0 +1,360 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Every test here drives libnp_paged.so through the Python binding and
+compares element by element with the oracle on the same seeded bytes:
+fp32 within atol 1e-5 + rtol 1e-4, bf16 within atol 2e-2, appends bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import golden_cases
+import oracle
+import workloads as wl
+from step_helpers import assert_parity, gpu_step, oracle_step, to64
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _custom(contexts, q_heads, kv_heads, head_dim, block_size, dtype, seed=11, spare=3,
+            scale=None):
+    return wl.Workload(f"custom-{seed}", rows=len(contexts), q_heads=q_heads,
+                       kv_heads=kv_heads, head_dim=head_dim, block_size=block_size,
+                       dtype=dtype, ctx=("fixed", tuple(contexts)), pool=("spare", spare),
+                       seed=seed, scale=scale)
+
+
+def _full_parity(npg, w, num_splits=None, append=True, device=DEV):
+    inp = wl.make_inputs(w, device="cpu")
+    host = wl.full_host(inp)
+    dinp = wl.Inputs(w, inp.md, *(t.to(device) for t in
+                                  (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new)))
+    out, s, _ = gpu_step(npg, dinp, num_splits=num_splits, append=append)
+    ref, _ = oracle_step(host, w.softmax_scale, append=append)
+    return assert_parity(out, ref, w.dtype, f"{w.name} splits={s}"), s
+
+
+# ------------------------------------------------------------------ golden --
+def _pad_dim(a, d_new):
+    pad = [(0, 0)] * (a.ndim - 1) + [(0, d_new - a.shape[-1])]
+    return np.pad(a, pad)
+
+
+def test_golden_read_three_tokens(nplib):
+    g = golden_cases.load("read_three_tokens_gqa.json")
+    D = 16  # smallest compiled head_dim; zero padding leaves scores unchanged
+    q = torch.from_numpy(_pad_dim(g["q"], D)).to(DEV)
+    kp = torch.from_numpy(_pad_dim(g["k_pool"], D).astype(np.float32)).to(DEV)
+    vp = torch.from_numpy(_pad_dim(g["v_pool"], D).astype(np.float32)).to(DEV)
+    for s in (1, 2):
+        out = torch.empty_like(q)
+        ws = nplib.workspace(1, 2, D, s)
+        bt = torch.from_numpy(g["block_tables"]).to(DEV)
+        cl = torch.from_numpy(g["context_lens"]).to(DEV)
+        nplib.decode_step(out, q, kp, vp, bt, cl, g["scale"], num_splits=s, workspace=ws)
+        torch.cuda.synchronize()
+        o = to64(out)
+        np.testing.assert_allclose(o[..., :2], g["expected_out"], rtol=0, atol=g["atol"])
+        assert np.all(o[..., 2:] == 0)
+
+
+def test_golden_append_then_read(nplib):
+    g = golden_cases.load("append_then_read.json")
+    D = 16
+    kp = torch.from_numpy(_pad_dim(g["k_pool"], D).astype(np.float32)).to(DEV)
+    vp = torch.from_numpy(_pad_dim(g["v_pool"], D).astype(np.float32)).to(DEV)
+    kn = torch.from_numpy(_pad_dim(g["k_new"], D).astype(np.float32)).to(DEV)
+    vn = torch.from_numpy(_pad_dim(g["v_new"], D).astype(np.float32)).to(DEV)
+    sm = torch.from_numpy(g["slot_mapping"]).to(DEV)
+    q = torch.from_numpy(_pad_dim(g["q"], D)).to(DEV)
+    out = torch.empty_like(q)
+    nplib.decode_step(out, q, kp, vp, torch.from_numpy(g["block_tables"]).to(DEV),
+                      torch.from_numpy(g["context_lens"]).to(DEV), g["scale"], k_new=kn[:1],
+                      v_new=vn[:1], slot_mapping=sm[:1])
+    nplib.np_kv_append(kp, vp, kn[1:], vn[1:], sm[1:])  # the padding token: skipped
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to64(kp)[..., :1], g["expected_k_pool"])
+    np.testing.assert_array_equal(to64(vp)[..., :1], g["expected_v_pool"])
+    np.testing.assert_allclose(to64(out)[..., :1], g["expected_out"], rtol=0, atol=g["atol"])
+
+
+# --------------------------------------------------------- the workloads ---
+@pytest.mark.parametrize("name", ["tiny-fp32", "llama-fp32"])
+def test_workload_full_parity(nplib, name):
+    w = wl.WORKLOADS[name]
+    _full_parity(nplib, w)
+    _full_parity(nplib, w, num_splits=1)
+
+
+@pytest.mark.parametrize("name,sample", [
+    ("bf16-gqa4", 8), ("bf16-long", 3), ("bf16-ragged-bs8", 12), ("bf16-ragged-bs32", 12)])
+def test_workload_full_size_sampled_rows(nplib, name, sample):
+    """Full-size pools drawn on the GPU, the launch the bench times, rows sampled.
+
+    The sampled rows always include the longest and the shortest context.
+    """
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w, device=DEV)
+    cl = inp.context_lens
+    g = torch.Generator().manual_seed(99)
+    rows = {int(cl.argmax()), int(cl.argmin())}
+    for r in torch.randperm(w.rows, generator=g).tolist():
+        if len(rows) >= sample:
+            break
+        rows.add(r)
+    rows = sorted(rows)
+    host = wl.row_subproblem(inp, rows)          # copied before any kernel runs
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, s, _ = gpu_step(nplib, inp, err=err)
+    assert int(err.item()) == 0
+    ref, _ = oracle_step(host, w.softmax_scale)
+    assert_parity(out[rows], ref, w.dtype, f"{name} rows={rows} splits={s}")
+    assert torch.isfinite(out.float()).all()
+
+
+# ------------------------------------------------------------ split-K ----
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 16, 32])
+def test_split_counts_fp32(nplib, splits):
+    _full_parity(nplib, wl.WORKLOADS["llama-fp32"], num_splits=splits)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 40])
+def test_split_counts_bf16(nplib, splits):
+    w = _custom([1, 63, 64, 65, 700, 2500, 333], 40, 8, 128, 16, "bf16", seed=5)
+    _full_parity(nplib, w, num_splits=splits)
+
+
+def test_partials_match_oracle_splits(nplib):
+    """The workspace holds, per split, the normalised output and natural-log lse."""
+    w = _custom([5, 64, 130, 640, 1000], 16, 4, 64, 16, "f32", seed=6)
+    inp = wl.make_inputs(w)
+    host = wl.full_host(inp)
+    d = wl.Inputs(w, inp.md, *(t.to(DEV) for t in
+                               (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new)))
+    S = 9
+    out, _, ws = gpu_step(nplib, d, num_splits=S)
+    sl = nplib.np_paged_decode_split_len(w.block_size, w.max_blocks_per_row, S)
+    n_o = w.rows * w.q_heads * S * w.head_dim
+    wsf = ws.view(torch.float32)
+    o = wsf[:n_o].view(w.rows, w.q_heads, S, w.head_dim)
+    off = (n_o * 4 + 255) // 256 * 256 // 4
+    lse = wsf[off:off + w.rows * w.q_heads * S].view(w.rows, w.q_heads, S)
+    ro, rl = oracle_step(host, w.softmax_scale, split_len=sl, num_splits=S)
+    lse_g = to64(lse)
+    assert np.array_equal(np.isinf(lse_g), np.isinf(rl))
+    fin = np.isfinite(rl)
+    np.testing.assert_allclose(lse_g[fin], rl[fin], rtol=1e-5, atol=1e-5)
+    og = to64(o)
+    assert_parity(og[fin], ro[fin], "f32", "partials")
+    full, _ = oracle_step(host, w.softmax_scale)
+    assert_parity(out, full, "f32", "reduced")
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_reduce_alone(nplib, out_dtype):
+    R, H, S, D = 5, 6, 7, 128
+    g = torch.Generator().manual_seed(3)
+    o = torch.randn(R, H, S, D, generator=g, dtype=torch.float32)
+    lse = torch.randn(R, H, S, generator=g, dtype=torch.float32) * 4
+    lse[0, :, 3] = -float("inf")
+    o[0, :, 3] = float("nan")            # an empty split's o is never read
+    lse[1, 2, :] = -float("inf")         # every split empty -> zeros
+    o[1, 2, :] = float("nan")
+    ws = nplib.workspace(R, H, D, S)
+    wsf = ws.view(torch.float32)
+    n_o = R * H * S * D
+    wsf[:n_o] = o.reshape(-1).to(DEV)
+    off = (n_o * 4 + 255) // 256 * 256 // 4
+    wsf[off:off + R * H * S] = lse.reshape(-1).to(DEV)
+    out = torch.empty(R, H, D, dtype=out_dtype, device=DEV)
+    nplib.np_paged_decode_reduce(out, ws, S)
+    torch.cuda.synchronize()
+    ref = oracle.reduce(o.double().numpy(), lse.double().numpy())
+    assert np.all(to64(out)[1, 2] == 0)
+    if out_dtype == torch.float32:
+        assert_parity(out, ref, "f32", "reduce")
+    else:
+        assert_parity(out, ref, "bf16", "reduce")
+
+
+# --------------------------------------------------------------- append ---
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_append_bit_exact(nplib, dtype):
+    w = _custom([3, 17, 40, 1, 0, 9], 8, 4, 128, 8, dtype, seed=8)
+    inp = wl.make_inputs(w, poison=False)
+    host = wl.full_host(inp)
+    kp, vp = inp.k_pool.to(DEV), inp.v_pool.to(DEV)
+    sm = inp.slot_mapping.clone()
+    sm[1] = -1                                   # padding token
+    nslots = inp.md.num_blocks * w.block_size
+    sm[3] = nslots                               # past the pool: skipped, flagged
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    nplib.np_kv_append(kp, vp, inp.k_new.to(DEV), inp.v_new.to(DEV), sm.to(DEV), err)
+    torch.cuda.synchronize()
+    rk, rv = host["k_pool"].copy(), host["v_pool"].copy()
+    rc = oracle.kv_append(rk, rv, host["k_new"], host["v_new"], sm.numpy())
+    assert rc == oracle.BAD_BLOCK
+    assert int(err.item()) == nplib.NP_FLAG_SLOT
+    assert wl.host_array(kp).tobytes() == rk.tobytes()
+    assert wl.host_array(vp).tobytes() == rv.tobytes()
+
+
+def test_append_many_tokens_bit_exact(nplib):
+    g = torch.Generator().manual_seed(4)
+    nb, bs, hk, d, T = 64, 16, 8, 128, 300
+    kp = torch.randn(nb, bs, hk, d, generator=g).to(torch.bfloat16)
+    vp = torch.randn(nb, bs, hk, d, generator=g).to(torch.bfloat16)
+    kn = torch.randn(T, hk, d, generator=g).to(torch.bfloat16)
+    vn = torch.randn(T, hk, d, generator=g).to(torch.bfloat16)
+    sm = torch.randperm(nb * bs, generator=g)[:T].to(torch.int64)
+    dk, dv = kp.to(DEV), vp.to(DEV)
+    nplib.np_kv_append(dk, dv, kn.to(DEV), vn.to(DEV), sm.to(DEV))
+    torch.cuda.synchronize()
+    rk, rv = wl.host_array(kp), wl.host_array(vp)
+    oracle.kv_append(rk, rv, wl.host_array(kn), wl.host_array(vn), sm.numpy())
+    assert wl.host_array(dk).tobytes() == rk.tobytes()
+    assert wl.host_array(dv).tobytes() == rv.tobytes()
+
+
+# ------------------------------------------------- every compiled variant --
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("head_dim", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("group", [1, 2, 4, 5, 8])
+def test_every_head_dim_and_group(nplib, dtype, head_dim, group):
+    w = _custom([1, 37, 200, 16], 2 * group, 2, head_dim, 16, dtype, seed=head_dim + group)
+    _full_parity(nplib, w)
+    _full_parity(nplib, w, num_splits=3)
+
+
+@pytest.mark.parametrize("kv_heads", [1, 3, 5, 12, 16])
+def test_kv_head_grouping(nplib, kv_heads):
+    """kv_heads not a multiple of 8 and > 8 (several head groups per row)."""
+    w = _custom([50, 129, 7], 2 * kv_heads, kv_heads, 64, 16, "bf16", seed=20 + kv_heads)
+    _full_parity(nplib, w)
+    _full_parity(nplib, w, num_splits=4)
+
+
+@pytest.mark.parametrize("block_size", [1, 3, 8, 16, 24, 32, 64, 128])
+def test_block_sizes(nplib, block_size):
+    w = _custom([1, 31, 32, 33, 255, 513], 8, 2, 128, block_size, "f32", seed=30 + block_size)
+    _full_parity(nplib, w)
+    _full_parity(nplib, w, num_splits=5)
+
+
+def test_edge_contexts(nplib):
+    """Empty rows, one token, exact chunk and split boundaries, full tables."""
+    ctx = [0, 1, 2, 15, 16, 17, 63, 64, 65, 127, 128, 129, 512]
+    w = _custom(ctx, 8, 8, 128, 16, "bf16", seed=40)
+    for s in (1, 2, 8, 32):
+        _full_parity(nplib, w, num_splits=s)
+    w = _custom(ctx, 4, 2, 128, 16, "f32", seed=41)
+    for s in (1, 3, 9):
+        _full_parity(nplib, w, num_splits=s)
+
+
+def test_zero_context_gives_zeros_and_single_token_gives_v(nplib):
+    w = _custom([0, 1, 1], 8, 2, 128, 16, "f32", seed=42)
+    inp = wl.make_inputs(w)
+    d = wl.Inputs(w, inp.md, *(t.to(DEV) for t in
+                               (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new)))
+    for s in (1, 2):
+        out, _, _ = gpu_step(nplib, d, num_splits=s)
+        o = to64(out)
+        assert np.all(o[0] == 0)
+        vnew = to64(inp.v_new)                       # the only token is the new one
+        np.testing.assert_array_equal(o[1], np.repeat(vnew[1], 4, axis=0))
+
+
+# ---------------------------------------------------------- robustness ----
+def test_bad_block_id_is_flagged_not_faulted(nplib):
+    w = _custom([40, 40], 8, 2, 128, 16, "f32", seed=50)
+    inp = wl.make_inputs(w, poison=False)
+    host = wl.full_host(inp)
+    bt = inp.block_tables.clone()
+    bt[0, 1] = inp.md.num_blocks + 1000                 # outside the pool
+    d = wl.Inputs(w, wl.Metadata(inp.context_lens, bt, inp.slot_mapping, inp.md.num_blocks),
+                  *(t.to(DEV) for t in (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new)))
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, _, _ = gpu_step(nplib, d, num_splits=1, err=err)
+    assert int(err.item()) & nplib.NP_FLAG_BLOCK_ID
+    ref, _ = oracle_step(host, w.softmax_scale)
+    assert_parity(out[1:], ref[1:], "f32", "the untouched row")
+
+
+def test_context_past_table_is_clamped_and_flagged(nplib):
+    w = _custom([40, 64], 8, 2, 128, 16, "f32", seed=51)
+    inp = wl.make_inputs(w)
+    host = wl.full_host(inp)
+    cl = inp.context_lens.clone()
+    cl[0] = 10_000                                      # table holds 64
+    dmd = wl.Metadata(cl, inp.block_tables, inp.slot_mapping, inp.md.num_blocks)
+    d = wl.Inputs(w, dmd, *(t.to(DEV) for t in
+                            (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new)))
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, _, _ = gpu_step(nplib, d, num_splits=1, err=err)
+    assert int(err.item()) & nplib.NP_FLAG_CONTEXT
+    ref, _ = oracle_step(host, w.softmax_scale)
+    assert_parity(out[1:], ref[1:], "f32", "the untouched row")
+
+
+def test_validation_errors_return_before_launch(nplib):
+    w = _custom([10], 8, 2, 128, 16, "f32", seed=52)
+    inp = wl.make_inputs(w)
+    d = [t.to(DEV) for t in (inp.q, inp.k_pool, inp.v_pool)]
+    bt, cl = inp.block_tables.to(DEV), inp.context_lens.to(DEV)
+    out = torch.empty_like(d[0])
+    with pytest.raises(nplib.NPError) as e:
+        nplib.np_paged_decode(out, d[0], d[1], d[2], bt, cl, float("inf"))
+    assert e.value.status == nplib.NP_ERR_INVALID_ARG
+    with pytest.raises(nplib.NPError) as e:
+        nplib.np_paged_decode(None, d[0], d[1], d[2], bt, cl, 0.1, num_splits=4)
+    assert e.value.status == nplib.NP_ERR_WORKSPACE
+    small = torch.empty(16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(nplib.NPError) as e:
+        nplib.np_paged_decode(None, d[0], d[1], d[2], bt, cl, 0.1, num_splits=4, workspace=small)
+    assert e.value.status == nplib.NP_ERR_WORKSPACE
+
+
+# ------------------------------------------------------ launch contexts ---
+def test_cuda_graph_capture_and_replay(nplib):
+    w = _custom([100, 3000, 17, 1200], 40, 8, 128, 32, "bf16", seed=60)
+    inp = wl.make_inputs(w)
+    host = wl.full_host(inp)
+    q, kp, vp, kn, vn = (t.to(DEV) for t in (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new))
+    bt, cl, sm = (t.to(DEV) for t in (inp.block_tables, inp.context_lens, inp.slot_mapping))
+    S = nplib.np_paged_decode_plan(w.rows, w.q_heads, w.kv_heads, w.head_dim, w.block_size,
+                                   bt.shape[1], torch.bfloat16)
+    ws = nplib.workspace(w.rows, w.q_heads, w.head_dim, S)
+    out = torch.empty_like(q)
+    # first call on the device outside capture (sets kernel attributes)
+    nplib.decode_step(out, q, kp, vp, bt, cl, w.softmax_scale, k_new=kn, v_new=vn,
+                      slot_mapping=sm, num_splits=S, workspace=ws)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    out.zero_()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        nplib.decode_step(out, q, kp, vp, bt, cl, w.softmax_scale, k_new=kn, v_new=vn,
+                          slot_mapping=sm, num_splits=S, workspace=ws)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    ref, _ = oracle_step(host, w.softmax_scale)
+    assert_parity(out, ref, "bf16", "graph replay")
+
+
+def test_non_default_stream_and_determinism(nplib):
+    w = _custom([900, 50, 2048], 32, 8, 128, 16, "bf16", seed=61)
+    inp = wl.make_inputs(w)
+    d = wl.Inputs(w, inp.md, *(t.to(DEV) for t in
+                               (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new)))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        a, _, _ = gpu_step(nplib, d, stream=s)
+    b, _, _ = gpu_step(nplib, d)
+    assert torch.equal(a, b)

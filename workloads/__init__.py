@@ -324,3 +324,21 @@ def row_subproblem(inp: Inputs, rows: list[int]) -> dict:
 def kv_bytes(w: Workload, context_lens: torch.Tensor) -> int:
     """K and V bytes of history one read must stream: sum_r c_r * 2 * Hk * D * es."""
     return int(context_lens.to(torch.int64).sum()) * 2 * w.kv_heads * w.head_dim * w.elem_size
+
+
+def full_host(inp: Inputs) -> dict:
+    """Host copies of every input of the step (small workloads only)."""
+    return dict(
+        q=host_array(inp.q), k_new=host_array(inp.k_new), v_new=host_array(inp.v_new),
+        k_pool=host_array(inp.k_pool), v_pool=host_array(inp.v_pool),
+        block_tables=inp.block_tables.numpy().copy(),
+        context_lens=inp.context_lens.numpy().astype(np.int32),
+        slot_mapping=inp.slot_mapping.numpy().copy(),
+    )
+
+
+# Tolerances of the parity gate: fp32 output within atol 1e-5 + rtol 1e-4
+# (the kernel tolerance the streamed read is held to against the exact
+# reference); bf16 output within atol 2e-2 of the exact result on the same
+# bf16 inputs (the bf16 rounding of the output alone is up to 2^-9 relative).
+TOLERANCE = {"f32": (1e-5, 1e-4), "bf16": (2e-2, 0.0)}
