@@ -3,6 +3,7 @@
 // for every supported GQA group, behind one launcher function.
 #include "decode_kernel.cuh"
 #include "decode_launch.h"
+#include "decode_mma.cuh"
 
 #ifndef NPK_BF16
 #error "define NPK_BF16"
@@ -26,11 +27,27 @@ using StorageT = float;
 namespace npk {
 namespace {
 
+// bf16 pools run on the tensor cores (decode_mma.cuh); fp32 pools keep full
+// fp32 products on the FMA pipes (decode_kernel.cuh).
+template <int G>
+struct Variant {
+#if NPK_BF16
+  using SM = MmaSmem<NPK_D, G>;
+  static constexpr auto kernel = paged_decode_mma_kernel<NPK_D, G>;
+  static size_t fixed(int) { return 16 + 128; }
+#else
+  using SM = DecodeSmem<StorageT, NPK_D, G>;
+  static constexpr auto kernel = paged_decode_kernel<StorageT, NPK_D, G>;
+  static size_t fixed(int warps) { return SM::ptile_bytes(warps) + 16 + 128; }
+#endif
+};
+
 template <int G>
 np_status launch_one(DecodeLaunch& L, DecodeParams& p) {
-  using SM = DecodeSmem<StorageT, NPK_D, G>;
+  using V = Variant<G>;
+  using SM = typename V::SM;
   const int warps = L.head_group * L.token_warps;
-  const size_t fixed = SM::ptile_bytes(warps) + 16 + 128;
+  const size_t fixed = V::fixed(warps);
   const size_t sb = SM::stage_bytes(L.head_group);
   if (L.smem_budget <= fixed) return NP_ERR_UNSUPPORTED;
   size_t stages = (L.smem_budget - fixed) / (sb + 16);
@@ -43,7 +60,7 @@ np_status launch_one(DecodeLaunch& L, DecodeParams& p) {
   L.stages = (int)stages;
   L.smem_bytes = smem;
 
-  auto kern = paged_decode_kernel<StorageT, NPK_D, G>;
+  auto kern = V::kernel;
   // The opt-in shared-memory limit is a per-device function attribute.
   static unsigned long long configured = 0;  // bit d: done on device d
   int dev = 0;
