@@ -268,8 +268,8 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
     inp = wl.make_inputs(w, device=dev, poison=False)
     md = inp.md
     bt, cl, sm = (t.to(dev) for t in (md.block_tables, md.context_lens, md.slot_mapping))
-    S = npg.np_paged_decode_plan(w.rows, w.q_heads, w.kv_heads, w.head_dim, w.block_size,
-                                 bt.shape[1], w.torch_dtype)
+    S = args.splits or npg.np_paged_decode_plan(w.rows, w.q_heads, w.kv_heads, w.head_dim,
+                                                w.block_size, bt.shape[1], w.torch_dtype)
     ws = npg.workspace(w.rows, w.q_heads, w.head_dim, S, device=dev)
     out = torch.empty_like(inp.q)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -433,10 +433,16 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=2.0)
+    ap.add_argument("--splits", type=int, default=None,
+                    help="override the library's split plan (profiling)")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="keep only the first N rows of the workload (small profiling cases)")
     args = ap.parse_args(argv)
     if args.impl == "ours" and args.warmup < 3:
         args.warmup = 3  # timing rule: at least 3 untimed warm-up steps
     w = wl.WORKLOADS[args.workload]
+    if args.rows is not None and args.rows < w.rows:
+        w = wl.truncated(w, args.rows)
     dist, rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         line = run_reference(args, w, dist, rank)

@@ -30,23 +30,23 @@ def nvcc() -> str:
     return cand
 
 
-def _units(extra: list[str]) -> list[tuple[str, str, list[str]]]:
+def _units(extra: list[str], build_dir: str, csrc: str) -> list[tuple[str, str, list[str]]]:
     """(source, object, extra flags) for every translation unit."""
-    objdir = os.path.join(BUILD, "obj")
+    objdir = os.path.join(build_dir, "obj")
     units = [
-        (os.path.join(CSRC, "api.cu"), os.path.join(objdir, "api.o"), []),
-        (os.path.join(CSRC, "append_reduce.cu"), os.path.join(objdir, "append_reduce.o"), []),
+        (os.path.join(csrc, "api.cu"), os.path.join(objdir, "api.o"), []),
+        (os.path.join(csrc, "append_reduce.cu"), os.path.join(objdir, "append_reduce.o"), []),
     ]
     for bf16 in (0, 1):
         for d in HEAD_DIMS:
             name = f"decode_{'bf16' if bf16 else 'f32'}_d{d}.o"
-            units.append((os.path.join(CSRC, "decode_inst.cu"), os.path.join(objdir, name),
+            units.append((os.path.join(csrc, "decode_inst.cu"), os.path.join(objdir, name),
                           [f"-DNPK_BF16={bf16}", f"-DNPK_D={d}"]))
-    return [(s, o, f + extra) for s, o, f in units]
+    return [(s, o, ["-I", csrc] + f + extra) for s, o, f in units]
 
 
-def _deps() -> list[str]:
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+def _deps(csrc: str) -> list[str]:
+    files = [os.path.join(csrc, f) for f in os.listdir(csrc)]
     files.append(os.path.join(INCLUDE, "np_paged.h"))
     files.append(os.path.abspath(__file__))
     return files
@@ -61,7 +61,7 @@ def _stale(target: str, deps: list[str]) -> bool:
 
 def _compile(src: str, obj: str, flags: list[str], verbose_ptxas: bool) -> str:
     cmd = [nvcc(), "-std=c++17", "-O3", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
-           "-I", INCLUDE, "-I", CSRC, *flags, "-c", src, "-o", obj + ".tmp"]
+           "-I", INCLUDE, *flags, "-c", src, "-o", obj + ".tmp"]
     if verbose_ptxas:
         cmd.insert(1, "-Xptxas=-v")
     p = subprocess.run(cmd, capture_output=True, text=True)
@@ -72,14 +72,24 @@ def _compile(src: str, obj: str, flags: list[str], verbose_ptxas: bool) -> str:
 
 
 def build(force: bool = False, extra_flags: list[str] | None = None, out: str | None = None,
-          verbose_ptxas: bool = False, jobs: int | None = None) -> str:
-    """Compile (incrementally) and link; returns the library path."""
+          verbose_ptxas: bool = False, jobs: int | None = None,
+          build_dir: str | None = None, csrc: str | None = None) -> str:
+    """Compile (incrementally) and link; returns the library path.
+
+    ``extra_flags`` (e.g. -D tuning macros) or another source directory
+    ``csrc`` need their own ``build_dir`` and ``out`` so they never mix with
+    the default build's objects.
+    """
     out = out or LIB
+    build_dir = build_dir or BUILD
+    csrc = csrc or CSRC
     extra = list(extra_flags or [])
-    units = _units(extra)
-    os.makedirs(os.path.join(BUILD, "obj"), exist_ok=True)
-    deps = _deps()
-    todo = [u for u in units if force or extra or _stale(u[1], deps)]
+    if (extra or csrc != CSRC) and build_dir == BUILD:
+        raise ValueError("extra_flags / csrc need a separate build_dir")
+    units = _units(extra, build_dir, csrc)
+    os.makedirs(os.path.join(build_dir, "obj"), exist_ok=True)
+    deps = _deps(csrc)
+    todo = [u for u in units if force or _stale(u[1], deps)]
     logs = {}
     if todo:
         jobs = jobs or min(len(todo), max(1, os.cpu_count() or 1))

@@ -6,10 +6,17 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
+
+#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled_v12000
 
 #include "decode_kernel.cuh"
 #include "decode_launch.h"
 #include "np_paged.h"
+
+#ifndef NPK_SPLIT_BYTES
+#define NPK_SPLIT_BYTES (2ll << 20)  // K+V bytes one split should read
+#endif
 
 #ifndef NPK_SMEM_BUDGET
 #define NPK_SMEM_BUDGET 0  // 0: the device's opt-in maximum per block
@@ -71,6 +78,85 @@ np_status device_info(int* sms, int* smem) {
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---- tiled TMA maps of the pools (bf16, head_dim a multiple of 64)
+// The driver's encoder is reached through the runtime (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Map of one pool as a 3-D tensor (dim, slot, kv head) -- the kv-head
+// dimension is listed last although its stride (head_dim*2 bytes) is the
+// smaller one, so that a box {64, box_tokens, head_group} lands in shared
+// memory as [head][token][64 dims] (each head's tokens in consecutive
+// 128-byte rows, 128-byte swizzle).  Returns false if the driver refuses.
+bool encode_pool_map(CUtensorMap* m, const void* pool, int64_t slots, int32_t kv_heads,
+                     int32_t head_dim, int box_tokens, int head_group) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)slots, (cuuint64_t)kv_heads};
+  cuuint64_t strides[2] = {(cuuint64_t)kv_heads * head_dim * 2, (cuuint64_t)head_dim * 2};
+  cuuint32_t box[3] = {64u, (cuuint32_t)box_tokens, (cuuint32_t)head_group};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult rc = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS;
+}
+
+// Small per-thread cache: the same pools are read step after step.
+struct MapKey {
+  const void* k;
+  const void* v;
+  int64_t slots;
+  int32_t kv_heads, head_dim, box_tokens, head_group, device;
+  bool operator==(const MapKey& o) const {
+    return k == o.k && v == o.v && slots == o.slots && kv_heads == o.kv_heads &&
+           head_dim == o.head_dim && box_tokens == o.box_tokens && head_group == o.head_group &&
+           device == o.device;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap mk, mv;
+  bool ok;
+  bool used;
+};
+
+bool pool_maps(DecodeParams& p, const void* k, const void* v, int64_t slots, int32_t kv_heads,
+               int32_t head_dim, int box_tokens, int head_group) {
+  thread_local MapEntry cache[4] = {};
+  thread_local int next = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  MapKey key{k, v, slots, kv_heads, head_dim, box_tokens, head_group, dev};
+  for (auto& e : cache) {
+    if (e.used && e.key == key) {
+      p.tm_k = e.mk;
+      p.tm_v = e.mv;
+      return e.ok;
+    }
+  }
+  MapEntry& e = cache[next];
+  next = (next + 1) % 4;
+  e.key = key;
+  e.used = true;
+  e.ok = encode_pool_map(&e.mk, k, slots, kv_heads, head_dim, box_tokens, head_group) &&
+         encode_pool_map(&e.mv, v, slots, kv_heads, head_dim, box_tokens, head_group);
+  p.tm_k = e.mk;
+  p.tm_v = e.mv;
+  return e.ok;
+}
 
 npk::DecodeLauncher launcher_for(np_dtype dt, int32_t d) {
   if (dt == NP_F32) {
@@ -165,7 +251,7 @@ np_status np_paged_decode_plan(int32_t rows, int32_t q_heads, int32_t kv_heads,
   // Tokens per split: about 2 MB of K+V per CTA, and at least 128x the
   // partial result it writes (so partials + reduce stay ~1% of the traffic).
   const int64_t tok_bytes = 2ll * hg * head_dim * es;
-  int64_t sl = (2ll << 20) / tok_bytes;
+  int64_t sl = NPK_SPLIT_BYTES / tok_bytes;
   const int64_t sl_partial = 256ll * g / es;
   if (sl < sl_partial) sl = sl_partial;
   sl = (sl + 63) / 64 * 64;
@@ -252,6 +338,21 @@ np_status np_paged_decode(void* out, const void* q, const void* k_pool, const vo
   p.num_splits = num_splits;
   p.stages = 0;
   p.qscale = scale * 1.4426950408889634f;  // log2(e)
+  // bf16 pools with head_dim a multiple of 64 stage K/V through tiled TMA
+  // boxes of box_tokens tokens: the largest power of two <= 16 dividing the
+  // block size, with box_tokens * head_group a multiple of 8 (each box then
+  // starts on a 1024-byte swizzle boundary) and slot coordinates in int32.
+  p.use_tmap = 0;
+  p.box_tokens = 1;
+  if (dtype == NP_BF16 && head_dim % 64 == 0 && slots <= INT32_MAX) {
+    int bt = 1;
+    while (bt < 16 && block_size % (bt * 2) == 0) bt *= 2;
+    if ((bt * hg) % 8 == 0 &&
+        pool_maps(p, k_pool, v_pool, slots, kv_heads, head_dim, bt, hg)) {
+      p.use_tmap = 1;
+      p.box_tokens = bt;
+    }
+  }
 
   DecodeLaunch L{};
   L.params = &p;

@@ -27,14 +27,15 @@ using StorageT = float;
 namespace npk {
 namespace {
 
-// bf16 pools run on the tensor cores (decode_mma.cuh); fp32 pools keep full
-// fp32 products on the FMA pipes (decode_kernel.cuh).
-template <int G>
+// bf16 pools run on the tensor cores (decode_mma.cuh): through tiled TMA
+// boxes when the host built pool maps, else through per-token copies.  fp32
+// pools keep full fp32 products on the FMA pipes (decode_kernel.cuh).
+template <int G, bool TMAP>
 struct Variant {
 #if NPK_BF16
-  using SM = MmaSmem<NPK_D, G>;
-  static constexpr auto kernel = paged_decode_mma_kernel<NPK_D, G>;
-  static size_t fixed(int) { return 16 + 128; }
+  using SM = MmaSmem<NPK_D, G, TMAP>;
+  static constexpr auto kernel = paged_decode_mma_kernel<NPK_D, G, TMAP>;
+  static size_t fixed(int) { return 16 + 128 + 1024; }
 #else
   using SM = DecodeSmem<StorageT, NPK_D, G>;
   static constexpr auto kernel = paged_decode_kernel<StorageT, NPK_D, G>;
@@ -42,9 +43,9 @@ struct Variant {
 #endif
 };
 
-template <int G>
-np_status launch_one(DecodeLaunch& L, DecodeParams& p) {
-  using V = Variant<G>;
+template <int G, bool TMAP>
+np_status launch_variant(DecodeLaunch& L, DecodeParams& p) {
+  using V = Variant<G, TMAP>;
   using SM = typename V::SM;
   const int warps = L.head_group * L.token_warps;
   const size_t fixed = V::fixed(warps);
@@ -65,19 +66,24 @@ np_status launch_one(DecodeLaunch& L, DecodeParams& p) {
   static unsigned long long configured = 0;  // bit d: done on device d
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return NP_ERR_CUDA;
-  if (dev < 64 && !((__atomic_load_n(&configured, __ATOMIC_ACQUIRE) >> dev) & 1ull)) {
+  if (dev >= 64 || !((__atomic_load_n(&configured, __ATOMIC_ACQUIRE) >> dev) & 1ull)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)L.smem_budget) != cudaSuccess)
       return NP_ERR_CUDA;
-    __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
-  } else if (dev >= 64) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)L.smem_budget) != cudaSuccess)
-      return NP_ERR_CUDA;
+    if (dev < 64) __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
   }
   dim3 grid(L.splits, L.rows, L.head_groups);
   kern<<<grid, 32 * (warps + 1), smem, L.stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? NP_OK : NP_ERR_CUDA;
+}
+
+template <int G>
+np_status launch_one(DecodeLaunch& L, DecodeParams& p) {
+#if NPK_BF16 && (NPK_D % 64 == 0)
+  if (p.use_tmap) return launch_variant<G, true>(L, p);
+#endif
+  p.use_tmap = 0;
+  return launch_variant<G, false>(L, p);
 }
 
 }  // namespace

@@ -41,6 +41,11 @@
 namespace npk {
 
 struct DecodeParams {
+  // Tiled TMA maps of the K and V pools as [head_dim, slot, kv_head] with the
+  // kv-head stride innermost after head_dim's (see decode_mma.cuh); only
+  // read when use_tmap is set.
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
   void* out;             // [R, Hq, D] T, when num_splits == 1
   float* ws_o;           // [R, Hq, S, D] fp32, when num_splits > 1
   float* ws_lse;         // [R, Hq, S] fp32 (natural log)
@@ -60,6 +65,8 @@ struct DecodeParams {
   int32_t q_heads;
   int32_t num_splits;
   int32_t stages;        // ring depth
+  int32_t use_tmap;      // 1: K/V arrive through tm_k/tm_v boxes
+  int32_t box_tokens;    // tokens per TMA box (divides block_size and the chunk)
   float qscale;          // softmax scale * log2(e)
 };
 
@@ -130,7 +137,8 @@ struct DecodeSmem {
 };
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kMaxThreads, 1) paged_decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kMaxThreads, 1)
+    paged_decode_kernel(const __grid_constant__ DecodeParams p) {
   using C = DecodeCfg<T, D, G>;
   using S = DecodeSmem<T, D, G>;
   constexpr unsigned FULL = 0xffffffffu;
@@ -179,7 +187,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) paged_decode_kernel(const Deco
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
       mbar_init(smem_u32(&full_bar[i]), 1);
-      mbar_init(smem_u32(&empty_bar[i]), HG * 32);
+      mbar_init(smem_u32(&empty_bar[i]), HG);  // one arrive per consumer warp
     }
     *abort = 0;
     fence_mbar_init();
@@ -252,11 +260,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) paged_decode_kernel(const Deco
     // every stage.  In normal operation the consumers already did.
     if (*abort) {
       for (int64_t ch = max((int64_t)0, issued - stages); ch < issued; ++ch) {
-        const uint32_t fb = smem_u32(&full_bar[ch % stages]);
-        const uint64_t tstart = global_ns();
-        while (!mbar_try_wait(fb, (uint32_t)((ch / stages) & 1)) &&
-               global_ns() - tstart < kWaitLimitNs) {
-        }
+        mbar_wait_drain(smem_u32(&full_bar[ch % stages]), (uint32_t)((ch / stages) & 1));
       }
     }
   } else {
@@ -385,7 +389,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) paged_decode_kernel(const Deco
         }
         __syncwarp();
       }
-      mbar_arrive(smem_u32(&empty_bar[st]));
+      __syncwarp();  // every lane's reads of this stage are done
+      if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
     }
 
     // ---- combine the lanes' partial sums

@@ -2,10 +2,10 @@
 // (warp-level mma.sync m16n8k16, bf16 inputs, fp32 accumulation).
 //
 // Same operation, grid and pipeline roles as decode_kernel.cuh (see there for
-// the citations): producer warp walks the block table and moves K/V with
-// bulk TMA copies into an mbarrier ring; consumer warp (hl, tw) owns kv head
-// hl and every G-th query head of its group.  What changes is the consumer's
-// arithmetic, which is a pair of small dense products per 16-token tile:
+// the citations): a producer warp walks the block table and moves K/V with
+// TMA into an mbarrier ring; consumer warp (hl, tw) owns kv head hl and the G
+// query heads of its group.  The consumer's arithmetic is a pair of small
+// dense products per 16-token tile:
 //
 //   S^T[h, t] = q[h, :] . K[t, :]      M = 16 query heads (G real, rest 0),
 //                                      N = 8 tokens, K = 16 dims per mma;
@@ -24,9 +24,14 @@
 // with two xor-shuffles.  P is rounded to bf16 for the PV product (relative
 // error 2^-9 per weight; the accumulation stays fp32).
 //
-// Shared-memory rows: the producer copies each token's [HG, D] row on its
-// own, to a row stride of HG*D*2 + 16 bytes, so the 8 rows one ldmatrix
-// phase reads fall in 8 different bank groups (no conflicts).
+// Staging (how a chunk of CT tokens x HG kv heads lands in shared memory):
+//  * TMAP (head_dim a multiple of 64): tiled TMA boxes of {64 dims, B tokens,
+//    HG heads} from a tensor map whose dimensions are (dim, slot, kv head) --
+//    so inside a box each head's B token rows are consecutive 128-byte rows,
+//    stored with the 128-byte swizzle.  The 8 token rows one ldmatrix phase
+//    reads then sit in 8 different bank groups.  A 64 KB chunk is 4 copies.
+//  * otherwise: one 1-D bulk copy per token row, to a row stride padded by
+//    16 bytes (the same conflict-free property, more copy instructions).
 #pragma once
 
 #include <math.h>
@@ -64,22 +69,32 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int D, int G>
+#ifndef NPK_MMA_CT
+#define NPK_MMA_CT 16  // tokens per pipeline stage for head_dim >= 64
+#endif
+#ifndef NPK_MMA_MIN_BLOCKS
+#define NPK_MMA_MIN_BLOCKS 1  // resident CTAs per SM the register budget targets
+#endif
+
+template <int D, int G, bool TMAP>
 struct MmaCfg {
-  static constexpr int ES = 2;
-  static constexpr int KS = D / 16;        // mma k-steps over head_dim (QK), m-tiles (PV)
-  static constexpr int ST = 16;            // tokens per softmax tile
-  static constexpr int CT = D >= 256 ? 16 : (D >= 64 ? 16 : 32);  // tokens per stage
+  static constexpr int KS = D / 16;  // mma k-steps over head_dim (QK), m-tiles (PV)
+  static constexpr int ST = 16;      // tokens per softmax tile
+  static constexpr int CT = D >= 64 ? NPK_MMA_CT : 32;  // tokens per stage
+  // CT < ST is allowed: the tile's rows past the chunk are masked and their
+  // shared-memory reads are redirected to the tile's first row.
   static_assert(D % 16 == 0 && G >= 1 && G <= 8, "shape");
-  static_assert(CT % ST == 0 && CT <= 32, "tiling");
+  static_assert((CT % ST == 0 || ST % CT == 0) && CT <= 32, "tiling");
+  static_assert(!TMAP || D % 64 == 0, "TMA boxes are 64 dims wide");
 };
 
-template <int D, int G>
+template <int D, int G, bool TMAP>
 struct MmaSmem {
-  using C = MmaCfg<D, G>;
+  using C = MmaCfg<D, G, TMAP>;
+  // bytes between consecutive token rows (padded layout only)
   __host__ __device__ static constexpr size_t row_stride(int hg) { return (size_t)hg * D * 2 + 16; }
   __host__ __device__ static constexpr size_t stage_bytes(int hg) {
-    return 2ull * C::CT * row_stride(hg);
+    return TMAP ? 2ull * C::CT * hg * D * 2 : 2ull * C::CT * row_stride(hg);
   }
   __host__ __device__ static constexpr size_t merge_bytes(int warps) {
     return (size_t)warps * G * (D + 2) * sizeof(float);
@@ -87,17 +102,19 @@ struct MmaSmem {
   __host__ __device__ static constexpr size_t ring_bytes(int hg, int stages, int warps) {
     size_t ring = stage_bytes(hg) * stages;
     size_t m = merge_bytes(warps);
-    return ((ring > m ? ring : m) + 127) / 128 * 128;
+    return ((ring > m ? ring : m) + 1023) / 1024 * 1024;
   }
+  // + 1024: the ring starts at the first 1024-byte boundary of the window
   __host__ __device__ static constexpr size_t total(int hg, int stages, int warps) {
-    return ring_bytes(hg, stages, warps) + 16ull * stages + 16;
+    return 1024 + ring_bytes(hg, stages, warps) + 16ull * stages + 16;
   }
 };
 
-template <int D, int G>
-__global__ void __launch_bounds__(kMaxThreads, 1) paged_decode_mma_kernel(const DecodeParams p) {
-  using C = MmaCfg<D, G>;
-  using S = MmaSmem<D, G>;
+template <int D, int G, bool TMAP>
+__global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
+    paged_decode_mma_kernel(const __grid_constant__ DecodeParams p) {
+  using C = MmaCfg<D, G, TMAP>;
+  using S = MmaSmem<D, G, TMAP>;
   constexpr unsigned FULL = 0xffffffffu;
 
   const int split = blockIdx.x;
@@ -130,9 +147,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) paged_decode_mma_kernel(const 
     return;
   }
 
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // the ring starts 1024-byte aligned (TMA's 128-byte swizzle repeats every
+  // 1024 bytes of shared-memory address)
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int stages = p.stages;
-  const uint32_t RS = (uint32_t)S::row_stride(HG);
   const size_t stage_bytes = S::stage_bytes(HG);
   const size_t ring = S::ring_bytes(HG, stages, NC);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + ring);
@@ -142,7 +161,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) paged_decode_mma_kernel(const 
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
       mbar_init(smem_u32(&full_bar[i]), 1);
-      mbar_init(smem_u32(&empty_bar[i]), HG * 32);
+      mbar_init(smem_u32(&empty_bar[i]), HG);  // one arrive per consumer warp
     }
     *abort = 0;
     fence_mbar_init();
@@ -151,13 +170,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1) paged_decode_mma_kernel(const 
 
   const int64_t nch = (t1 - t0 + C::CT - 1) / C::CT;
   const uint32_t row_bytes = (uint32_t)HG * D * 2;  // one token, HG kv heads
+  // TMAP layout of a stage: [K | V] x [D/64 slabs of 64 dims] x [CT/B boxes]
+  //                         x [HG heads] x [B token rows of 128 bytes]
+  const int BT = TMAP ? p.box_tokens : 1;
+  const uint32_t half_bytes = (uint32_t)C::CT * HG * 128;  // one 64-dim slab of a chunk
+  const uint32_t box_bytes = (uint32_t)BT * HG * 128;      // one box within a slab
+  const uint32_t RS = (uint32_t)S::row_stride(HG);         // padded layout
 
-  // running softmax state; lanes 4h..4h+3 hold head h's values
   float m_run = -INFINITY, l_run = 0.f;
-  float o[C::KS][4];  // O^T fragments: rows d = 16*mt + lane/4 (+8), cols h = 2*(lane%4) (+1)
+  float o[C::KS][4];  // O^T fragments: rows d = 16*mi + lane/4 (+8), cols h = 2*(lane%4) (+1)
 
   if (warp == NC) {
-    // ======================= producer warp: one bulk copy per token row
+    // ======================= producer warp
     const uint64_t pol = policy_evict_first();
     const int64_t bs = p.block_size;
     const int64_t tab0 = (int64_t)r * p.max_blocks_per_row;
@@ -179,7 +203,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) paged_decode_mma_kernel(const 
       const uint32_t fb = smem_u32(&full_bar[st]);
       const uint32_t kdst = smem_u32(smem + st * stage_bytes);
       const uint32_t vdst = kdst + (uint32_t)(stage_bytes / 2);
-      if (lane == 0) mbar_arrive_expect_tx(fb, 2u * (uint32_t)n * row_bytes);
       const int64_t jfirst = cb / bs;
       const int64_t jlast = (cb + n - 1) / bs;
       if (win < 0 || jlast >= win + 32) {
@@ -187,36 +210,61 @@ __global__ void __launch_bounds__(kMaxThreads, 1) paged_decode_mma_kernel(const 
         const int64_t jj = win + lane;
         my_id = jj < nblk ? p.block_tables[tab0 + jj] : 0;
       }
-      const int64_t t = cb + (lane < n ? lane : 0);
-      const int64_t j = t / bs;
-      int64_t b = __shfl_sync(FULL, my_id, (int)(j - win));
-      if (b < 0 || b >= p.num_blocks) {
-        if (lane < n) set_flag(p.err, NP_FLAG_BLOCK_ID);
-        b = 0;
-      }
-      if (lane < n) {
-        const int64_t slot = b * bs + (t - j * bs);
-        bulk_g2s(kdst + lane * RS, kpool + slot * pool_row, row_bytes, fb, pol);
-        bulk_g2s(vdst + lane * RS, vpool + slot * pool_row, row_bytes, fb, pol);
+      if constexpr (TMAP) {
+        // boxes of BT tokens; each lies inside one block (BT divides the block
+        // size and the chunk start) and is copied whole (rows past the
+        // history are masked by the consumers)
+        const int nbox = (n + BT - 1) / BT;
+        if (lane == 0) mbar_arrive_expect_tx(fb, 2u * (D / 64) * nbox * box_bytes);
+        const int items = nbox * (D / 64) * 2;  // (box, slab, K|V)
+        const int rounds = (items + 31) / 32;
+        for (int rd = 0; rd < rounds; ++rd) {
+          const int it = rd * 32 + lane;
+          const int bx = (it < items ? it : 0) / ((D / 64) * 2);
+          const int64_t t = cb + (int64_t)bx * BT;
+          const int64_t j = t / bs;
+          int64_t b = __shfl_sync(FULL, my_id, (int)(j - win));
+          if (it < items) {
+            const int slab = (it >> 1) % (D / 64);
+            const bool isv = (it & 1) != 0;
+            if (b < 0 || b >= p.num_blocks) {
+              set_flag(p.err, NP_FLAG_BLOCK_ID);
+              b = 0;
+            }
+            const int64_t slot = b * bs + (t - j * bs);
+            const uint32_t dst = (isv ? vdst : kdst) + slab * half_bytes + bx * box_bytes;
+            tma_load_3d(dst, isv ? &p.tm_v : &p.tm_k, slab * 64, (int32_t)slot, hgi * HG, fb,
+                        pol);
+          }
+        }
+      } else {
+        if (lane == 0) mbar_arrive_expect_tx(fb, 2u * (uint32_t)n * row_bytes);
+        const int64_t t = cb + (lane < n ? lane : 0);
+        const int64_t j = t / bs;
+        int64_t b = __shfl_sync(FULL, my_id, (int)(j - win));
+        if (b < 0 || b >= p.num_blocks) {
+          if (lane < n) set_flag(p.err, NP_FLAG_BLOCK_ID);
+          b = 0;
+        }
+        if (lane < n) {
+          const int64_t slot = b * bs + (t - j * bs);
+          bulk_g2s(kdst + lane * RS, kpool + slot * pool_row, row_bytes, fb, pol);
+          bulk_g2s(vdst + lane * RS, vpool + slot * pool_row, row_bytes, fb, pol);
+        }
       }
       issued = ch + 1;
     }
-    if (*abort) {
-      for (int64_t ch = max((int64_t)0, issued - stages); ch < issued; ++ch) {
-        const uint32_t fb = smem_u32(&full_bar[ch % stages]);
-        const uint64_t tstart = global_ns();
-        while (!mbar_try_wait(fb, (uint32_t)((ch / stages) & 1)) &&
-               global_ns() - tstart < kWaitLimitNs) {
-        }
-      }
+    if (*abort) {  // never leave copies in flight (bounded)
+      for (int64_t ch = max((int64_t)0, issued - stages); ch < issued; ++ch)
+        mbar_wait_drain(smem_u32(&full_bar[ch % stages]), (uint32_t)((ch / stages) & 1));
     }
   } else {
     // ======================= consumer warp: kv head hl, chunks tw, tw+TW, ...
     const int hl = warp % HG;
     const int tw = warp / HG;
     const int kvh = hgi * HG + hl;
-    const int g4 = lane >> 2;   // fragment row group
-    const int c4 = lane & 3;    // fragment column pair
+    const int g4 = lane >> 2;  // fragment row group
+    const int c4 = lane & 3;   // fragment column pair
 
     // q as mma A fragments (rows = query heads of this group; rows >= G zero)
     uint32_t qa0[C::KS], qa2[C::KS];
@@ -235,15 +283,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) paged_decode_mma_kernel(const 
       }
     }
 #pragma unroll
-    for (int mt = 0; mt < C::KS; ++mt)
+    for (int mi = 0; mi < C::KS; ++mi)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) o[mt][e] = 0.f;
+      for (int e = 0; e < 4; ++e) o[mi][e] = 0.f;
 
-    // ldmatrix lane addressing: matrix (lane/8): token 8*(lane/16) + lane%8,
-    // column chunk 8*((lane/8)%2) -- the same pattern serves K (B of QK) and
-    // V (A of PV, transposed load)
+    // ldmatrix lane addressing: matrix (lane/8) covers tokens 8*(lane/16) +
+    // (0..7) and the 8-dim column chunk (lane/8)%2 of a 16-dim step; the same
+    // pattern serves K (B of QK) and V (A of PV, transposed load)
     const int ld_tok = ((lane >> 4) << 3) + (lane & 7);
-    const int ld_col = ((lane >> 3) & 1) * 8;
+    const int ld_c = (lane >> 3) & 1;
 
     for (int64_t ch = tw; ch < nch; ch += TW) {
       const int st = (int)(ch % stages);
@@ -253,21 +301,37 @@ __global__ void __launch_bounds__(kMaxThreads, 1) paged_decode_mma_kernel(const 
         break;
       }
       const int nvalid = (int)min((int64_t)C::CT, t1 - (t0 + ch * C::CT));
-      const uint32_t kbase = smem_u32(smem + st * stage_bytes) + hl * D * 2;
-      const uint32_t vbase = kbase + (uint32_t)(stage_bytes / 2);
+      const uint32_t kst = smem_u32(smem + st * stage_bytes);
+      const uint32_t vst = kst + (uint32_t)(stage_bytes / 2);
 
       for (int sb = 0; sb < nvalid; sb += C::ST) {
-        // rows past the valid tokens are read from row 0 of the tile instead
-        // (finite data; their probabilities are exactly 0)
+        // rows past the valid tokens read row sb instead (finite data; their
+        // probabilities are exactly 0)
         const int tok = (sb + ld_tok < nvalid) ? sb + ld_tok : sb;
-        const uint32_t kaddr = kbase + tok * RS + ld_col * 2;
-        const uint32_t vaddr = vbase + tok * RS + ld_col * 2;
+        // this lane's row within a slab, and its swizzle
+        uint32_t row_off, swz = 0;
+        if constexpr (TMAP) {
+          const int bx = tok / BT, tr = tok - bx * BT;
+          row_off = bx * box_bytes + (hl * BT + tr) * 128;
+          swz = (row_off >> 7) & 7;
+        } else {
+          row_off = tok * RS + hl * D * 2;
+        }
+        // address of this lane's 16-byte chunk of dims [16*ks + 8*ld_c, +8)
+        auto chunk_addr = [&](uint32_t base, int ks) -> uint32_t {
+          if constexpr (TMAP) {
+            const uint32_t cidx = ((2 * ks) & 7) + ld_c;  // chunk within the 128-byte row
+            return base + (ks >> 2) * half_bytes + row_off + ((cidx ^ swz) << 4);
+          } else {
+            return base + row_off + ks * 32 + ld_c * 16;
+          }
+        };
         // ---- S^T = q K^T for 16 tokens (two n-tiles of 8)
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int ks = 0; ks < C::KS; ++ks) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(kaddr + ks * 32, b0, b1, b2, b3);
+          ldsm_x4(chunk_addr(kst, ks), b0, b1, b2, b3);
           mma_bf16(s0, qa0[ks], 0u, qa2[ks], 0u, b0, b1);
           mma_bf16(s1, qa0[ks], 0u, qa2[ks], 0u, b2, b3);
         }
@@ -306,12 +370,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) paged_decode_mma_kernel(const 
 #pragma unroll
         for (int mi = 0; mi < C::KS; ++mi) {
           uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(vaddr + mi * 32, a0, a1, a2, a3);
+          ldsm_x4_t(chunk_addr(vst, mi), a0, a1, a2, a3);
           mma_bf16(o[mi], a0, a1, a2, a3, pb0, pb1);
         }
       }
-      __syncwarp();
-      mbar_arrive(smem_u32(&empty_bar[st]));
+      __syncwarp();  // every lane's reads of this stage are done
+      if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
     }
     // the head's sum over its 4 lanes
     l_run += __shfl_xor_sync(FULL, l_run, 1);
@@ -346,13 +410,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) paged_decode_mma_kernel(const 
   if (warp >= NC || warp / HG != 0) return;
   const int hl = warp;  // tw == 0
   const int kvh = hgi * HG + hl;
+  constexpr int DL = D >= 32 ? D / 32 : 1;  // dims per lane
+  const int d0 = lane * DL;
   for (int h = 0; h < G; ++h) {
     float mm = -INFINITY;
     for (int w2 = 0; w2 < TW; ++w2) mm = fmaxf(mm, merge[(hl + w2 * HG) * stride_w + h]);
     float ll = 0.f;
-    constexpr int DL = D >= 32 ? D / 32 : 1;  // dims per lane
     float acc[DL];
-    const int d0 = lane * DL;
 #pragma unroll
     for (int e = 0; e < DL; ++e) acc[e] = 0.f;
     for (int w2 = 0; w2 < TW; ++w2) {
@@ -371,7 +435,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) paged_decode_mma_kernel(const 
     for (int e = 0; e < DL; ++e) ov[e] = acc[e] * inv;
     if (d0 < D) {
       if (p.num_splits == 1) {
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + ((int64_t)r * p.q_heads + hq) * D;
+        __nv_bfloat16* orow =
+            static_cast<__nv_bfloat16*>(p.out) + ((int64_t)r * p.q_heads + hq) * D;
         Storage<__nv_bfloat16>::template store<DL>(orow + d0, ov);
       } else {
         const int64_t rs = ((int64_t)r * p.q_heads + hq) * p.num_splits + split;

@@ -3,6 +3,7 @@
 // widening, error flags.  sm_103a only.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (type only; the library never links libcuda)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -17,15 +18,11 @@ __device__ __forceinline__ void set_flag(int32_t* err, int32_t bit) {
 }
 
 // ----------------------------------------------------------------- time ---
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// A pipeline wait gives up after this long (nothing legitimate takes more
-// than microseconds; this bounds a wait that could otherwise never end).
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+// A pipeline wait gives up after this many SM clock cycles (about 1 s at the
+// GB300's 2.07 GHz maximum clock; nothing legitimate takes more than
+// microseconds).  clock64 is the SM's own counter: cheap to read, unlike the
+// global timer.
+constexpr long long kWaitLimitCycles = 2000000000ll;
 
 // ------------------------------------------------------------- mbarrier ---
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -65,21 +62,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity has completed.  Bounded: gives
-// up (returns false) when *abort becomes non-zero or after kWaitLimitNs, in
+// up (returns false) when *abort becomes non-zero or after kWaitLimitCycles, in
 // which case it sets *abort itself so every other waiter in the block stops.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
+  const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (clock64() - t0 > kWaitLimitCycles) {
         *abort = 1;
         return false;
       }
     }
+  }
+}
+
+// Bounded wait that ignores the abort flag (used to drain copies in flight).
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < kWaitLimitCycles) {
   }
 }
 
@@ -99,6 +103,19 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// Tiled 3-D TMA load: the box at coordinates (c0, c1, c2) of `map` into this
+// CTA's shared memory, completing its bytes on `bar`.  c0 * element size must
+// be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t c0,
+                                           int32_t c1, int32_t c2, uint32_t bar,
+                                           uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
       : "memory");
 }
 

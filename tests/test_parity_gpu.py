@@ -245,6 +245,18 @@ def test_block_sizes(nplib, block_size):
     _full_parity(nplib, w, num_splits=5)
 
 
+@pytest.mark.parametrize("kv_heads", [1, 8])
+@pytest.mark.parametrize("block_size", [1, 3, 4, 8, 24, 32, 64])
+def test_block_sizes_bf16(nplib, block_size, kv_heads):
+    """bf16 staging: tiled TMA boxes of 1..16 tokens (one or several per
+    chunk) and, where a box would not start on a swizzle boundary
+    (box tokens x kv heads per CTA not a multiple of 8), per-token copies."""
+    w = _custom([1, 15, 16, 17, 100, 700], 2 * kv_heads, kv_heads, 128, block_size, "bf16",
+                seed=70 + block_size + kv_heads)
+    _full_parity(nplib, w)
+    _full_parity(nplib, w, num_splits=3)
+
+
 def test_edge_contexts(nplib):
     """Empty rows, one token, exact chunk and split boundaries, full tables."""
     ctx = [0, 1, 2, 15, 16, 17, 63, 64, 65, 127, 128, 129, 512]

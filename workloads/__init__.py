@@ -49,6 +49,7 @@ class Workload:
     seed: int
     scale: float | None = None  # None -> 1/sqrt(head_dim)
     description: str = ""
+    table_capacity: int | None = None  # tokens a block table can hold (default: max context)
 
     @property
     def group(self) -> int:
@@ -68,6 +69,8 @@ class Workload:
 
     @property
     def max_context(self) -> int:
+        if self.table_capacity is not None:
+            return self.table_capacity
         kind = self.ctx[0]
         return max(self.ctx[1]) if kind == "fixed" else int(self.ctx[2])
 
@@ -131,6 +134,18 @@ def context_lengths(w: Workload) -> torch.Tensor:
         c = torch.exp(math.log(lo) + u * (math.log(hi) - math.log(lo)))
         return torch.round(c).clamp(lo, hi).to(torch.int32)
     raise ValueError(kind)
+
+
+def truncated(w: Workload, rows: int) -> Workload:
+    """The same recipe with only its first ``rows`` rows (same contexts)."""
+    cl = context_lengths(w)[:rows]
+    pool = w.pool if w.pool[0] != "fixed" else ("spare", 0)
+    if pool[0] == "capacity":
+        pool = ("spare", 0)
+    return w.replace(name=f"{w.name}[:{rows}]", rows=rows,
+                     ctx=("fixed", tuple(int(c) for c in cl)), pool=pool,
+                     table_capacity=w.max_context,
+                     description=f"{w.description}; first {rows} rows")
 
 
 def pool_blocks(w: Workload, needed_total: int) -> int:
