@@ -44,53 +44,96 @@ np_status launch_append(void* k_pool, void* v_pool, int64_t num_slots, int64_t r
   return cudaGetLastError() == cudaSuccess ? NP_OK : NP_ERR_CUDA;
 }
 
-// One warp per (row, query head).  L = max_s lse_s; out = sum_s e^(lse_s-L)
-// o_s / sum_s e^(lse_s-L) over the splits with finite lse; zeros if none.
-// Lane l owns dims {4l + 128k}; head_dim <= 256.
+// One CTA of 4 warps per (row, query head).  L = max_s lse_s; out =
+// sum_s e^(lse_s-L) o_s / sum_s e^(lse_s-L) over the splits with finite lse;
+// zeros if none.  Warp w takes splits w, w+4, ...; its loads are unrolled
+// and unconditional (an empty split's o is masked by a select, never
+// multiplied), so many rows are in flight at once.  Lane l owns dims
+// {4l + 128k}; head_dim <= 256.
+constexpr int kReduceWarps = 4;
+constexpr int kReduceUnroll = 4;
+
 template <typename TO>
-__global__ void __launch_bounds__(128) lse_reduce_kernel(TO* __restrict__ out,
-                                                         const float* __restrict__ ws_o,
-                                                         const float* __restrict__ ws_lse,
-                                                         int64_t units, int32_t num_splits,
-                                                         int32_t head_dim) {
+__global__ void __launch_bounds__(32 * kReduceWarps) lse_reduce_kernel(
+    TO* __restrict__ out, const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
+    int32_t num_splits, int32_t head_dim) {
   constexpr unsigned FULL = 0xffffffffu;
-  const int64_t u = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  __shared__ float part[kReduceWarps][2][128 + 4];
+  __shared__ float wpart[kReduceWarps];
+  const int64_t u = blockIdx.x;
+  const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (u >= units) return;
   const float* lse = ws_lse + u * num_splits;
   float big = -INFINITY;
-  for (int s = lane; s < num_splits; s += 32) big = fmaxf(big, lse[s]);
+  int last = -1;  // the last split holding tokens
+  for (int s = lane; s < num_splits; s += 32) {
+    const float ls = lse[s];
+    big = fmaxf(big, ls);
+    if (ls != -INFINITY) last = s;
+  }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) big = fmaxf(big, __shfl_xor_sync(FULL, big, off));
+  for (int off = 16; off > 0; off >>= 1) {
+    big = fmaxf(big, __shfl_xor_sync(FULL, big, off));
+    last = max(last, __shfl_xor_sync(FULL, last, off));
+  }
+  const int nsplit = last + 1;  // splits past it are empty: never loaded
 
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   float wsum = 0.f;
+  const bool k0 = 4 * lane < head_dim, k1 = 4 * lane + 128 < head_dim;
   if (big != -INFINITY) {
-    for (int s = 0; s < num_splits; ++s) {
-      const float ls = lse[s];
-      if (ls == -INFINITY) continue;
-      const float w = expf(ls - big);
-      wsum += w;
-      const float* o = ws_o + (u * num_splits + s) * head_dim;
+    const float* ob = ws_o + u * num_splits * (int64_t)head_dim + 4 * lane;
+    for (int s0 = warp; s0 < nsplit; s0 += kReduceWarps * kReduceUnroll) {
+      float w[kReduceUnroll];
+      float4 v0[kReduceUnroll], v1[kReduceUnroll];
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int d = 4 * lane + 128 * k;
-        if (d < head_dim) {
-          const float4 v = *reinterpret_cast<const float4*>(o + d);
-          acc[k][0] = fmaf(w, v.x, acc[k][0]);
-          acc[k][1] = fmaf(w, v.y, acc[k][1]);
-          acc[k][2] = fmaf(w, v.z, acc[k][2]);
-          acc[k][3] = fmaf(w, v.w, acc[k][3]);
-        }
+      for (int i = 0; i < kReduceUnroll; ++i) {
+        const int s = s0 + i * kReduceWarps;
+        const bool in = s < nsplit;
+        const float ls = in ? lse[s] : -INFINITY;
+        w[i] = (ls == -INFINITY) ? 0.f : expf(ls - big);
+        const float* o = ob + (int64_t)(in ? s : 0) * head_dim;
+        v0[i] = k0 ? *reinterpret_cast<const float4*>(o) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v1[i] = k1 ? *reinterpret_cast<const float4*>(o + 128) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int i = 0; i < kReduceUnroll; ++i) {
+        const bool use = w[i] > 0.f;
+        wsum += w[i];
+        acc[0][0] += use ? w[i] * v0[i].x : 0.f;
+        acc[0][1] += use ? w[i] * v0[i].y : 0.f;
+        acc[0][2] += use ? w[i] * v0[i].z : 0.f;
+        acc[0][3] += use ? w[i] * v0[i].w : 0.f;
+        acc[1][0] += use ? w[i] * v1[i].x : 0.f;
+        acc[1][1] += use ? w[i] * v1[i].y : 0.f;
+        acc[1][2] += use ? w[i] * v1[i].z : 0.f;
+        acc[1][3] += use ? w[i] * v1[i].w : 0.f;
       }
     }
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) part[warp][k][4 * lane + e] = acc[k][e];
+  if (lane == 0) wpart[warp] = wsum;
+  __syncthreads();
+  if (warp != 0) return;
+  float tot = 0.f;
+#pragma unroll
+  for (int w2 = 0; w2 < kReduceWarps; ++w2) tot += wpart[w2];
+  const float inv = tot > 0.f ? 1.f / tot : 0.f;
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const int d = 4 * lane + 128 * k;
     if (d < head_dim) {
-      float x[4] = {acc[k][0] * inv, acc[k][1] * inv, acc[k][2] * inv, acc[k][3] * inv};
+      float x[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float a = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < kReduceWarps; ++w2) a += part[w2][k][4 * lane + e];
+        x[e] = a * inv;
+      }
       Storage<TO>::template store<4>(out + u * head_dim + d, x);
     }
   }
@@ -101,13 +144,13 @@ np_status launch_reduce(void* out, np_dtype out_dtype, const float* ws_o, const 
                         cudaStream_t s) {
   const int64_t units = (int64_t)rows * q_heads;
   if (units == 0) return NP_OK;
-  const int64_t blocks = (units + 3) / 4;
+  if (units > 0x7fffffffll) return NP_ERR_UNSUPPORTED;
   if (out_dtype == NP_BF16)
-    lse_reduce_kernel<__nv_bfloat16><<<(unsigned)blocks, 128, 0, s>>>(
-        static_cast<__nv_bfloat16*>(out), ws_o, ws_lse, units, num_splits, head_dim);
+    lse_reduce_kernel<__nv_bfloat16><<<(unsigned)units, 32 * kReduceWarps, 0, s>>>(
+        static_cast<__nv_bfloat16*>(out), ws_o, ws_lse, num_splits, head_dim);
   else
-    lse_reduce_kernel<float><<<(unsigned)blocks, 128, 0, s>>>(static_cast<float*>(out), ws_o,
-                                                              ws_lse, units, num_splits, head_dim);
+    lse_reduce_kernel<float><<<(unsigned)units, 32 * kReduceWarps, 0, s>>>(
+        static_cast<float*>(out), ws_o, ws_lse, num_splits, head_dim);
   return cudaGetLastError() == cudaSuccess ? NP_OK : NP_ERR_CUDA;
 }
 
