@@ -194,6 +194,46 @@ np_status np_paged_decode_reduce(void* out, np_dtype out_dtype,
                                  int32_t head_dim, int32_t num_splits,
                                  np_stream_t stream);
 
+/*
+ * np_paged_decode_noalloc -- np_paged_decode followed by
+ * np_paged_decode_reduce, for callers that cannot allocate device memory.
+ * The pages have no counterpart to this call; it exists for callers that
+ * are handed their inputs, outputs and a stream and nothing else -- a host
+ * framework calling this library as a plugin without exposing its
+ * allocator, or a serving loop that must not allocate once it is running
+ * (cudaMalloc can synchronise the device and can fail under memory
+ * pressure).  Such callers cannot provide the split workspace, so this
+ * call keeps the split partials in a fixed array compiled into the library:
+ * NP_NOALLOC_SCRATCH_BYTES of device memory that every GPU loading the
+ * library holds until the process exits.
+ *
+ * Arguments, layouts and errors are those of np_paged_decode, with `out`
+ * always written and no workspace.  It allocates and frees nothing.
+ *   - Returns NP_ERR_WORKSPACE, before anything is enqueued, when the
+ *     partials, np_paged_decode_workspace_bytes(rows, q_heads, head_dim,
+ *     num_splits), exceed NP_NOALLOC_SCRATCH_BYTES; a smaller num_splits
+ *     fits.  num_splits <= 1 uses no scratch at all.
+ *   - The first call on a device looks up the array's device address for
+ *     that device (cudaGetSymbolAddress); make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array, which keeps the last
+ *     call's contents (nothing in it needs to start zeroed).  Calls whose
+ *     execution overlaps on the GPU (different streams, or overlapping
+ *     graph launches) race on it: order them on one stream.
+ */
+#define NP_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB per device */
+
+np_status np_paged_decode_noalloc(void* out, const void* q, const void* k_pool,
+                                  const void* v_pool, np_dtype dtype,
+                                  int64_t num_blocks, int32_t block_size,
+                                  int32_t kv_heads, int32_t head_dim,
+                                  const int32_t* block_tables,
+                                  int32_t max_blocks_per_row,
+                                  const int32_t* context_lens, int32_t rows,
+                                  int32_t q_heads, float scale,
+                                  int32_t num_splits, int32_t* err_word,
+                                  np_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

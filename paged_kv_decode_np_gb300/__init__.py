@@ -31,6 +31,7 @@ __all__ = [
     "load", "NPError", "np_abi_version", "np_status_string", "np_kv_append",
     "np_paged_decode_plan", "np_paged_decode_split_len",
     "np_paged_decode_workspace_bytes", "np_paged_decode", "np_paged_decode_reduce",
+    "np_paged_decode_noalloc", "NP_NOALLOC_SCRATCH_BYTES",
     "workspace", "decode_step", "NP_OK", "NP_ERR_INVALID_ARG", "NP_ERR_UNSUPPORTED",
     "NP_ERR_WORKSPACE", "NP_ERR_OUT_OF_RANGE", "NP_ERR_CUDA", "NP_F32", "NP_BF16",
     "NP_FLAG_BLOCK_ID", "NP_FLAG_CONTEXT", "NP_FLAG_SLOT", "NP_FLAG_TIMEOUT",
@@ -50,6 +51,8 @@ NP_FLAG_BLOCK_ID = 0x1
 NP_FLAG_CONTEXT = 0x2
 NP_FLAG_SLOT = 0x4
 NP_FLAG_TIMEOUT = 0x8
+
+NP_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libnp_paged.so")
@@ -95,6 +98,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.np_paged_decode.argtypes = [_P, _P, _P, _P, ctypes.c_int, _I64, _I32, _I32, _I32, _P,
                                     _I32, _P, _I32, _I32, ctypes.c_float, _I32, _P,
                                     ctypes.c_size_t, _P, _P]
+    lib.np_paged_decode_noalloc.restype = ctypes.c_int
+    lib.np_paged_decode_noalloc.argtypes = [_P, _P, _P, _P, ctypes.c_int, _I64, _I32, _I32, _I32,
+                                            _P, _I32, _P, _I32, _I32, ctypes.c_float, _I32, _P,
+                                            _P]
     lib.np_paged_decode_reduce.restype = ctypes.c_int
     lib.np_paged_decode_reduce.argtypes = [_P, ctypes.c_int, _P, ctypes.c_size_t, _I32, _I32,
                                            _I32, _I32, _P]
@@ -222,6 +229,29 @@ def np_paged_decode_reduce(out, workspace, num_splits: int, stream=None):
         _dev(out, "out"), _dtype_code(out.dtype), _dev(workspace, "workspace"), ws_bytes, rows,
         q_heads, d, num_splits, _stream(stream))
     _check(st, "np_paged_decode_reduce")
+
+
+def np_paged_decode_noalloc(out, q, k_pool, v_pool, block_tables, context_lens, scale,
+                            num_splits: int = 1, err_word=None, stream=None):
+    """The read plus the split merge with no workspace argument: for callers
+    that cannot allocate device memory, the split partials go to a fixed
+    NP_NOALLOC_SCRATCH_BYTES array inside the library (see np_paged.h)."""
+    rows, q_heads, d = q.shape
+    nb, bs, hk, d2 = k_pool.shape
+    if d2 != d or v_pool.shape != k_pool.shape or q.dtype != k_pool.dtype or \
+            v_pool.dtype != k_pool.dtype or out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("np_paged_decode_noalloc: q/out/pool shape or dtype mismatch")
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or \
+            block_tables.shape[0] != rows:
+        raise ValueError("np_paged_decode_noalloc: block_tables must be int32 [rows, max_blocks]")
+    if context_lens.dtype != torch.int32 or context_lens.shape != (rows,):
+        raise ValueError("np_paged_decode_noalloc: context_lens must be int32 [rows]")
+    st = load().np_paged_decode_noalloc(
+        _dev(out, "out"), _dev(q, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+        _dtype_code(q.dtype), nb, bs, hk, d, _dev(block_tables, "block_tables"),
+        block_tables.shape[1], _dev(context_lens, "context_lens"), rows, q_heads,
+        float(scale), num_splits, _opt(err_word, "err_word"), _stream(stream))
+    _check(st, "np_paged_decode_noalloc")
 
 
 def decode_step(out, q, k_pool, v_pool, block_tables, context_lens, scale, *, k_new=None,

@@ -36,6 +36,7 @@ def _units(extra: list[str], build_dir: str, csrc: str) -> list[tuple[str, str, 
     units = [
         (os.path.join(csrc, "api.cu"), os.path.join(objdir, "api.o"), []),
         (os.path.join(csrc, "append_reduce.cu"), os.path.join(objdir, "append_reduce.o"), []),
+        (os.path.join(csrc, "noalloc.cu"), os.path.join(objdir, "noalloc.o"), []),
     ]
     for bf16 in (0, 1):
         for d in HEAD_DIMS:
