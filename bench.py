@@ -110,7 +110,8 @@ class ClockSampler:
         except Exception:
             pass
         self.proc = None
-        self.lines: list[str] = []
+        self.lines: list[tuple[float, str]] = []
+        self.window = None
 
     def __enter__(self):
         try:
@@ -127,7 +128,11 @@ class ClockSampler:
 
     def _read(self):
         for ln in self.proc.stdout:
-            self.lines.append(ln.strip())
+            self.lines.append((time.time(), ln.strip()))
+
+    def mark(self, start: float, end: float) -> None:
+        """The host wall-clock window of the timed region."""
+        self.window = (start, end)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -142,7 +147,11 @@ class ClockSampler:
     def summary(self) -> dict:
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines = self.lines
+        if self.window is not None:  # samples taken while the timed steps ran
+            inside = [x for x in lines if self.window[0] <= x[0] <= self.window[1] + 0.05]
+            lines = inside or lines
+        for _, ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -157,7 +166,8 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "in_timed_region": self.window is not None and lines is not self.lines}
 
 
 # ------------------------------------------------------------ distributed --
@@ -314,6 +324,7 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
     with ClockSampler(dev) as clk:
         barrier(dist)
         torch.cuda.synchronize()
+        wall0 = time.time()
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
@@ -325,6 +336,7 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
             st_ev[i][1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
+        clk.mark(wall0, time.time())
         barrier(dist)
     if flush is None:
         elapsed_ms = t_start.elapsed_time(t_end)
@@ -402,7 +414,9 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
             "parallelism": f"replicas x{world} (rows independent, no collective)",
         },
         "roofline": {
-            "bound": "hbm", "kernel": "paged_decode_kernel", "achieved": achieved,
+            "bound": "hbm",
+            "kernel": "paged_decode_mma_kernel" if w.dtype == "bf16" else "paged_decode_kernel",
+            "achieved": achieved,
             "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
             if peak_kind == "measured" else "fallback 6.8 TB/s",
             "unit": "GB/s", "frac": achieved / peak,
@@ -427,7 +441,7 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
