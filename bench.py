@@ -51,8 +51,9 @@ def algorithmic_bytes(w: wl.Workload, md: wl.Metadata) -> dict:
 
     decode: every history token's K and V rows once, q once, out once, the
     table entries the walk needs once, the context lengths once (the split
-    partials are not algorithmic: they are this implementation's overhead).
-    append: the new tokens' K/V read once and written once, plus slots.
+    partials are not algorithmic: they are this implementation's overhead),
+    plus the fused append: the new tokens' K/V read once and written once and
+    their slots.
     """
     cl = md.context_lens.to(torch.int64)
     es = w.elem_size
@@ -60,7 +61,7 @@ def algorithmic_bytes(w: wl.Workload, md: wl.Metadata) -> dict:
     qo = 2 * w.rows * w.q_heads * w.head_dim * es
     tab = int(((cl + w.block_size - 1) // w.block_size).sum()) * 4 + 4 * w.rows
     app = 2 * 2 * w.rows * w.kv_heads * w.head_dim * es + 8 * w.rows
-    return {"kv": kv, "decode": kv + qo + tab, "append": app}
+    return {"kv": kv, "decode": kv + qo + tab + app, "append": app}
 
 
 def measured_peak() -> tuple[float, str]:
@@ -292,13 +293,13 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
     def step(rec=None):
+        # append fused into the read's launch, then the split merge
         launches = 0
-        npg.np_kv_append(inp.k_pool, inp.v_pool, inp.k_new, inp.v_new, sm, err, stream)
-        launches += 1
         if rec is not None:
             rec[0].record(stream)
-        npg.np_paged_decode(out if S == 1 else None, inp.q, inp.k_pool, inp.v_pool, bt, cl,
-                            w.softmax_scale, S, ws, err, stream)
+        npg.np_paged_append_decode(out if S == 1 else None, inp.q, inp.k_new, inp.v_new, sm,
+                                   inp.k_pool, inp.v_pool, bt, cl, w.softmax_scale, S, ws, err,
+                                   stream)
         if rec is not None:
             rec[1].record(stream)
         launches += 1
@@ -357,10 +358,9 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
     def e2e_step():
         for k in pin:
             dbuf[k].copy_(pin[k], non_blocking=True)
-        npg.np_kv_append(inp.k_pool, inp.v_pool, dbuf["k_new"], dbuf["v_new"], dbuf["sm"], err,
-                         stream)
-        npg.np_paged_decode(out if S == 1 else None, dbuf["q"], inp.k_pool, inp.v_pool,
-                            dbuf["bt"], dbuf["cl"], w.softmax_scale, S, ws, err, stream)
+        npg.np_paged_append_decode(out if S == 1 else None, dbuf["q"], dbuf["k_new"],
+                                   dbuf["v_new"], dbuf["sm"], inp.k_pool, inp.v_pool,
+                                   dbuf["bt"], dbuf["cl"], w.softmax_scale, S, ws, err, stream)
         if S > 1:
             npg.np_paged_decode_reduce(out, ws, S, stream)
         out_host.copy_(out, non_blocking=True)

@@ -80,8 +80,10 @@ typedef enum np_dtype { NP_F32 = 0, NP_BF16 = 1 } np_dtype;
                                 [0, num_blocks); block 0 was read instead */
 #define NP_FLAG_CONTEXT 0x2  /* context_lens[r] < 0 or > max_blocks_per_row *
                                 block_size; clamped into that range */
-#define NP_FLAG_SLOT 0x4     /* an append slot >= num_blocks * block_size;
-                                that token was not written */
+#define NP_FLAG_SLOT 0x4     /* an append slot >= num_blocks * block_size, or
+                                (np_paged_append_decode) not the slot of the
+                                row's newest position; that token was not
+                                written */
 #define NP_FLAG_TIMEOUT 0x8  /* an internal pipeline wait gave up (never
                                 expected; the output of that block is wrong) */
 
@@ -178,6 +180,33 @@ np_status np_paged_decode(void* out, const void* q, const void* k_pool,
                           int32_t q_heads, float scale, int32_t num_splits,
                           void* workspace, size_t workspace_bytes,
                           int32_t* err_word, np_stream_t stream);
+
+/*
+ * np_paged_append_decode -- np_kv_append of one new token per row followed
+ * by np_paged_decode, in ONE kernel launch (same results, bit for bit in
+ * the pools).  Row r's new K and V rows (k_new/v_new [rows, kv_heads,
+ * head_dim]) go to pool slot slot_mapping[r], which must be the slot of the
+ * row's newest position, context_lens[r] - 1, under its block table (the
+ * usual decode step: append, then read the whole history); a negative entry
+ * means "no new token for this row".  The thread block whose split holds
+ * that position writes the token before it reads it.  An entry that names
+ * any other slot is not written and is flagged (NP_FLAG_SLOT) -- use
+ * np_kv_append + np_paged_decode for arbitrary slots.  Other arguments,
+ * layouts and errors as np_paged_decode; with num_splits > 1, call
+ * np_paged_decode_reduce next.
+ */
+np_status np_paged_append_decode(void* out, const void* q, const void* k_new,
+                                 const void* v_new, const int64_t* slot_mapping,
+                                 void* k_pool, void* v_pool, np_dtype dtype,
+                                 int64_t num_blocks, int32_t block_size,
+                                 int32_t kv_heads, int32_t head_dim,
+                                 const int32_t* block_tables,
+                                 int32_t max_blocks_per_row,
+                                 const int32_t* context_lens, int32_t rows,
+                                 int32_t q_heads, float scale,
+                                 int32_t num_splits, void* workspace,
+                                 size_t workspace_bytes, int32_t* err_word,
+                                 np_stream_t stream);
 
 /*
  * np_paged_decode_reduce -- merge split partials into out.

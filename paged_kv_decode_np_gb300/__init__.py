@@ -31,7 +31,7 @@ __all__ = [
     "load", "NPError", "np_abi_version", "np_status_string", "np_kv_append",
     "np_paged_decode_plan", "np_paged_decode_split_len",
     "np_paged_decode_workspace_bytes", "np_paged_decode", "np_paged_decode_reduce",
-    "np_paged_decode_noalloc", "NP_NOALLOC_SCRATCH_BYTES",
+    "np_paged_decode_noalloc", "NP_NOALLOC_SCRATCH_BYTES", "np_paged_append_decode",
     "workspace", "decode_step", "NP_OK", "NP_ERR_INVALID_ARG", "NP_ERR_UNSUPPORTED",
     "NP_ERR_WORKSPACE", "NP_ERR_OUT_OF_RANGE", "NP_ERR_CUDA", "NP_F32", "NP_BF16",
     "NP_FLAG_BLOCK_ID", "NP_FLAG_CONTEXT", "NP_FLAG_SLOT", "NP_FLAG_TIMEOUT",
@@ -98,6 +98,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.np_paged_decode.argtypes = [_P, _P, _P, _P, ctypes.c_int, _I64, _I32, _I32, _I32, _P,
                                     _I32, _P, _I32, _I32, ctypes.c_float, _I32, _P,
                                     ctypes.c_size_t, _P, _P]
+    lib.np_paged_append_decode.restype = ctypes.c_int
+    lib.np_paged_append_decode.argtypes = [_P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _I64, _I32,
+                                           _I32, _I32, _P, _I32, _P, _I32, _I32, ctypes.c_float,
+                                           _I32, _P, ctypes.c_size_t, _P, _P]
     lib.np_paged_decode_noalloc.restype = ctypes.c_int
     lib.np_paged_decode_noalloc.argtypes = [_P, _P, _P, _P, ctypes.c_int, _I64, _I32, _I32, _I32,
                                             _P, _I32, _P, _I32, _I32, ctypes.c_float, _I32, _P,
@@ -221,6 +225,39 @@ def np_paged_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale,
     _check(st, "np_paged_decode")
 
 
+def np_paged_append_decode(out, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables,
+                           context_lens, scale, num_splits: int = 1, workspace=None,
+                           err_word=None, stream=None):
+    """Append each row's new token (at its newest position) and read, in one launch."""
+    rows, q_heads, d = q.shape
+    nb, bs, hk, d2 = k_pool.shape
+    if d2 != d or v_pool.shape != k_pool.shape or q.dtype != k_pool.dtype or \
+            v_pool.dtype != k_pool.dtype:
+        raise ValueError("np_paged_append_decode: q/pool shape or dtype mismatch")
+    if k_new.shape != (rows, hk, d) or v_new.shape != k_new.shape or \
+            k_new.dtype != k_pool.dtype or v_new.dtype != k_pool.dtype:
+        raise ValueError("np_paged_append_decode: k_new/v_new must be [rows, kv_heads, head_dim]")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.shape != (rows,):
+        raise ValueError("np_paged_append_decode: slot_mapping must be int64 [rows]")
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or \
+            block_tables.shape[0] != rows:
+        raise ValueError("np_paged_append_decode: block_tables must be int32 [rows, max_blocks]")
+    if context_lens.dtype != torch.int32 or context_lens.shape != (rows,):
+        raise ValueError("np_paged_append_decode: context_lens must be int32 [rows]")
+    if out is not None and (out.shape != q.shape or out.dtype != q.dtype):
+        raise ValueError("np_paged_append_decode: out must match q")
+    ws_ptr = _opt(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().np_paged_append_decode(
+        _opt(out, "out"), _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+        _dev(slot_mapping, "slot_mapping"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+        _dtype_code(q.dtype), nb, bs, hk, d, _dev(block_tables, "block_tables"),
+        block_tables.shape[1], _dev(context_lens, "context_lens"), rows, q_heads,
+        float(scale), num_splits, ws_ptr, ws_bytes, _opt(err_word, "err_word"),
+        _stream(stream))
+    _check(st, "np_paged_append_decode")
+
+
 def np_paged_decode_reduce(out, workspace, num_splits: int, stream=None):
     """Merge split partials in ``workspace`` into ``out`` [rows, q_heads, head_dim]."""
     rows, q_heads, d = out.shape
@@ -256,18 +293,26 @@ def np_paged_decode_noalloc(out, q, k_pool, v_pool, block_tables, context_lens, 
 
 def decode_step(out, q, k_pool, v_pool, block_tables, context_lens, scale, *, k_new=None,
                 v_new=None, slot_mapping=None, num_splits: int = 1, workspace=None,
-                err_word=None, stream=None) -> int:
+                err_word=None, stream=None, fused: bool = True) -> int:
     """One decode step: append (if new K/V given), read, reduce (if split).
 
-    Returns the number of library kernels launched.
+    With ``fused`` (the default) and one new token per row, the append runs
+    inside the read's launch (np_paged_append_decode); otherwise
+    np_kv_append runs first.  Returns the number of library kernels launched.
     """
     launches = 0
-    if k_new is not None:
-        np_kv_append(k_pool, v_pool, k_new, v_new, slot_mapping, err_word, stream)
-        launches += 1 if k_new.shape[0] > 0 else 0
-    np_paged_decode(out if num_splits == 1 else None, q, k_pool, v_pool, block_tables,
-                    context_lens, scale, num_splits, workspace, err_word, stream)
-    launches += 1 if q.shape[0] > 0 else 0
+    o = out if num_splits == 1 else None
+    if k_new is not None and fused and k_new.shape[0] == q.shape[0]:
+        np_paged_append_decode(o, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables,
+                               context_lens, scale, num_splits, workspace, err_word, stream)
+        launches += 1 if q.shape[0] > 0 else 0
+    else:
+        if k_new is not None:
+            np_kv_append(k_pool, v_pool, k_new, v_new, slot_mapping, err_word, stream)
+            launches += 1 if k_new.shape[0] > 0 else 0
+        np_paged_decode(o, q, k_pool, v_pool, block_tables, context_lens, scale, num_splits,
+                        workspace, err_word, stream)
+        launches += 1 if q.shape[0] > 0 else 0
     if num_splits > 1:
         np_paged_decode_reduce(out, workspace, num_splits, stream)
         launches += 1 if q.shape[0] > 0 else 0

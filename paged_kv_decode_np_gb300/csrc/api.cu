@@ -274,12 +274,18 @@ size_t np_paged_decode_workspace_bytes(int32_t rows, int32_t q_heads, int32_t he
   return round_up(units * head_dim * sizeof(float), 256) + round_up(units * sizeof(float), 256);
 }
 
-np_status np_paged_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
-                          np_dtype dtype, int64_t num_blocks, int32_t block_size,
-                          int32_t kv_heads, int32_t head_dim, const int32_t* block_tables,
-                          int32_t max_blocks_per_row, const int32_t* context_lens, int32_t rows,
-                          int32_t q_heads, float scale, int32_t num_splits, void* workspace,
-                          size_t workspace_bytes, int32_t* err_word, np_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The read, optionally with the fused append (k_new/v_new/slot_mapping non-null).
+np_status decode_impl(void* out, const void* q, const void* k_pool, const void* v_pool,
+                      np_dtype dtype, int64_t num_blocks, int32_t block_size, int32_t kv_heads,
+                      int32_t head_dim, const int32_t* block_tables, int32_t max_blocks_per_row,
+                      const int32_t* context_lens, int32_t rows, int32_t q_heads, float scale,
+                      int32_t num_splits, void* workspace, size_t workspace_bytes,
+                      int32_t* err_word, np_stream_t stream, const void* k_new,
+                      const void* v_new, const int64_t* slot_mapping) {
   const int es = elem_size(dtype);
   if (es == 0) return NP_ERR_UNSUPPORTED;
   if (rows < 0 || q_heads <= 0 || kv_heads <= 0 || q_heads % kv_heads != 0 ||
@@ -338,6 +344,9 @@ np_status np_paged_decode(void* out, const void* q, const void* k_pool, const vo
   p.num_splits = num_splits;
   p.stages = 0;
   p.qscale = scale * 1.4426950408889634f;  // log2(e)
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.slot_mapping = slot_mapping;
   // bf16 pools with head_dim a multiple of 64 stage K/V through tiled TMA
   // boxes of box_tokens tokens: the largest power of two <= 16 dividing the
   // block size, with box_tokens * head_group a multiple of 8 (each box then
@@ -368,6 +377,41 @@ np_status np_paged_decode(void* out, const void* q, const void* k_pool, const vo
   npk::DecodeLauncher fn = launcher_for(dtype, head_dim);
   if (!fn) return NP_ERR_UNSUPPORTED;
   return fn(L, p);
+}
+
+}  // namespace
+
+extern "C" {
+
+np_status np_paged_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                          np_dtype dtype, int64_t num_blocks, int32_t block_size,
+                          int32_t kv_heads, int32_t head_dim, const int32_t* block_tables,
+                          int32_t max_blocks_per_row, const int32_t* context_lens, int32_t rows,
+                          int32_t q_heads, float scale, int32_t num_splits, void* workspace,
+                          size_t workspace_bytes, int32_t* err_word, np_stream_t stream) {
+  return decode_impl(out, q, k_pool, v_pool, dtype, num_blocks, block_size, kv_heads, head_dim,
+                     block_tables, max_blocks_per_row, context_lens, rows, q_heads, scale,
+                     num_splits, workspace, workspace_bytes, err_word, stream, nullptr, nullptr,
+                     nullptr);
+}
+
+np_status np_paged_append_decode(void* out, const void* q, const void* k_new, const void* v_new,
+                                 const int64_t* slot_mapping, void* k_pool, void* v_pool,
+                                 np_dtype dtype, int64_t num_blocks, int32_t block_size,
+                                 int32_t kv_heads, int32_t head_dim,
+                                 const int32_t* block_tables, int32_t max_blocks_per_row,
+                                 const int32_t* context_lens, int32_t rows, int32_t q_heads,
+                                 float scale, int32_t num_splits, void* workspace,
+                                 size_t workspace_bytes, int32_t* err_word, np_stream_t stream) {
+  if (rows > 0) {
+    if (!k_new || !v_new || !slot_mapping) return NP_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8))
+      return NP_ERR_INVALID_ARG;
+  }
+  return decode_impl(out, q, k_pool, v_pool, dtype, num_blocks, block_size, kv_heads, head_dim,
+                     block_tables, max_blocks_per_row, context_lens, rows, q_heads, scale,
+                     num_splits, workspace, workspace_bytes, err_word, stream, k_new, v_new,
+                     slot_mapping);
 }
 
 np_status np_paged_decode_reduce(void* out, np_dtype out_dtype, const void* workspace,

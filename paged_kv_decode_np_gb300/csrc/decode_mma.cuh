@@ -136,6 +136,8 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
   const int64_t t0 = (int64_t)split * p.split_len;
   const int64_t t1 = min(t0 + p.split_len, c);
 
+  fused_append<D, 2>(p, r, hgi, HG, c, t0, t1);
+
   if (t0 >= t1) {
     if (p.num_splits > 1) {
       for (int i = threadIdx.x; i < HG * G; i += blockDim.x)

@@ -9,7 +9,7 @@ import workloads as wl
 
 
 def gpu_step(npg, inp: wl.Inputs, num_splits: int | None = None, append: bool = True,
-             err: torch.Tensor | None = None, stream=None):
+             err: torch.Tensor | None = None, stream=None, fused: bool = True):
     """Append + read (+ reduce) with the library; returns (out, num_splits, workspace)."""
     w = inp.w
     dev = inp.q.device
@@ -23,7 +23,8 @@ def gpu_step(npg, inp: wl.Inputs, num_splits: int | None = None, append: bool = 
     out = torch.full_like(inp.q, float("nan"))
     kw = dict(k_new=inp.k_new, v_new=inp.v_new, slot_mapping=sm) if append else {}
     npg.decode_step(out, inp.q, inp.k_pool, inp.v_pool, bt, cl, w.softmax_scale,
-                    num_splits=num_splits, workspace=ws, err_word=err, stream=stream, **kw)
+                    num_splits=num_splits, workspace=ws, err_word=err, stream=stream,
+                    fused=fused, **kw)
     torch.cuda.synchronize()
     return out, num_splits, ws
 

@@ -28,14 +28,22 @@ def _custom(contexts, q_heads, kv_heads, head_dim, block_size, dtype, seed=11, s
                        seed=seed, scale=scale)
 
 
-def _full_parity(npg, w, num_splits=None, append=True, device=DEV):
+def _full_parity(npg, w, num_splits=None, append=True, device=DEV, fused=True):
+    """The step (append + read [+ reduce]) against the oracle; by default the
+    append runs fused in the read's launch, fused=False uses np_kv_append.
+    The pools after the step must equal the oracle's append bit for bit."""
     inp = wl.make_inputs(w, device="cpu")
     host = wl.full_host(inp)
     dinp = wl.Inputs(w, inp.md, *(t.to(device) for t in
                                   (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new)))
-    out, s, _ = gpu_step(npg, dinp, num_splits=num_splits, append=append)
+    out, s, _ = gpu_step(npg, dinp, num_splits=num_splits, append=append, fused=fused)
     ref, _ = oracle_step(host, w.softmax_scale, append=append)
-    return assert_parity(out, ref, w.dtype, f"{w.name} splits={s}"), s
+    if append:
+        rk, rv = host["k_pool"].copy(), host["v_pool"].copy()
+        oracle.kv_append(rk, rv, host["k_new"], host["v_new"], host["slot_mapping"])
+        assert wl.host_array(dinp.k_pool).tobytes() == rk.tobytes(), "K pool after the step"
+        assert wl.host_array(dinp.v_pool).tobytes() == rv.tobytes(), "V pool after the step"
+    return assert_parity(out, ref, w.dtype, f"{w.name} splits={s} fused={fused}"), s
 
 
 # ------------------------------------------------------------------ golden --
@@ -83,11 +91,12 @@ def test_golden_append_then_read(nplib):
 
 
 # --------------------------------------------------------- the workloads ---
+@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("name", ["tiny-fp32", "llama-fp32"])
-def test_workload_full_parity(nplib, name):
+def test_workload_full_parity(nplib, name, fused):
     w = wl.WORKLOADS[name]
-    _full_parity(nplib, w)
-    _full_parity(nplib, w, num_splits=1)
+    _full_parity(nplib, w, fused=fused)
+    _full_parity(nplib, w, num_splits=1, fused=fused)
 
 
 @pytest.mark.parametrize("name,sample", [
@@ -97,6 +106,15 @@ def test_workload_full_size_sampled_rows(nplib, name, sample):
 
     The sampled rows always include the longest and the shortest context.
     """
+    _sampled_rows(nplib, name, sample, fused=True)
+
+
+@pytest.mark.parametrize("name", ["bf16-long", "bf16-ragged-bs8"])
+def test_workload_full_size_unfused_append(nplib, name):
+    _sampled_rows(nplib, name, 4, fused=False)
+
+
+def _sampled_rows(nplib, name, sample, fused):
     w = wl.WORKLOADS[name]
     inp = wl.make_inputs(w, device=DEV)
     cl = inp.context_lens
@@ -109,10 +127,10 @@ def test_workload_full_size_sampled_rows(nplib, name, sample):
     rows = sorted(rows)
     host = wl.row_subproblem(inp, rows)          # copied before any kernel runs
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    out, s, _ = gpu_step(nplib, inp, err=err)
+    out, s, _ = gpu_step(nplib, inp, err=err, fused=fused)
     assert int(err.item()) == 0
     ref, _ = oracle_step(host, w.softmax_scale)
-    assert_parity(out[rows], ref, w.dtype, f"{name} rows={rows} splits={s}")
+    assert_parity(out[rows], ref, w.dtype, f"{name} rows={rows} splits={s} fused={fused}")
     assert torch.isfinite(out.float()).all()
 
 
@@ -243,6 +261,7 @@ def test_block_sizes(nplib, block_size):
     w = _custom([1, 31, 32, 33, 255, 513], 8, 2, 128, block_size, "f32", seed=30 + block_size)
     _full_parity(nplib, w)
     _full_parity(nplib, w, num_splits=5)
+    _full_parity(nplib, w, num_splits=5, fused=False)
 
 
 @pytest.mark.parametrize("kv_heads", [1, 8])
@@ -255,6 +274,7 @@ def test_block_sizes_bf16(nplib, block_size, kv_heads):
                 seed=70 + block_size + kv_heads)
     _full_parity(nplib, w)
     _full_parity(nplib, w, num_splits=3)
+    _full_parity(nplib, w, num_splits=3, fused=False)
 
 
 def test_edge_contexts(nplib):
@@ -279,6 +299,36 @@ def test_zero_context_gives_zeros_and_single_token_gives_v(nplib):
         assert np.all(o[0] == 0)
         vnew = to64(inp.v_new)                       # the only token is the new one
         np.testing.assert_array_equal(o[1], np.repeat(vnew[1], 4, axis=0))
+
+
+def test_fused_append_refuses_a_slot_that_is_not_the_newest_position(nplib):
+    """A slot-mapping entry that is not where the row's newest position lives
+    is flagged and not written (the row then reads its pool as it was)."""
+    w = _custom([40, 25, 64], 8, 2, 128, 16, "bf16", seed=55)
+    inp = wl.make_inputs(w, poison=False)
+    host = wl.full_host(inp)
+    sm = inp.slot_mapping.clone()
+    sm[1] = int(inp.slot_mapping[0])           # row 0's slot: not row 1's position
+    md = wl.Metadata(inp.context_lens, inp.block_tables, sm, inp.md.num_blocks)
+    d = wl.Inputs(w, md, *(t.to(DEV) for t in
+                           (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new)))
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for s in (1, 4):
+        d.k_pool.copy_(inp.k_pool.to(DEV))
+        d.v_pool.copy_(inp.v_pool.to(DEV))
+        err.zero_()
+        out, _, _ = gpu_step(nplib, d, num_splits=s, err=err)
+        assert int(err.item()) == nplib.NP_FLAG_SLOT
+        keep = np.array([0, 2])
+        h2 = dict(host, slot_mapping=np.array([int(inp.slot_mapping[0]), -1,
+                                               int(inp.slot_mapping[2])], dtype=np.int64))
+        ref, _ = oracle_step(h2, w.softmax_scale)
+        assert_parity(out, ref, "bf16", f"mismatched slot splits={s}")
+        rk = host["k_pool"].copy()
+        rv = host["v_pool"].copy()
+        oracle.kv_append(rk, rv, host["k_new"][keep], host["v_new"][keep],
+                         inp.slot_mapping.numpy()[keep])
+        assert wl.host_array(d.k_pool).tobytes() == rk.tobytes()
 
 
 # ---------------------------------------------------------- robustness ----
