@@ -66,7 +66,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.restype = ctypes.c_int
         fn.argtypes = [_P, _P, _P, _P, _P, ctypes.c_int, _I64, _I32, _I32, _I32,
-                       _P, _I32, _P, _I32, _I32, ctypes.c_double, _I64, _I32]
+                       _P, _I32, _P, _I32, _I32, _I32, ctypes.c_double, _I64, _I32]
     lib.npo_reduce_f64.restype = ctypes.c_int
     lib.npo_reduce_f64.argtypes = [_P, _P, _P, _I32, _I32, _I32, _I32]
     return lib
@@ -93,10 +93,13 @@ def paged_decode(q, k_pool, v_pool, block_tables, context_lens, scale, *,
                  precision: str = "f64", lib: ctypes.CDLL | None = None):
     """Decode read over the paged pool.
 
-    Returns ``(out, lse)``: out [rows, q_heads, head_dim] and lse
-    [rows, q_heads] when ``num_splits == 1``; otherwise the per-split
-    partials out [rows, q_heads, num_splits, head_dim] and lse
-    [rows, q_heads, num_splits], split s covering tokens
+    ``q`` is [rows, q_heads, head_dim] (one query token per row) or
+    [rows, query_len, q_heads, head_dim] (query token i of row r sits at
+    position context_lens[r] - query_len + i and sees the history up to it).
+    Returns ``(out, lse)`` with q's leading shape: out [..., q_heads,
+    head_dim] and lse [..., q_heads] when ``num_splits == 1``; otherwise the
+    per-split partials out [..., q_heads, num_splits, head_dim] and lse
+    [..., q_heads, num_splits], split s covering tokens
     [s * split_len, (s + 1) * split_len).  ``precision`` is "f64" (the primary
     oracle) or "f32".
     """
@@ -107,7 +110,12 @@ def paged_decode(q, k_pool, v_pool, block_tables, context_lens, scale, *,
         raise TypeError("q and both pools must share one dtype")
     bt = _c(block_tables, np.int32)
     cl = _c(context_lens, np.int32)
-    rows, q_heads, head_dim = q.shape
+    multi = q.ndim == 4
+    if multi:
+        rows, query_len, q_heads, head_dim = q.shape
+    else:
+        rows, q_heads, head_dim = q.shape
+        query_len = 1
     num_blocks, block_size, kv_heads, hd2 = k_pool.shape
     if hd2 != head_dim or v_pool.shape != k_pool.shape:
         raise ValueError("pool shape does not match q")
@@ -118,15 +126,17 @@ def paged_decode(q, k_pool, v_pool, block_tables, context_lens, scale, *,
         split_len = max(1, mb * block_size)
     real = np.float64 if precision == "f64" else np.float32
     fn = lib.npo_paged_decode_f64 if precision == "f64" else lib.npo_paged_decode_f32
-    out = np.zeros((rows, q_heads, num_splits, head_dim), dtype=real)
-    lse = np.zeros((rows, q_heads, num_splits), dtype=real)
+    out = np.zeros((rows, query_len, q_heads, num_splits, head_dim), dtype=real)
+    lse = np.zeros((rows, query_len, q_heads, num_splits), dtype=real)
     rc = fn(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_pool), _ptr(v_pool), code,
             num_blocks, block_size, kv_heads, head_dim, _ptr(bt), mb, _ptr(cl),
-            rows, q_heads, float(scale), int(split_len), num_splits)
+            rows, query_len, q_heads, float(scale), int(split_len), num_splits)
     if rc != OK:
         raise OracleError(rc, "paged_decode")
+    if not multi:
+        out, lse = out[:, 0], lse[:, 0]
     if num_splits == 1:
-        return out[:, :, 0, :], lse[:, :, 0]
+        return out[..., 0, :], lse[..., 0]
     return out, lse
 
 

@@ -381,6 +381,77 @@ def check_refusals(lib):
     assert np.all(out[0] == 0) and np.all(lse[0] == -np.inf) and np.isfinite(out[1]).all()
 
 
+def _mq_case(rng, contexts, query_len, q_heads, kv_heads, head_dim, block_size, dtype="f32"):
+    c = _case(rng, contexts, q_heads, kv_heads, head_dim, block_size, dtype)
+    rows = len(contexts)
+    q_st, q64 = _store(rng.standard_normal((rows, query_len, q_heads, head_dim)), dtype)
+    c["q"], c["q64"] = q_st, q64
+    return c
+
+
+def _sdpa_causal(q64_row, hk, hv, scale):
+    """torch SDPA (fp64) of Q query tokens that are the last Q positions of a
+    c-token history: query i may see positions t <= c - Q + i."""
+    qn, c = q64_row.shape[0], hk.shape[0]
+    q = torch.from_numpy(q64_row).permute(1, 0, 2)[None]          # [1, Hq, Q, D]
+    k = torch.from_numpy(hk).permute(1, 0, 2)[None]               # [1, Hk, c, D]
+    v = torch.from_numpy(hv).permute(1, 0, 2)[None]
+    pos = torch.arange(c)[None, :]
+    lim = (c - qn + torch.arange(qn))[:, None]
+    mask = pos <= lim                                             # [Q, c]
+    out = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale, enable_gqa=True)
+    return out[0].permute(1, 0, 2).numpy()                         # [Q, Hq, D]
+
+
+def check_multi_query_sdpa(lib):
+    rng = np.random.default_rng(RNG_SEED + 10)
+    for contexts, qn, hq, hk, d, bs, dt in [
+        ([5, 40, 17], 3, 4, 2, 8, 4, "f32"),
+        ([64, 9], 4, 8, 2, 16, 8, "bf16"),
+        ([33, 100], 2, 10, 2, 8, 16, "f32"),
+    ]:
+        c = _mq_case(rng, contexts, qn, hq, hk, d, bs, dt)
+        out, lse = _run(lib, c)
+        assert out.shape == (len(contexts), qn, hq, d)
+        for r in range(len(contexts)):
+            ref = _sdpa_causal(c["q64"][r], c["hist_k"][r], c["hist_v"][r], c["scale"])
+            np.testing.assert_allclose(out[r], ref, rtol=0, atol=1e-12)
+            for i in range(qn):
+                e = contexts[r] - qn + i + 1
+                np.testing.assert_allclose(
+                    lse[r, i], _lse(c["q64"][r][i], c["hist_k"][r][:e], c["scale"]),
+                    rtol=0, atol=1e-12)
+
+
+def check_multi_query_prefix(lib):
+    """Query i of a Q-token read is the one-token read of the history's first
+    c - Q + i + 1 positions, bit for bit (same tokens, same order)."""
+    rng = np.random.default_rng(RNG_SEED + 11)
+    contexts, qn = [20, 7, 33], 4
+    c = _mq_case(rng, contexts, qn, 4, 2, 8, 4, "f32")
+    out, lse = _run(lib, c)
+    for i in range(qn):
+        ctx_i = np.array([n - qn + i + 1 for n in contexts], dtype=np.int32)
+        single = dict(c, q=c["q"][:, i], context_lens=ctx_i)
+        o1, l1 = _run(lib, single)
+        assert np.array_equal(out[:, i], o1) and np.array_equal(lse[:, i], l1)
+
+
+def check_multi_query_splits_and_short_rows(lib):
+    rng = np.random.default_rng(RNG_SEED + 12)
+    contexts, qn = [2, 50, 90], 3
+    c = _mq_case(rng, contexts, qn, 4, 2, 8, 8, "f32")
+    full, full_lse = _run(lib, c)
+    part, plse = _run(lib, c, split_len=16, num_splits=12)
+    merged = oracle.reduce(part.reshape(3, qn * 4, 12, 8), plse.reshape(3, qn * 4, 12), lib=lib)
+    np.testing.assert_allclose(merged.reshape(3, qn, 4, 8), full, rtol=0, atol=1e-12)
+    # a row shorter than the query run: its first query tokens see nothing
+    c2 = _mq_case(rng, [2], 4, 4, 2, 8, 8, "f32")
+    out, lse = _run(lib, c2)
+    assert np.all(out[0, :2] == 0) and np.all(lse[0, :2] == -np.inf)
+    assert np.isfinite(out[0, 2:]).all()
+
+
 ALL_CHECKS = [
     check_widen,
     check_sdpa_equivalence,
@@ -393,4 +464,7 @@ ALL_CHECKS = [
     check_f32_twin,
     check_append,
     check_refusals,
+    check_multi_query_sdpa,
+    check_multi_query_prefix,
+    check_multi_query_splits_and_short_rows,
 ]

@@ -35,14 +35,20 @@ MUTANTS = {
     # softmax not normalised
     "no_normalise": ("decode_body.h", "o[d] /= z;", "o[d] /= 1;"),
     # the last history token dropped
-    "range_off_by_one": ("decode_body.h", "tb + split_len < c ? tb + split_len : c",
-                         "tb + split_len < c - 1 ? tb + split_len : c - 1"),
+    "range_off_by_one": ("decode_body.h", "tb + split_len < e ? tb + split_len : e",
+                         "tb + split_len < e - 1 ? tb + split_len : e - 1"),
     # one slot past the history read
-    "range_one_past": ("decode_body.h", "tb + split_len < c ? tb + split_len : c",
-                       "tb + split_len < c + 1 ? tb + split_len : c + 1"),
+    "range_one_past": ("decode_body.h", "tb + split_len < e ? tb + split_len : e",
+                       "tb + split_len < e + 1 ? tb + split_len : e + 1"),
+    # causal limit of a query token off by one
+    "causal_limit": ("decode_body.h", "int64_t e = c - query_len + qi + 1;",
+                     "int64_t e = c - query_len + qi;"),
+    # query tokens read in the wrong order
+    "query_order": ("decode_body.h", "int64_t rq = (int64_t)r * query_len + qi;",
+                    "int64_t rq = (int64_t)r * query_len + (query_len - 1 - qi);"),
     # query element taken from the wrong head
-    "q_wrong_head": ("decode_body.h", "((int64_t)r * q_heads + h) * head_dim + d);",
-                     "((int64_t)r * q_heads + kh) * head_dim + d);"),
+    "q_wrong_head": ("decode_body.h", "(rq * q_heads + h) * head_dim + d);",
+                     "(rq * q_heads + kh) * head_dim + d);"),
     # V gathered from the K pool
     "v_from_k": ("decode_body.h", "npo_load(v_pool, dtype, idx)", "npo_load(k_pool, dtype, idx)"),
     # lse missing the max
