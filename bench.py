@@ -57,10 +57,11 @@ def algorithmic_bytes(w: wl.Workload, md: wl.Metadata) -> dict:
     """
     cl = md.context_lens.to(torch.int64)
     es = w.elem_size
+    qn = w.query_len
     kv = int(cl.sum()) * 2 * w.kv_heads * w.head_dim * es
-    qo = 2 * w.rows * w.q_heads * w.head_dim * es
+    qo = 2 * w.rows * qn * w.q_heads * w.head_dim * es
     tab = int(((cl + w.block_size - 1) // w.block_size).sum()) * 4 + 4 * w.rows
-    app = 2 * 2 * w.rows * w.kv_heads * w.head_dim * es + 8 * w.rows
+    app = 2 * 2 * w.rows * qn * w.kv_heads * w.head_dim * es + 8 * w.rows * qn
     return {"kv": kv, "decode": kv + qo + tab + app, "append": app}
 
 
@@ -281,7 +282,7 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
     bt, cl, sm = (t.to(dev) for t in (md.block_tables, md.context_lens, md.slot_mapping))
     S = args.splits or npg.np_paged_decode_plan(w.rows, w.q_heads, w.kv_heads, w.head_dim,
                                                 w.block_size, bt.shape[1], w.torch_dtype)
-    ws = npg.workspace(w.rows, w.q_heads, w.head_dim, S, device=dev)
+    ws = npg.workspace(w.rows, w.q_heads, w.head_dim, S, device=dev, query_len=w.query_len)
     out = torch.empty_like(inp.q)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -403,6 +404,7 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
         "config": {
             "workload": w.name, "description": w.description, "rows": w.rows,
             "q_heads": w.q_heads, "kv_heads": w.kv_heads, "head_dim": w.head_dim,
+            "query_len": w.query_len,
             "block_size": w.block_size, "max_blocks_per_row": bt.shape[1],
             "num_blocks": md.num_blocks, "num_splits": S,
             "split_len": npg.np_paged_decode_split_len(w.block_size, bt.shape[1], S),

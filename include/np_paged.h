@@ -45,9 +45,16 @@
  *   - Pools: k_pool and v_pool are separate arrays, each
  *     [num_blocks, block_size, kv_heads, head_dim] of `dtype`.
  *   - Supported: dtype NP_F32 or NP_BF16; head_dim in {16, 32, 64, 128, 256};
- *     group q_heads/kv_heads in {1, 2, 4, 5, 8}; any block_size >= 1; any
- *     kv_heads >= 1.  Arithmetic is fp32 in every case (bf16 is widened
- *     exactly); q and out have the pool dtype.
+ *     group g = q_heads/kv_heads in {1, 2, 4, 5, 8}; any block_size >= 1;
+ *     any kv_heads >= 1; query_len 1, or (bf16 pools) any query_len with
+ *     g * query_len <= 16.  Arithmetic is fp32 in every case (bf16 is
+ *     widened exactly); q and out have the pool dtype.
+ *   - Several query tokens per row (query_len Q > 1, speculative or chunked
+ *     decode): the row's Q query tokens are its last Q positions
+ *     c - Q .. c - 1 (c = context_lens[r], counting them); query token i
+ *     attends causally to positions 0 .. c - Q + i.  q and out are then
+ *     [rows, Q, q_heads, head_dim]; everything sized "per row and head"
+ *     below is per (row, query token) and head.
  */
 #ifndef NP_PAGED_H
 #define NP_PAGED_H
@@ -59,7 +66,7 @@
 extern "C" {
 #endif
 
-#define NP_ABI_VERSION 1
+#define NP_ABI_VERSION 2
 
 /* Same type as cudaStream_t / CUstream, without pulling in CUDA headers. */
 typedef struct CUstream_st* np_stream_t;
@@ -86,6 +93,8 @@ typedef enum np_dtype { NP_F32 = 0, NP_BF16 = 1 } np_dtype;
                                 written */
 #define NP_FLAG_TIMEOUT 0x8  /* an internal pipeline wait gave up (never
                                 expected; the output of that block is wrong) */
+#define NP_FLAG_CONFIG 0x10  /* a thread block found its launch configuration
+                                inconsistent and did nothing (never expected) */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* np_status_string(np_status status);
@@ -139,6 +148,7 @@ int64_t np_paged_decode_split_len(int32_t block_size,
  *   partial outputs  [rows, q_heads, num_splits, head_dim] fp32 at offset 0,
  *   partial lse      [rows, q_heads, num_splits] fp32 at the next 256-byte
  *                    boundary (natural log; -inf for an empty split).
+ * For query_len > 1 pass rows * query_len as `rows`.
  * 0 when num_splits <= 1.
  */
 size_t np_paged_decode_workspace_bytes(int32_t rows, int32_t q_heads,
@@ -146,9 +156,10 @@ size_t np_paged_decode_workspace_bytes(int32_t rows, int32_t q_heads,
 
 /*
  * np_paged_decode -- the decode read.
- *   out            [rows, q_heads, head_dim] dtype; written when
+ *   out            [rows, query_len, q_heads, head_dim] dtype; written when
  *                  num_splits == 1 (may be NULL otherwise)
- *   q              [rows, q_heads, head_dim] dtype
+ *   q              [rows, query_len, q_heads, head_dim] dtype
+ *   query_len      query tokens per row (1 = the usual decode step)
  *   k_pool, v_pool [num_blocks, block_size, kv_heads, head_dim] dtype
  *   block_tables   [rows, max_blocks_per_row] int32: logical block j of row
  *                  r is physical block block_tables[r*max_blocks_per_row+j];
@@ -177,23 +188,24 @@ np_status np_paged_decode(void* out, const void* q, const void* k_pool,
                           const int32_t* block_tables,
                           int32_t max_blocks_per_row,
                           const int32_t* context_lens, int32_t rows,
-                          int32_t q_heads, float scale, int32_t num_splits,
-                          void* workspace, size_t workspace_bytes,
-                          int32_t* err_word, np_stream_t stream);
+                          int32_t query_len, int32_t q_heads, float scale,
+                          int32_t num_splits, void* workspace,
+                          size_t workspace_bytes, int32_t* err_word,
+                          np_stream_t stream);
 
 /*
- * np_paged_append_decode -- np_kv_append of one new token per row followed
+ * np_paged_append_decode -- np_kv_append of the rows' new tokens followed
  * by np_paged_decode, in ONE kernel launch (same results, bit for bit in
- * the pools).  Row r's new K and V rows (k_new/v_new [rows, kv_heads,
- * head_dim]) go to pool slot slot_mapping[r], which must be the slot of the
- * row's newest position, context_lens[r] - 1, under its block table (the
+ * the pools).  Row r's query_len new tokens (k_new/v_new [rows, query_len,
+ * kv_heads, head_dim]) go to pool slots slot_mapping[r*query_len + j]
+ * ([rows, query_len] int64), which must be the slots of the row's newest
+ * positions, context_lens[r] - query_len + j, under its block table (the
  * usual decode step: append, then read the whole history); a negative entry
- * means "no new token for this row".  The thread block whose split holds
- * that position writes the token before it reads it.  An entry that names
- * any other slot is not written and is flagged (NP_FLAG_SLOT) -- use
- * np_kv_append + np_paged_decode for arbitrary slots.  Other arguments,
- * layouts and errors as np_paged_decode; with num_splits > 1, call
- * np_paged_decode_reduce next.
+ * means "no new token here".  The thread block whose split holds a position
+ * writes that token before it reads it.  An entry that names any other slot
+ * is not written and is flagged (NP_FLAG_SLOT) -- use np_kv_append +
+ * np_paged_decode for arbitrary slots.  Other arguments, layouts and errors
+ * as np_paged_decode; with num_splits > 1, call np_paged_decode_reduce next.
  */
 np_status np_paged_append_decode(void* out, const void* q, const void* k_new,
                                  const void* v_new, const int64_t* slot_mapping,
@@ -203,14 +215,15 @@ np_status np_paged_append_decode(void* out, const void* q, const void* k_new,
                                  const int32_t* block_tables,
                                  int32_t max_blocks_per_row,
                                  const int32_t* context_lens, int32_t rows,
-                                 int32_t q_heads, float scale,
-                                 int32_t num_splits, void* workspace,
-                                 size_t workspace_bytes, int32_t* err_word,
-                                 np_stream_t stream);
+                                 int32_t query_len, int32_t q_heads,
+                                 float scale, int32_t num_splits,
+                                 void* workspace, size_t workspace_bytes,
+                                 int32_t* err_word, np_stream_t stream);
 
 /*
  * np_paged_decode_reduce -- merge split partials into out.
- *   out        [rows, q_heads, head_dim] of out_dtype
+ *   out        [rows, q_heads, head_dim] of out_dtype (for query_len > 1:
+ *              pass rows * query_len as `rows`)
  *   workspace  as written by np_paged_decode with the same rows, q_heads,
  *              head_dim and num_splits
  * For each (row, head): L = max_s lse_s; out = sum_s e^(lse_s - L) o_s /
@@ -239,9 +252,9 @@ np_status np_paged_decode_reduce(void* out, np_dtype out_dtype,
  * Arguments, layouts and errors are those of np_paged_decode, with `out`
  * always written and no workspace.  It allocates and frees nothing.
  *   - Returns NP_ERR_WORKSPACE, before anything is enqueued, when the
- *     partials, np_paged_decode_workspace_bytes(rows, q_heads, head_dim,
- *     num_splits), exceed NP_NOALLOC_SCRATCH_BYTES; a smaller num_splits
- *     fits.  num_splits <= 1 uses no scratch at all.
+ *     partials, np_paged_decode_workspace_bytes(rows * query_len, q_heads,
+ *     head_dim, num_splits), exceed NP_NOALLOC_SCRATCH_BYTES; a smaller
+ *     num_splits fits.  num_splits <= 1 uses no scratch at all.
  *   - The first call on a device looks up the array's device address for
  *     that device (cudaGetSymbolAddress); make that first call before any
  *     stream capture.
@@ -259,9 +272,9 @@ np_status np_paged_decode_noalloc(void* out, const void* q, const void* k_pool,
                                   const int32_t* block_tables,
                                   int32_t max_blocks_per_row,
                                   const int32_t* context_lens, int32_t rows,
-                                  int32_t q_heads, float scale,
-                                  int32_t num_splits, int32_t* err_word,
-                                  np_stream_t stream);
+                                  int32_t query_len, int32_t q_heads,
+                                  float scale, int32_t num_splits,
+                                  int32_t* err_word, np_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -150,10 +150,12 @@ def kv_append(k_pool, v_pool, k_new, v_new, slot_mapping, *, lib=None) -> int:
     for a in (k_pool, v_pool):
         if not a.flags.c_contiguous:
             raise ValueError("pools must be C-contiguous (written in place)")
-    k_new, v_new = _c(k_new), _c(v_new)
-    code = dtype_code(k_pool)
-    sm = _c(slot_mapping, np.int64)
     num_blocks, block_size, kv_heads, head_dim = k_pool.shape
+    # [R, Q, Hk, D] tokens with [R, Q] slots are R*Q tokens
+    k_new = _c(k_new).reshape(-1, kv_heads, head_dim)
+    v_new = _c(v_new).reshape(-1, kv_heads, head_dim)
+    code = dtype_code(k_pool)
+    sm = _c(slot_mapping, np.int64).reshape(-1)
     n = sm.shape[0]
     if k_new.shape != (n, kv_heads, head_dim) or v_new.shape != k_new.shape:
         raise ValueError("k_new/v_new must be [num_tokens, kv_heads, head_dim]")

@@ -34,7 +34,7 @@ __all__ = [
     "np_paged_decode_noalloc", "NP_NOALLOC_SCRATCH_BYTES", "np_paged_append_decode",
     "workspace", "decode_step", "NP_OK", "NP_ERR_INVALID_ARG", "NP_ERR_UNSUPPORTED",
     "NP_ERR_WORKSPACE", "NP_ERR_OUT_OF_RANGE", "NP_ERR_CUDA", "NP_F32", "NP_BF16",
-    "NP_FLAG_BLOCK_ID", "NP_FLAG_CONTEXT", "NP_FLAG_SLOT", "NP_FLAG_TIMEOUT",
+    "NP_FLAG_BLOCK_ID", "NP_FLAG_CONTEXT", "NP_FLAG_SLOT", "NP_FLAG_TIMEOUT", "NP_FLAG_CONFIG",
 ]
 
 NP_OK = 0
@@ -51,6 +51,7 @@ NP_FLAG_BLOCK_ID = 0x1
 NP_FLAG_CONTEXT = 0x2
 NP_FLAG_SLOT = 0x4
 NP_FLAG_TIMEOUT = 0x8
+NP_FLAG_CONFIG = 0x10
 
 NP_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -96,16 +97,16 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.np_paged_decode_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32]
     lib.np_paged_decode.restype = ctypes.c_int
     lib.np_paged_decode.argtypes = [_P, _P, _P, _P, ctypes.c_int, _I64, _I32, _I32, _I32, _P,
-                                    _I32, _P, _I32, _I32, ctypes.c_float, _I32, _P,
+                                    _I32, _P, _I32, _I32, _I32, ctypes.c_float, _I32, _P,
                                     ctypes.c_size_t, _P, _P]
     lib.np_paged_append_decode.restype = ctypes.c_int
     lib.np_paged_append_decode.argtypes = [_P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _I64, _I32,
-                                           _I32, _I32, _P, _I32, _P, _I32, _I32, ctypes.c_float,
-                                           _I32, _P, ctypes.c_size_t, _P, _P]
+                                           _I32, _I32, _P, _I32, _P, _I32, _I32, _I32,
+                                           ctypes.c_float, _I32, _P, ctypes.c_size_t, _P, _P]
     lib.np_paged_decode_noalloc.restype = ctypes.c_int
     lib.np_paged_decode_noalloc.argtypes = [_P, _P, _P, _P, ctypes.c_int, _I64, _I32, _I32, _I32,
-                                            _P, _I32, _P, _I32, _I32, ctypes.c_float, _I32, _P,
-                                            _P]
+                                            _P, _I32, _P, _I32, _I32, _I32, ctypes.c_float, _I32,
+                                            _P, _P]
     lib.np_paged_decode_reduce.restype = ctypes.c_int
     lib.np_paged_decode_reduce.argtypes = [_P, ctypes.c_int, _P, ctypes.c_size_t, _I32, _I32,
                                            _I32, _I32, _P]
@@ -149,6 +150,16 @@ def _stream(stream) -> int | None:
     return int(stream)
 
 
+def _q_shape(q: torch.Tensor, name: str = "q"):
+    """(rows, query_len, q_heads, head_dim) of a [R, Hq, D] or [R, Q, Hq, D] tensor."""
+    if q.dim() == 3:
+        return q.shape[0], 1, q.shape[1], q.shape[2]
+    if q.dim() == 4:
+        return tuple(q.shape)
+    raise ValueError(f"{name} must be [rows, q_heads, head_dim] or "
+                     "[rows, query_len, q_heads, head_dim]")
+
+
 def np_abi_version() -> int:
     return load().np_abi_version()
 
@@ -158,8 +169,15 @@ def np_status_string(status: int) -> str:
 
 
 def np_kv_append(k_pool, v_pool, k_new, v_new, slot_mapping, err_word=None, stream=None):
-    """Scatter [T, Hk, D] new K/V rows into the pools at ``slot_mapping`` (int64)."""
+    """Scatter [T, Hk, D] new K/V rows into the pools at ``slot_mapping`` (int64 [T]).
+
+    Leading dimensions are flattened: [R, Q, Hk, D] tokens with [R, Q] slots
+    are R*Q tokens.
+    """
     nb, bs, hk, d = k_pool.shape
+    if k_new.dim() > 3:
+        k_new, v_new = k_new.reshape(-1, hk, d), v_new.reshape(-1, hk, d)
+        slot_mapping = slot_mapping.reshape(-1)
     if v_pool.shape != k_pool.shape or k_new.shape != v_new.shape or \
             k_new.shape[1:] != (hk, d) or k_new.dtype != k_pool.dtype or \
             v_new.dtype != k_pool.dtype or v_pool.dtype != k_pool.dtype:
@@ -191,35 +209,46 @@ def np_paged_decode_workspace_bytes(rows, q_heads, head_dim, num_splits) -> int:
     return load().np_paged_decode_workspace_bytes(rows, q_heads, head_dim, num_splits)
 
 
-def workspace(rows, q_heads, head_dim, num_splits, device="cuda") -> torch.Tensor | None:
+def workspace(rows, q_heads, head_dim, num_splits, device="cuda",
+              query_len: int = 1) -> torch.Tensor | None:
     """A torch-allocated workspace of the size the library asks for (None if unsplit)."""
-    n = np_paged_decode_workspace_bytes(rows, q_heads, head_dim, num_splits)
+    n = np_paged_decode_workspace_bytes(rows * query_len, q_heads, head_dim, num_splits)
     if n == 0:
         return None
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def np_paged_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale,
-                    num_splits: int = 1, workspace=None, err_word=None, stream=None):
-    """The decode read (see np_paged.h).  Writes ``out`` when num_splits == 1."""
-    rows, q_heads, d = q.shape
+def _check_read_args(call, out, q, k_pool, v_pool, block_tables, context_lens):
+    rows, qn, q_heads, d = _q_shape(q)
     nb, bs, hk, d2 = k_pool.shape
     if d2 != d or v_pool.shape != k_pool.shape or q.dtype != k_pool.dtype or \
             v_pool.dtype != k_pool.dtype:
-        raise ValueError("np_paged_decode: q/pool shape or dtype mismatch")
+        raise ValueError(f"{call}: q/pool shape or dtype mismatch")
     if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or \
             block_tables.shape[0] != rows:
-        raise ValueError("np_paged_decode: block_tables must be int32 [rows, max_blocks]")
+        raise ValueError(f"{call}: block_tables must be int32 [rows, max_blocks]")
     if context_lens.dtype != torch.int32 or context_lens.shape != (rows,):
-        raise ValueError("np_paged_decode: context_lens must be int32 [rows]")
+        raise ValueError(f"{call}: context_lens must be int32 [rows]")
     if out is not None and (out.shape != q.shape or out.dtype != q.dtype):
-        raise ValueError("np_paged_decode: out must match q")
+        raise ValueError(f"{call}: out must match q")
+    return rows, qn, q_heads, d, nb, bs, hk
+
+
+def np_paged_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale,
+                    num_splits: int = 1, workspace=None, err_word=None, stream=None):
+    """The decode read (see np_paged.h).  Writes ``out`` when num_splits == 1.
+
+    q is [rows, q_heads, head_dim] (one query token per row) or
+    [rows, query_len, q_heads, head_dim] (the rows' last query_len positions).
+    """
+    rows, qn, q_heads, d, nb, bs, hk = _check_read_args(
+        "np_paged_decode", out, q, k_pool, v_pool, block_tables, context_lens)
     ws_ptr = _opt(workspace, "workspace")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load().np_paged_decode(
         _opt(out, "out"), _dev(q, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
         _dtype_code(q.dtype), nb, bs, hk, d, _dev(block_tables, "block_tables"),
-        block_tables.shape[1], _dev(context_lens, "context_lens"), rows, q_heads,
+        block_tables.shape[1], _dev(context_lens, "context_lens"), rows, qn, q_heads,
         float(scale), num_splits, ws_ptr, ws_bytes, _opt(err_word, "err_word"),
         _stream(stream))
     _check(st, "np_paged_decode")
@@ -228,43 +257,40 @@ def np_paged_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale,
 def np_paged_append_decode(out, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables,
                            context_lens, scale, num_splits: int = 1, workspace=None,
                            err_word=None, stream=None):
-    """Append each row's new token (at its newest position) and read, in one launch."""
-    rows, q_heads, d = q.shape
-    nb, bs, hk, d2 = k_pool.shape
-    if d2 != d or v_pool.shape != k_pool.shape or q.dtype != k_pool.dtype or \
-            v_pool.dtype != k_pool.dtype:
-        raise ValueError("np_paged_append_decode: q/pool shape or dtype mismatch")
-    if k_new.shape != (rows, hk, d) or v_new.shape != k_new.shape or \
+    """Append each row's new tokens (at its newest positions) and read, in one launch.
+
+    k_new/v_new: [rows, kv_heads, head_dim] (or [rows, query_len, kv_heads,
+    head_dim]); slot_mapping: int64 [rows] (or [rows, query_len]).
+    """
+    rows, qn, q_heads, d, nb, bs, hk = _check_read_args(
+        "np_paged_append_decode", out, q, k_pool, v_pool, block_tables, context_lens)
+    want = (rows, hk, d) if q.dim() == 3 else (rows, qn, hk, d)
+    if tuple(k_new.shape) != want or v_new.shape != k_new.shape or \
             k_new.dtype != k_pool.dtype or v_new.dtype != k_pool.dtype:
-        raise ValueError("np_paged_append_decode: k_new/v_new must be [rows, kv_heads, head_dim]")
-    if slot_mapping.dtype != torch.int64 or slot_mapping.shape != (rows,):
-        raise ValueError("np_paged_append_decode: slot_mapping must be int64 [rows]")
-    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or \
-            block_tables.shape[0] != rows:
-        raise ValueError("np_paged_append_decode: block_tables must be int32 [rows, max_blocks]")
-    if context_lens.dtype != torch.int32 or context_lens.shape != (rows,):
-        raise ValueError("np_paged_append_decode: context_lens must be int32 [rows]")
-    if out is not None and (out.shape != q.shape or out.dtype != q.dtype):
-        raise ValueError("np_paged_append_decode: out must match q")
+        raise ValueError(f"np_paged_append_decode: k_new/v_new must be {list(want)}")
+    want_sm = (rows,) if q.dim() == 3 else (rows, qn)
+    if slot_mapping.dtype != torch.int64 or tuple(slot_mapping.shape) != want_sm:
+        raise ValueError(f"np_paged_append_decode: slot_mapping must be int64 {list(want_sm)}")
     ws_ptr = _opt(workspace, "workspace")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load().np_paged_append_decode(
         _opt(out, "out"), _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
         _dev(slot_mapping, "slot_mapping"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
         _dtype_code(q.dtype), nb, bs, hk, d, _dev(block_tables, "block_tables"),
-        block_tables.shape[1], _dev(context_lens, "context_lens"), rows, q_heads,
+        block_tables.shape[1], _dev(context_lens, "context_lens"), rows, qn, q_heads,
         float(scale), num_splits, ws_ptr, ws_bytes, _opt(err_word, "err_word"),
         _stream(stream))
     _check(st, "np_paged_append_decode")
 
 
 def np_paged_decode_reduce(out, workspace, num_splits: int, stream=None):
-    """Merge split partials in ``workspace`` into ``out`` [rows, q_heads, head_dim]."""
-    rows, q_heads, d = out.shape
+    """Merge split partials in ``workspace`` into ``out`` ([rows, q_heads, head_dim]
+    or [rows, query_len, q_heads, head_dim])."""
+    rows, qn, q_heads, d = _q_shape(out, "out")
     ws_bytes = workspace.numel() * workspace.element_size()
     st = load().np_paged_decode_reduce(
-        _dev(out, "out"), _dtype_code(out.dtype), _dev(workspace, "workspace"), ws_bytes, rows,
-        q_heads, d, num_splits, _stream(stream))
+        _dev(out, "out"), _dtype_code(out.dtype), _dev(workspace, "workspace"), ws_bytes,
+        rows * qn, q_heads, d, num_splits, _stream(stream))
     _check(st, "np_paged_decode_reduce")
 
 
@@ -273,20 +299,14 @@ def np_paged_decode_noalloc(out, q, k_pool, v_pool, block_tables, context_lens, 
     """The read plus the split merge with no workspace argument: for callers
     that cannot allocate device memory, the split partials go to a fixed
     NP_NOALLOC_SCRATCH_BYTES array inside the library (see np_paged.h)."""
-    rows, q_heads, d = q.shape
-    nb, bs, hk, d2 = k_pool.shape
-    if d2 != d or v_pool.shape != k_pool.shape or q.dtype != k_pool.dtype or \
-            v_pool.dtype != k_pool.dtype or out.shape != q.shape or out.dtype != q.dtype:
-        raise ValueError("np_paged_decode_noalloc: q/out/pool shape or dtype mismatch")
-    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or \
-            block_tables.shape[0] != rows:
-        raise ValueError("np_paged_decode_noalloc: block_tables must be int32 [rows, max_blocks]")
-    if context_lens.dtype != torch.int32 or context_lens.shape != (rows,):
-        raise ValueError("np_paged_decode_noalloc: context_lens must be int32 [rows]")
+    if out is None:
+        raise ValueError("np_paged_decode_noalloc: out is required")
+    rows, qn, q_heads, d, nb, bs, hk = _check_read_args(
+        "np_paged_decode_noalloc", out, q, k_pool, v_pool, block_tables, context_lens)
     st = load().np_paged_decode_noalloc(
         _dev(out, "out"), _dev(q, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
         _dtype_code(q.dtype), nb, bs, hk, d, _dev(block_tables, "block_tables"),
-        block_tables.shape[1], _dev(context_lens, "context_lens"), rows, q_heads,
+        block_tables.shape[1], _dev(context_lens, "context_lens"), rows, qn, q_heads,
         float(scale), num_splits, _opt(err_word, "err_word"), _stream(stream))
     _check(st, "np_paged_decode_noalloc")
 
@@ -302,7 +322,8 @@ def decode_step(out, q, k_pool, v_pool, block_tables, context_lens, scale, *, k_
     """
     launches = 0
     o = out if num_splits == 1 else None
-    if k_new is not None and fused and k_new.shape[0] == q.shape[0]:
+    if k_new is not None and fused and k_new.shape[0] == q.shape[0] and \
+            k_new.dim() == q.dim():
         np_paged_append_decode(o, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables,
                                context_lens, scale, num_splits, workspace, err_word, stream)
         launches += 1 if q.shape[0] > 0 else 0

@@ -282,17 +282,20 @@ namespace {
 np_status decode_impl(void* out, const void* q, const void* k_pool, const void* v_pool,
                       np_dtype dtype, int64_t num_blocks, int32_t block_size, int32_t kv_heads,
                       int32_t head_dim, const int32_t* block_tables, int32_t max_blocks_per_row,
-                      const int32_t* context_lens, int32_t rows, int32_t q_heads, float scale,
-                      int32_t num_splits, void* workspace, size_t workspace_bytes,
-                      int32_t* err_word, np_stream_t stream, const void* k_new,
-                      const void* v_new, const int64_t* slot_mapping) {
+                      const int32_t* context_lens, int32_t rows, int32_t query_len,
+                      int32_t q_heads, float scale, int32_t num_splits, void* workspace,
+                      size_t workspace_bytes, int32_t* err_word, np_stream_t stream,
+                      const void* k_new, const void* v_new, const int64_t* slot_mapping) {
   const int es = elem_size(dtype);
   if (es == 0) return NP_ERR_UNSUPPORTED;
-  if (rows < 0 || q_heads <= 0 || kv_heads <= 0 || q_heads % kv_heads != 0 ||
+  if (rows < 0 || query_len <= 0 || q_heads <= 0 || kv_heads <= 0 || q_heads % kv_heads != 0 ||
       num_blocks <= 0 || block_size <= 0 || max_blocks_per_row <= 0 || num_splits <= 0 ||
       num_splits > 65535 || !isfinite(scale))
     return NP_ERR_INVALID_ARG;
   if (!head_dim_supported(head_dim) || !group_supported(q_heads / kv_heads))
+    return NP_ERR_UNSUPPORTED;
+  // several query tokens: bf16 pools, (query token, head) rows of a group <= 16
+  if (query_len > 1 && (dtype != NP_BF16 || (q_heads / kv_heads) * query_len > 16))
     return NP_ERR_UNSUPPORTED;
   int64_t slots = 0, pool_elems = 0, pool_bytes = 0, tab = 0;
   if (!mul_ok(num_blocks, block_size, &slots) ||
@@ -311,12 +314,14 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
   float* ws_o = nullptr;
   float* ws_lse = nullptr;
   if (num_splits > 1) {
-    const size_t need = np_paged_decode_workspace_bytes(rows, q_heads, head_dim, num_splits);
+    const int32_t units_rows = rows * query_len;  // rows of the partial layout
+    const size_t need =
+        np_paged_decode_workspace_bytes(units_rows, q_heads, head_dim, num_splits);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return NP_ERR_WORKSPACE;
     ws_o = static_cast<float*>(workspace);
     ws_lse = reinterpret_cast<float*>(
         static_cast<char*>(workspace) +
-        round_up((size_t)rows * q_heads * num_splits * head_dim * sizeof(float), 256));
+        round_up((size_t)units_rows * q_heads * num_splits * head_dim * sizeof(float), 256));
   }
   int sms = 0, smem_optin = 0;
   np_status st = device_info(&sms, &smem_optin);
@@ -347,15 +352,18 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
   p.k_new = k_new;
   p.v_new = v_new;
   p.slot_mapping = slot_mapping;
+  p.query_len = query_len;
   // bf16 pools with head_dim a multiple of 64 stage K/V through tiled TMA
-  // boxes of box_tokens tokens: the largest power of two <= 16 dividing the
-  // block size, with box_tokens * head_group a multiple of 8 (each box then
-  // starts on a 1024-byte swizzle boundary) and slot coordinates in int32.
+  // boxes of box_tokens tokens: the largest power of two dividing the block
+  // size, at most the stage's token count, with box_tokens * head_group a
+  // multiple of 8 (each box then starts on a 1024-byte swizzle boundary) and
+  // slot coordinates in int32.
   p.use_tmap = 0;
   p.box_tokens = 1;
   if (dtype == NP_BF16 && head_dim % 64 == 0 && slots <= INT32_MAX) {
+    const int ct = npk::mma_chunk_tokens(head_dim);  // a box never exceeds a stage
     int bt = 1;
-    while (bt < 16 && block_size % (bt * 2) == 0) bt *= 2;
+    while (bt < ct && block_size % (bt * 2) == 0) bt *= 2;
     if ((bt * hg) % 8 == 0 &&
         pool_maps(p, k_pool, v_pool, slots, kv_heads, head_dim, bt, hg)) {
       p.use_tmap = 1;
@@ -387,12 +395,13 @@ np_status np_paged_decode(void* out, const void* q, const void* k_pool, const vo
                           np_dtype dtype, int64_t num_blocks, int32_t block_size,
                           int32_t kv_heads, int32_t head_dim, const int32_t* block_tables,
                           int32_t max_blocks_per_row, const int32_t* context_lens, int32_t rows,
-                          int32_t q_heads, float scale, int32_t num_splits, void* workspace,
-                          size_t workspace_bytes, int32_t* err_word, np_stream_t stream) {
+                          int32_t query_len, int32_t q_heads, float scale, int32_t num_splits,
+                          void* workspace, size_t workspace_bytes, int32_t* err_word,
+                          np_stream_t stream) {
   return decode_impl(out, q, k_pool, v_pool, dtype, num_blocks, block_size, kv_heads, head_dim,
-                     block_tables, max_blocks_per_row, context_lens, rows, q_heads, scale,
-                     num_splits, workspace, workspace_bytes, err_word, stream, nullptr, nullptr,
-                     nullptr);
+                     block_tables, max_blocks_per_row, context_lens, rows, query_len, q_heads,
+                     scale, num_splits, workspace, workspace_bytes, err_word, stream, nullptr,
+                     nullptr, nullptr);
 }
 
 np_status np_paged_append_decode(void* out, const void* q, const void* k_new, const void* v_new,
@@ -400,18 +409,19 @@ np_status np_paged_append_decode(void* out, const void* q, const void* k_new, co
                                  np_dtype dtype, int64_t num_blocks, int32_t block_size,
                                  int32_t kv_heads, int32_t head_dim,
                                  const int32_t* block_tables, int32_t max_blocks_per_row,
-                                 const int32_t* context_lens, int32_t rows, int32_t q_heads,
-                                 float scale, int32_t num_splits, void* workspace,
-                                 size_t workspace_bytes, int32_t* err_word, np_stream_t stream) {
+                                 const int32_t* context_lens, int32_t rows, int32_t query_len,
+                                 int32_t q_heads, float scale, int32_t num_splits,
+                                 void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                 np_stream_t stream) {
   if (rows > 0) {
     if (!k_new || !v_new || !slot_mapping) return NP_ERR_INVALID_ARG;
     if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8))
       return NP_ERR_INVALID_ARG;
   }
   return decode_impl(out, q, k_pool, v_pool, dtype, num_blocks, block_size, kv_heads, head_dim,
-                     block_tables, max_blocks_per_row, context_lens, rows, q_heads, scale,
-                     num_splits, workspace, workspace_bytes, err_word, stream, k_new, v_new,
-                     slot_mapping);
+                     block_tables, max_blocks_per_row, context_lens, rows, query_len, q_heads,
+                     scale, num_splits, workspace, workspace_bytes, err_word, stream, k_new,
+                     v_new, slot_mapping);
 }
 
 np_status np_paged_decode_reduce(void* out, np_dtype out_dtype, const void* workspace,

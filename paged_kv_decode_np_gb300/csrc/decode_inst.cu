@@ -30,11 +30,11 @@ namespace {
 // bf16 pools run on the tensor cores (decode_mma.cuh): through tiled TMA
 // boxes when the host built pool maps, else through per-token copies.  fp32
 // pools keep full fp32 products on the FMA pipes (decode_kernel.cuh).
-template <int G, bool TMAP>
+template <int G, bool TMAP, bool TWO>
 struct Variant {
 #if NPK_BF16
   using SM = MmaSmem<NPK_D, G, TMAP>;
-  static constexpr auto kernel = paged_decode_mma_kernel<NPK_D, G, TMAP>;
+  static constexpr auto kernel = paged_decode_mma_kernel<NPK_D, G, TMAP, TWO>;
   static size_t fixed(int) { return 16 + 128 + 1024; }
 #else
   using SM = DecodeSmem<StorageT, NPK_D, G>;
@@ -43,9 +43,9 @@ struct Variant {
 #endif
 };
 
-template <int G, bool TMAP>
+template <int G, bool TMAP, bool TWO>
 np_status launch_variant(DecodeLaunch& L, DecodeParams& p) {
-  using V = Variant<G, TMAP>;
+  using V = Variant<G, TMAP, TWO>;
   using SM = typename V::SM;
   const int warps = L.head_group * L.token_warps;
   const size_t fixed = V::fixed(warps);
@@ -77,13 +77,22 @@ np_status launch_variant(DecodeLaunch& L, DecodeParams& p) {
   return cudaGetLastError() == cudaSuccess ? NP_OK : NP_ERR_CUDA;
 }
 
+// bf16: TWO when the (query token, head) rows spill past the first 8 mma
+// rows (G * query_len > 8).  fp32: one query token only (host-checked).
 template <int G>
 np_status launch_one(DecodeLaunch& L, DecodeParams& p) {
-#if NPK_BF16 && (NPK_D % 64 == 0)
-  if (p.use_tmap) return launch_variant<G, true>(L, p);
+#if NPK_BF16
+  const bool two = G * p.query_len > 8;
+#if NPK_D % 64 == 0
+  if (p.use_tmap)
+    return two ? launch_variant<G, true, true>(L, p) : launch_variant<G, true, false>(L, p);
 #endif
   p.use_tmap = 0;
-  return launch_variant<G, false>(L, p);
+  return two ? launch_variant<G, false, true>(L, p) : launch_variant<G, false, false>(L, p);
+#else
+  p.use_tmap = 0;
+  return launch_variant<G, false, false>(L, p);
+#endif
 }
 
 }  // namespace

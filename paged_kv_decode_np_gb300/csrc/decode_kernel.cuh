@@ -67,49 +67,69 @@ struct DecodeParams {
   int32_t stages;        // ring depth
   int32_t use_tmap;      // 1: K/V arrive through tm_k/tm_v boxes
   int32_t box_tokens;    // tokens per TMA box (divides block_size and the chunk)
+  int32_t query_len;     // query tokens per row (the last query_len positions)
   float qscale;          // softmax scale * log2(e)
-  // Fused append (np_paged_append_decode): row r's new K/V rows, written to
-  // pool slot slot_mapping[r] by the CTA whose split holds position
-  // context_lens[r] - 1, before that CTA reads it.  Null when not fused.
-  const void* k_new;     // [R, Hk, D] T
+  // Fused append (np_paged_append_decode): row r's new K/V rows, token j to
+  // pool slot slot_mapping[r*Q + j], written by the CTA whose split holds
+  // position context_lens[r] - Q + j, before that CTA reads it.  Null when
+  // not fused.
+  const void* k_new;     // [R, Q, Hk, D] T
   const void* v_new;
-  const int64_t* slot_mapping;  // [R]
+  const int64_t* slot_mapping;  // [R, Q]
 };
 
 // Fused append, run by every thread of the CTA before its pipeline starts.
-// The CTA whose token range [t0, t1) holds row r's newest position c - 1
-// writes its HG heads' slice of the new K and V rows to the slot the row's
-// block table gives that position -- the slot mapping must name that same
-// slot (a negative entry means "no new token"); an entry that does not is
-// flagged (NP_FLAG_SLOT) and nothing is written, so no other CTA can read a
-// slot being written.  The generic-proxy stores are made visible to this
-// CTA's TMA (async-proxy) reads by fence.proxy.async before the barrier that
-// precedes the first copy.
+// Row r's Q new tokens are its positions c - Q .. c - 1.  The CTA whose token
+// range [t0, t1) holds new token j's position writes its HG heads' slice of
+// that token's K and V rows to the slot the row's block table gives the
+// position -- the slot mapping must name that same slot (a negative entry
+// means "no new token"); an entry that does not is flagged (NP_FLAG_SLOT)
+// and nothing is written, so no other CTA can read a slot being written.
+// The generic-proxy stores are made visible to this CTA's TMA (async-proxy)
+// reads by fence.proxy.async before the barrier that precedes the first copy.
 template <int D, int ES>
 __device__ __forceinline__ void fused_append(const DecodeParams& p, int r, int hgi, int HG,
                                              int64_t c, int64_t t0, int64_t t1) {
-  if (p.slot_mapping == nullptr || c <= 0 || c - 1 < t0 || c - 1 >= t1) return;
-  const int64_t s = p.slot_mapping[r];
-  if (s < 0) return;
-  const int64_t bs = p.block_size;
-  const int64_t pos = c - 1;
-  const int64_t b = p.block_tables[(int64_t)r * p.max_blocks_per_row + pos / bs];
-  if (b < 0 || b >= p.num_blocks || s != b * bs + pos % bs) {
-    if (threadIdx.x == 0) set_flag(p.err, NP_FLAG_SLOT);
-    return;
+  if (p.slot_mapping == nullptr) return;
+  const int Q = p.query_len;
+  bool wrote = false;
+  for (int j = 0; j < Q; ++j) {
+    const int64_t pos = c - Q + j;
+    if (pos < 0 || pos < t0 || pos >= t1) continue;
+    const int64_t rq = (int64_t)r * Q + j;
+    const int64_t s = p.slot_mapping[rq];
+    if (s < 0) continue;
+    const int64_t bs = p.block_size;
+    const int64_t b = p.block_tables[(int64_t)r * p.max_blocks_per_row + pos / bs];
+    if (b < 0 || b >= p.num_blocks || s != b * bs + pos % bs) {
+      if (threadIdx.x == 0) set_flag(p.err, NP_FLAG_SLOT);
+      continue;
+    }
+    const int64_t nvec = (int64_t)HG * D * ES / 16;  // 16-byte vectors of the slice
+    const int64_t src0 = (rq * p.kv_heads + (int64_t)hgi * HG) * D * ES / 16;
+    const int64_t dst0 = (s * p.kv_heads + (int64_t)hgi * HG) * D * ES / 16;
+    const uint4* kn = static_cast<const uint4*>(p.k_new);
+    const uint4* vn = static_cast<const uint4*>(p.v_new);
+    uint4* kd = static_cast<uint4*>(const_cast<void*>(p.k_pool));
+    uint4* vd = static_cast<uint4*>(const_cast<void*>(p.v_pool));
+    for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+      kd[dst0 + i] = kn[src0 + i];
+      vd[dst0 + i] = vn[src0 + i];
+    }
+    wrote = true;
   }
-  const int64_t nvec = (int64_t)HG * D * ES / 16;  // 16-byte vectors of the slice
-  const int64_t src0 = ((int64_t)r * p.kv_heads + (int64_t)hgi * HG) * D * ES / 16;
-  const int64_t dst0 = (s * p.kv_heads + (int64_t)hgi * HG) * D * ES / 16;
-  const uint4* kn = static_cast<const uint4*>(p.k_new);
-  const uint4* vn = static_cast<const uint4*>(p.v_new);
-  uint4* kd = static_cast<uint4*>(const_cast<void*>(p.k_pool));
-  uint4* vd = static_cast<uint4*>(const_cast<void*>(p.v_pool));
-  for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
-    kd[dst0 + i] = kn[src0 + i];
-    vd[dst0 + i] = vn[src0 + i];
-  }
-  asm volatile("fence.proxy.async.global;" ::: "memory");
+  if (wrote) asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+#ifndef NPK_MMA_CT
+#define NPK_MMA_CT 16  // tokens per pipeline stage for 64 <= head_dim < 256
+#endif
+
+// Tokens per pipeline stage of the bf16 tensor-core read (host and device
+// agree on it: a TMA box never holds more tokens than a stage).  A stage
+// holds about 64 KB of K+V at 8 kv heads.
+__host__ __device__ constexpr int mma_chunk_tokens(int head_dim) {
+  return head_dim >= 256 ? 8 : (head_dim >= 64 ? NPK_MMA_CT : 32);
 }
 
 constexpr int kMaxConsumerWarps = 8;

@@ -18,6 +18,11 @@
 //                                      (the C layout of S^T is the B layout
 //                                      of P^T), so P never touches memory.
 //
+// With several query tokens per row (query_len Q, G*Q <= 16) the mma rows
+// are (query token, head) pairs, row = qi*G + h: one K/V fetch serves every
+// query token of the group; rows 8..15 use the second PV n-tile (TWO).  A
+// query token at position c - Q + qi only sees positions up to its own.
+//
 // Scores leave the tensor cores in fp32 and are scaled by scale*log2(e) there
 // (q stays exactly the stored bf16).  The online softmax keeps a running max
 // and sum per head in fp32; the 4 lanes that hold one head's scores reduce
@@ -69,18 +74,17 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-#ifndef NPK_MMA_CT
-#define NPK_MMA_CT 16  // tokens per pipeline stage for head_dim >= 64
-#endif
 #ifndef NPK_MMA_MIN_BLOCKS
 #define NPK_MMA_MIN_BLOCKS 1  // resident CTAs per SM the register budget targets
 #endif
+
+constexpr int kMmaRows = 16;  // mma M: (query token, head) rows per kv head
 
 template <int D, int G, bool TMAP>
 struct MmaCfg {
   static constexpr int KS = D / 16;  // mma k-steps over head_dim (QK), m-tiles (PV)
   static constexpr int ST = 16;      // tokens per softmax tile
-  static constexpr int CT = D >= 64 ? NPK_MMA_CT : 32;  // tokens per stage
+  static constexpr int CT = mma_chunk_tokens(D);  // tokens per stage
   // CT < ST is allowed: the tile's rows past the chunk are masked and their
   // shared-memory reads are redirected to the tile's first row.
   static_assert(D % 16 == 0 && G >= 1 && G <= 8, "shape");
@@ -97,7 +101,7 @@ struct MmaSmem {
     return TMAP ? 2ull * C::CT * hg * D * 2 : 2ull * C::CT * row_stride(hg);
   }
   __host__ __device__ static constexpr size_t merge_bytes(int warps) {
-    return (size_t)warps * G * (D + 2) * sizeof(float);
+    return (size_t)warps * kMmaRows * (D + 2) * sizeof(float);
   }
   __host__ __device__ static constexpr size_t ring_bytes(int hg, int stages, int warps) {
     size_t ring = stage_bytes(hg) * stages;
@@ -110,7 +114,26 @@ struct MmaSmem {
   }
 };
 
-template <int D, int G, bool TMAP>
+// One online-softmax row update for a 4-score slice (two token pairs) held by
+// the 4 lanes of a fragment row group.  Returns alpha (the rescale of the
+// row's running output); writes the probabilities into sc.  A row with no
+// visible token yet keeps m = -inf and gets alpha = p = 0 (no -inf - -inf).
+__device__ __forceinline__ float softmax_row(float (&sc)[4], float& m_run, float& l_run) {
+  constexpr unsigned FULL = 0xffffffffu;
+  float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+  mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 1));
+  mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 2));
+  const float mn = fmaxf(m_run, mt);
+  const float mref = (mn == -INFINITY) ? 0.f : mn;
+  const float alpha = ex2(m_run - mref);
+  m_run = mn;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) sc[e] = ex2(sc[e] - mref);
+  l_run = fmaf(l_run, alpha, (sc[0] + sc[1]) + (sc[2] + sc[3]));
+  return alpha;
+}
+
+template <int D, int G, bool TMAP, bool TWO>
 __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
     paged_decode_mma_kernel(const __grid_constant__ DecodeParams p) {
   using C = MmaCfg<D, G, TMAP>;
@@ -126,6 +149,8 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int hq0 = hgi * HG * G;
+  const int Q = p.query_len;
+  const int MR = G * Q;  // real mma rows (<= 16)
 
   const int64_t cap = (int64_t)p.max_blocks_per_row * p.block_size;
   int64_t c = p.context_lens[r];
@@ -139,12 +164,15 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
   fused_append<D, 2>(p, r, hgi, HG, c, t0, t1);
 
   if (t0 >= t1) {
-    if (p.num_splits > 1) {
-      for (int i = threadIdx.x; i < HG * G; i += blockDim.x)
-        p.ws_lse[((int64_t)r * p.q_heads + hq0 + i) * p.num_splits + split] = -INFINITY;
-    } else {
-      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + ((int64_t)r * p.q_heads + hq0) * D;
-      for (int i = threadIdx.x; i < HG * G * D; i += blockDim.x) o[i] = __float2bfloat16_rn(0.f);
+    for (int qi = 0; qi < Q; ++qi) {
+      const int64_t rq = (int64_t)r * Q + qi;
+      if (p.num_splits > 1) {
+        for (int i = threadIdx.x; i < HG * G; i += blockDim.x)
+          p.ws_lse[(rq * p.q_heads + hq0 + i) * p.num_splits + split] = -INFINITY;
+      } else {
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + (rq * p.q_heads + hq0) * D;
+        for (int i = threadIdx.x; i < HG * G * D; i += blockDim.x) o[i] = __float2bfloat16_rn(0.f);
+      }
     }
     return;
   }
@@ -175,12 +203,21 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
   // TMAP layout of a stage: [K | V] x [D/64 slabs of 64 dims] x [CT/B boxes]
   //                         x [HG heads] x [B token rows of 128 bytes]
   const int BT = TMAP ? p.box_tokens : 1;
+  if (TMAP && (BT < 1 || BT > C::CT || C::CT % BT != 0)) {
+    // a box must fit its stage; the host never launches otherwise
+    if (threadIdx.x == 0) set_flag(p.err, NP_FLAG_CONFIG);
+    return;
+  }
   const uint32_t half_bytes = (uint32_t)C::CT * HG * 128;  // one 64-dim slab of a chunk
   const uint32_t box_bytes = (uint32_t)BT * HG * 128;      // one box within a slab
   const uint32_t RS = (uint32_t)S::row_stride(HG);         // padded layout
 
-  float m_run = -INFINITY, l_run = 0.f;
-  float o[C::KS][4];  // O^T fragments: rows d = 16*mi + lane/4 (+8), cols h = 2*(lane%4) (+1)
+  // running softmax state of this lane's two fragment rows (g4 and g4 + 8)
+  float mA = -INFINITY, lA = 0.f, mB = -INFINITY, lB = 0.f;
+  // O^T fragments: rows d = 16*mi + lane/4 (+8); columns = mma rows
+  // 2*(lane%4) (+1) in oA, 8 + 2*(lane%4) (+1) in oB
+  float oA[C::KS][4];
+  float oB[TWO ? C::KS : 1][4];
 
   if (warp == NC) {
     // ======================= producer warp
@@ -265,29 +302,43 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
     const int hl = warp % HG;
     const int tw = warp / HG;
     const int kvh = hgi * HG + hl;
-    const int g4 = lane >> 2;  // fragment row group
+    const int g4 = lane >> 2;  // fragment row group: mma rows g4 and g4 + 8
     const int c4 = lane & 3;   // fragment column pair
 
-    // q as mma A fragments (rows = query heads of this group; rows >= G zero)
-    uint32_t qa0[C::KS], qa2[C::KS];
+    // q as mma A fragments; row = qi*G + h, rows >= MR zero.  The last
+    // position row `row` may see: c - Q + qi.
+    uint32_t qa0[C::KS], qa2[C::KS], qa1[TWO ? C::KS : 1], qa3[TWO ? C::KS : 1];
+    auto qrow = [&](int row) -> const __nv_bfloat16* {
+      const int qi = row / G, h = row - (row / G) * G;
+      return static_cast<const __nv_bfloat16*>(p.q) +
+             (((int64_t)r * Q + qi) * p.q_heads + kvh * G + h) * D;
+    };
+    const bool liveA = g4 < MR, liveB = g4 + 8 < MR;
+    const int64_t limA = liveA ? c - Q + g4 / G : -1;
+    const int64_t limB = liveB ? c - Q + (g4 + 8) / G : -1;
     {
-      const __nv_bfloat16* qrow =
-          static_cast<const __nv_bfloat16*>(p.q) + ((int64_t)r * p.q_heads + kvh * G) * D;
+      const __nv_bfloat16* qa = liveA ? qrow(g4) : nullptr;
 #pragma unroll
       for (int ks = 0; ks < C::KS; ++ks) {
-        if (g4 < G) {
-          qa0[ks] = *reinterpret_cast<const uint32_t*>(qrow + g4 * D + 16 * ks + 2 * c4);
-          qa2[ks] = *reinterpret_cast<const uint32_t*>(qrow + g4 * D + 16 * ks + 8 + 2 * c4);
-        } else {
-          qa0[ks] = 0u;
-          qa2[ks] = 0u;
+        qa0[ks] = liveA ? *reinterpret_cast<const uint32_t*>(qa + 16 * ks + 2 * c4) : 0u;
+        qa2[ks] = liveA ? *reinterpret_cast<const uint32_t*>(qa + 16 * ks + 8 + 2 * c4) : 0u;
+      }
+      if constexpr (TWO) {
+        const __nv_bfloat16* qb = liveB ? qrow(g4 + 8) : nullptr;
+#pragma unroll
+        for (int ks = 0; ks < C::KS; ++ks) {
+          qa1[ks] = liveB ? *reinterpret_cast<const uint32_t*>(qb + 16 * ks + 2 * c4) : 0u;
+          qa3[ks] = liveB ? *reinterpret_cast<const uint32_t*>(qb + 16 * ks + 8 + 2 * c4) : 0u;
         }
       }
     }
 #pragma unroll
     for (int mi = 0; mi < C::KS; ++mi)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) o[mi][e] = 0.f;
+      for (int e = 0; e < 4; ++e) {
+        oA[mi][e] = 0.f;
+        if constexpr (TWO) oB[mi][e] = 0.f;
+      }
 
     // ldmatrix lane addressing: matrix (lane/8) covers tokens 8*(lane/16) +
     // (0..7) and the 8-dim column chunk (lane/8)%2 of a 16-dim step; the same
@@ -302,7 +353,8 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
         set_flag(p.err, NP_FLAG_TIMEOUT);
         break;
       }
-      const int nvalid = (int)min((int64_t)C::CT, t1 - (t0 + ch * C::CT));
+      const int64_t tch = t0 + ch * C::CT;  // position of the chunk's first token
+      const int nvalid = (int)min((int64_t)C::CT, t1 - tch);
       const uint32_t kst = smem_u32(smem + st * stage_bytes);
       const uint32_t vst = kst + (uint32_t)(stage_bytes / 2);
 
@@ -334,38 +386,62 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
         for (int ks = 0; ks < C::KS; ++ks) {
           uint32_t b0, b1, b2, b3;
           ldsm_x4(chunk_addr(kst, ks), b0, b1, b2, b3);
-          mma_bf16(s0, qa0[ks], 0u, qa2[ks], 0u, b0, b1);
-          mma_bf16(s1, qa0[ks], 0u, qa2[ks], 0u, b2, b3);
+          if constexpr (TWO) {
+            mma_bf16(s0, qa0[ks], qa1[ks], qa2[ks], qa3[ks], b0, b1);
+            mma_bf16(s1, qa0[ks], qa1[ks], qa2[ks], qa3[ks], b2, b3);
+          } else {
+            mma_bf16(s0, qa0[ks], 0u, qa2[ks], 0u, b0, b1);
+            mma_bf16(s1, qa0[ks], 0u, qa2[ks], 0u, b2, b3);
+          }
         }
-        // ---- online softmax (this lane: head g4, tokens 2*c4+{0,1} and 8+2*c4+{0,1})
-        float sc[4] = {s0[0] * p.qscale, s0[1] * p.qscale, s1[0] * p.qscale, s1[1] * p.qscale};
-        const int tb = sb + 2 * c4;
-        if (tb >= nvalid) sc[0] = -INFINITY;
-        if (tb + 1 >= nvalid) sc[1] = -INFINITY;
-        if (tb + 8 >= nvalid) sc[2] = -INFINITY;
-        if (tb + 9 >= nvalid) sc[3] = -INFINITY;
-        float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-        mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 1));
-        mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 2));
-        const float mn = fmaxf(m_run, mt);
-        const float alpha = ex2(m_run - mn);
-        m_run = mn;
-        float pr[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) pr[e] = ex2(sc[e] - mn);
-        l_run = fmaf(l_run, alpha, (pr[0] + pr[1]) + (pr[2] + pr[3]));
-        const uint32_t pb0 = pack_bf16(pr[0], pr[1]);
-        const uint32_t pb1 = pack_bf16(pr[2], pr[3]);
-        // ---- rescale O^T columns (heads 2*c4, 2*c4+1) when some max moved
-        if (__any_sync(FULL, alpha != 1.f)) {
-          const float a_lo = __shfl_sync(FULL, alpha, 8 * c4);
-          const float a_hi = __shfl_sync(FULL, alpha, 8 * c4 + 4);
+        // ---- masks: token (tile-local) 2*c4 + {0, 1, 8, 9} must be a valid
+        // token of the chunk and at or before the row's own position
+        const int lt = sb + 2 * c4;
+        const int64_t pos = tch + lt;
+        const bool v0 = lt < nvalid, v1 = lt + 1 < nvalid, v8 = lt + 8 < nvalid,
+                   v9 = lt + 9 < nvalid;
+        float sa[4] = {s0[0] * p.qscale, s0[1] * p.qscale, s1[0] * p.qscale, s1[1] * p.qscale};
+        if (!(v0 && pos <= limA)) sa[0] = -INFINITY;
+        if (!(v1 && pos + 1 <= limA)) sa[1] = -INFINITY;
+        if (!(v8 && pos + 8 <= limA)) sa[2] = -INFINITY;
+        if (!(v9 && pos + 9 <= limA)) sa[3] = -INFINITY;
+        const float alphaA = softmax_row(sa, mA, lA);
+        const uint32_t pa0 = pack_bf16(sa[0], sa[1]);
+        const uint32_t pa1 = pack_bf16(sa[2], sa[3]);
+        float alphaB = 1.f;
+        uint32_t pb0 = 0u, pb1 = 0u;
+        if constexpr (TWO) {
+          float sbv[4] = {s0[2] * p.qscale, s0[3] * p.qscale, s1[2] * p.qscale,
+                          s1[3] * p.qscale};
+          if (!(v0 && pos <= limB)) sbv[0] = -INFINITY;
+          if (!(v1 && pos + 1 <= limB)) sbv[1] = -INFINITY;
+          if (!(v8 && pos + 8 <= limB)) sbv[2] = -INFINITY;
+          if (!(v9 && pos + 9 <= limB)) sbv[3] = -INFINITY;
+          alphaB = softmax_row(sbv, mB, lB);
+          pb0 = pack_bf16(sbv[0], sbv[1]);
+          pb1 = pack_bf16(sbv[2], sbv[3]);
+        }
+        // ---- rescale O^T columns (mma rows 2*c4, 2*c4+1 and +8) when a max moved
+        if (__any_sync(FULL, alphaA != 1.f || alphaB != 1.f)) {
+          const float a_lo = __shfl_sync(FULL, alphaA, 8 * c4);
+          const float a_hi = __shfl_sync(FULL, alphaA, 8 * c4 + 4);
 #pragma unroll
           for (int mi = 0; mi < C::KS; ++mi) {
-            o[mi][0] *= a_lo;
-            o[mi][1] *= a_hi;
-            o[mi][2] *= a_lo;
-            o[mi][3] *= a_hi;
+            oA[mi][0] *= a_lo;
+            oA[mi][1] *= a_hi;
+            oA[mi][2] *= a_lo;
+            oA[mi][3] *= a_hi;
+          }
+          if constexpr (TWO) {
+            const float b_lo = __shfl_sync(FULL, alphaB, 8 * c4);
+            const float b_hi = __shfl_sync(FULL, alphaB, 8 * c4 + 4);
+#pragma unroll
+            for (int mi = 0; mi < C::KS; ++mi) {
+              oB[mi][0] *= b_lo;
+              oB[mi][1] *= b_hi;
+              oB[mi][2] *= b_lo;
+              oB[mi][3] *= b_hi;
+            }
           }
         }
         // ---- O^T += V^T P^T
@@ -373,38 +449,59 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
         for (int mi = 0; mi < C::KS; ++mi) {
           uint32_t a0, a1, a2, a3;
           ldsm_x4_t(chunk_addr(vst, mi), a0, a1, a2, a3);
-          mma_bf16(o[mi], a0, a1, a2, a3, pb0, pb1);
+          mma_bf16(oA[mi], a0, a1, a2, a3, pa0, pa1);
+          if constexpr (TWO) mma_bf16(oB[mi], a0, a1, a2, a3, pb0, pb1);
         }
       }
       __syncwarp();  // every lane's reads of this stage are done
       if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
     }
-    // the head's sum over its 4 lanes
-    l_run += __shfl_xor_sync(FULL, l_run, 1);
-    l_run += __shfl_xor_sync(FULL, l_run, 2);
+    // each row's sum over its 4 lanes
+    lA += __shfl_xor_sync(FULL, lA, 1);
+    lA += __shfl_xor_sync(FULL, lA, 2);
+    lB += __shfl_xor_sync(FULL, lB, 1);
+    lB += __shfl_xor_sync(FULL, lB, 2);
   }
 
   // ======================= epilogue: stage (m, l, O) per warp, merge, store
   __syncthreads();  // (A) ring no longer in use
   float* merge = reinterpret_cast<float*>(smem);
-  const int stride_w = G * (D + 2);
+  constexpr int RW = kMmaRows;
+  const int stride_w = RW * (D + 2);
   if (warp < NC) {
     float* mg = merge + warp * stride_w;
-    if ((lane & 3) == 0 && (lane >> 2) < G) {
-      mg[lane >> 2] = m_run;
-      mg[G + (lane >> 2)] = l_run;
+    const int g4 = lane >> 2;
+    if ((lane & 3) == 0) {
+      if (g4 < MR) {
+        mg[g4] = mA;
+        mg[RW + g4] = lA;
+      }
+      if (TWO && g4 + 8 < MR) {
+        mg[g4 + 8] = mB;
+        mg[RW + g4 + 8] = lB;
+      }
     }
-    const int h0 = 2 * (lane & 3);
+    const int c0 = 2 * (lane & 3);  // mma rows of this lane's O^T columns
 #pragma unroll
     for (int mi = 0; mi < C::KS; ++mi) {
-      const int d = 16 * mi + (lane >> 2);
-      if (h0 < G) {
-        mg[2 * G + h0 * D + d] = o[mi][0];
-        mg[2 * G + h0 * D + d + 8] = o[mi][2];
+      const int d = 16 * mi + g4;
+      if (c0 < MR) {
+        mg[2 * RW + c0 * D + d] = oA[mi][0];
+        mg[2 * RW + c0 * D + d + 8] = oA[mi][2];
       }
-      if (h0 + 1 < G) {
-        mg[2 * G + (h0 + 1) * D + d] = o[mi][1];
-        mg[2 * G + (h0 + 1) * D + d + 8] = o[mi][3];
+      if (c0 + 1 < MR) {
+        mg[2 * RW + (c0 + 1) * D + d] = oA[mi][1];
+        mg[2 * RW + (c0 + 1) * D + d + 8] = oA[mi][3];
+      }
+      if constexpr (TWO) {
+        if (c0 + 8 < MR) {
+          mg[2 * RW + (c0 + 8) * D + d] = oB[mi][0];
+          mg[2 * RW + (c0 + 8) * D + d + 8] = oB[mi][2];
+        }
+        if (c0 + 9 < MR) {
+          mg[2 * RW + (c0 + 9) * D + d] = oB[mi][1];
+          mg[2 * RW + (c0 + 9) * D + d + 8] = oB[mi][3];
+        }
       }
     }
   }
@@ -414,22 +511,24 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
   const int kvh = hgi * HG + hl;
   constexpr int DL = D >= 32 ? D / 32 : 1;  // dims per lane
   const int d0 = lane * DL;
-  for (int h = 0; h < G; ++h) {
+  for (int row = 0; row < MR; ++row) {
     float mm = -INFINITY;
-    for (int w2 = 0; w2 < TW; ++w2) mm = fmaxf(mm, merge[(hl + w2 * HG) * stride_w + h]);
+    for (int w2 = 0; w2 < TW; ++w2) mm = fmaxf(mm, merge[(hl + w2 * HG) * stride_w + row]);
     float ll = 0.f;
     float acc[DL];
 #pragma unroll
     for (int e = 0; e < DL; ++e) acc[e] = 0.f;
     for (int w2 = 0; w2 < TW; ++w2) {
       const float* mg = merge + (hl + w2 * HG) * stride_w;
-      const float a = (mg[h] == -INFINITY) ? 0.f : ex2(mg[h] - mm);
-      ll = fmaf(mg[G + h], a, ll);
+      const float a = (mg[row] == -INFINITY) ? 0.f : ex2(mg[row] - mm);
+      ll = fmaf(mg[RW + row], a, ll);
       if (d0 < D) {
 #pragma unroll
-        for (int e = 0; e < DL; ++e) acc[e] = fmaf(mg[2 * G + h * D + d0 + e], a, acc[e]);
+        for (int e = 0; e < DL; ++e) acc[e] = fmaf(mg[2 * RW + row * D + d0 + e], a, acc[e]);
       }
     }
+    const int qi = row / G, h = row - qi * G;
+    const int64_t rq = (int64_t)r * Q + qi;
     const int hq = kvh * G + h;
     const float inv = ll > 0.f ? 1.f / ll : 0.f;
     float ov[DL];
@@ -437,11 +536,10 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
     for (int e = 0; e < DL; ++e) ov[e] = acc[e] * inv;
     if (d0 < D) {
       if (p.num_splits == 1) {
-        __nv_bfloat16* orow =
-            static_cast<__nv_bfloat16*>(p.out) + ((int64_t)r * p.q_heads + hq) * D;
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + (rq * p.q_heads + hq) * D;
         Storage<__nv_bfloat16>::template store<DL>(orow + d0, ov);
       } else {
-        const int64_t rs = ((int64_t)r * p.q_heads + hq) * p.num_splits + split;
+        const int64_t rs = (rq * p.q_heads + hq) * p.num_splits + split;
         float* orow = p.ws_o + rs * D + d0;
         if constexpr (DL >= 4) {
 #pragma unroll

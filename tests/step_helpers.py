@@ -19,7 +19,8 @@ def gpu_step(npg, inp: wl.Inputs, num_splits: int | None = None, append: bool = 
     if num_splits is None:
         num_splits = npg.np_paged_decode_plan(w.rows, w.q_heads, w.kv_heads, w.head_dim,
                                               w.block_size, bt.shape[1], w.torch_dtype)
-    ws = npg.workspace(w.rows, w.q_heads, w.head_dim, num_splits, device=dev)
+    ws = npg.workspace(w.rows, w.q_heads, w.head_dim, num_splits, device=dev,
+                       query_len=w.query_len)
     out = torch.full_like(inp.q, float("nan"))
     kw = dict(k_new=inp.k_new, v_new=inp.v_new, slot_mapping=sm) if append else {}
     npg.decode_step(out, inp.q, inp.k_pool, inp.v_pool, bt, cl, w.softmax_scale,
@@ -29,10 +30,17 @@ def gpu_step(npg, inp: wl.Inputs, num_splits: int | None = None, append: bool = 
     return out, num_splits, ws
 
 
+def oracle_append(kp, vp, host: dict) -> int:
+    """The step's append on the host copies (new tokens flattened to [T, Hk, D])."""
+    hk, d = kp.shape[2], kp.shape[3]
+    return oracle.kv_append(kp, vp, host["k_new"].reshape(-1, hk, d),
+                            host["v_new"].reshape(-1, hk, d), host["slot_mapping"].reshape(-1))
+
+
 def oracle_step(host: dict, scale: float, append: bool = True, **kw):
     kp, vp = host["k_pool"].copy(), host["v_pool"].copy()
     if append:
-        rc = oracle.kv_append(kp, vp, host["k_new"], host["v_new"], host["slot_mapping"])
+        rc = oracle_append(kp, vp, host)
         assert rc == oracle.OK
     return oracle.paged_decode(host["q"], kp, vp, host["block_tables"], host["context_lens"],
                                scale, **kw)

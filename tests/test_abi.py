@@ -56,11 +56,11 @@ def test_abi_version_and_status_strings(lib):
 
 def _decode(lib, **kw):
     a = dict(out=None, q=None, k=None, v=None, dtype=0, nb=16, bs=16, hk=2, d=128, bt=None,
-             mb=4, cl=None, rows=2, hq=4, scale=0.1, splits=1, ws=None, wsb=0, err=None)
+             mb=4, cl=None, rows=2, qlen=1, hq=4, scale=0.1, splits=1, ws=None, wsb=0, err=None)
     a.update(kw)
     return lib.np_paged_decode(a["out"], a["q"], a["k"], a["v"], a["dtype"], a["nb"], a["bs"],
-                               a["hk"], a["d"], a["bt"], a["mb"], a["cl"], a["rows"], a["hq"],
-                               a["scale"], a["splits"], a["ws"], a["wsb"], a["err"], None)
+                               a["hk"], a["d"], a["bt"], a["mb"], a["cl"], a["rows"], a["qlen"],
+                               a["hq"], a["scale"], a["splits"], a["ws"], a["wsb"], a["err"], None)
 
 
 FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced
@@ -84,6 +84,10 @@ def test_decode_validation(lib):
     assert _decode(lib, splits=4, **ok_ptrs) == 3            # no workspace
     assert _decode(lib, splits=4, ws=FAKE, wsb=100, **ok_ptrs) == 3
     assert _decode(lib, nb=2**62, **ok_ptrs) == 4            # pool bytes overflow
+    assert _decode(lib, qlen=0, **ok_ptrs) == 1              # no query token
+    assert _decode(lib, qlen=2, **ok_ptrs) == 2              # fp32: one query token only
+    assert _decode(lib, qlen=9, dtype=1, **ok_ptrs) == 2     # bf16: g*query_len > 16
+    assert _decode(lib, qlen=8, dtype=1, splits=4, **ok_ptrs) == 3   # workspace missing
 
 
 def test_append_validation(lib):

@@ -13,7 +13,7 @@ import torch
 import golden_cases
 import oracle
 import workloads as wl
-from step_helpers import assert_parity, gpu_step, oracle_step, to64
+from step_helpers import assert_parity, gpu_step, oracle_append, oracle_step, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -21,11 +21,11 @@ DEV = "cuda"
 
 
 def _custom(contexts, q_heads, kv_heads, head_dim, block_size, dtype, seed=11, spare=3,
-            scale=None):
+            scale=None, query_len=1):
     return wl.Workload(f"custom-{seed}", rows=len(contexts), q_heads=q_heads,
                        kv_heads=kv_heads, head_dim=head_dim, block_size=block_size,
                        dtype=dtype, ctx=("fixed", tuple(contexts)), pool=("spare", spare),
-                       seed=seed, scale=scale)
+                       seed=seed, scale=scale, query_len=query_len)
 
 
 def _full_parity(npg, w, num_splits=None, append=True, device=DEV, fused=True):
@@ -40,7 +40,7 @@ def _full_parity(npg, w, num_splits=None, append=True, device=DEV, fused=True):
     ref, _ = oracle_step(host, w.softmax_scale, append=append)
     if append:
         rk, rv = host["k_pool"].copy(), host["v_pool"].copy()
-        oracle.kv_append(rk, rv, host["k_new"], host["v_new"], host["slot_mapping"])
+        oracle_append(rk, rv, host)
         assert wl.host_array(dinp.k_pool).tobytes() == rk.tobytes(), "K pool after the step"
         assert wl.host_array(dinp.v_pool).tobytes() == rv.tobytes(), "V pool after the step"
     return assert_parity(out, ref, w.dtype, f"{w.name} splits={s} fused={fused}"), s
@@ -329,6 +329,39 @@ def test_fused_append_refuses_a_slot_that_is_not_the_newest_position(nplib):
         oracle.kv_append(rk, rv, host["k_new"][keep], host["v_new"][keep],
                          inp.slot_mapping.numpy()[keep])
         assert wl.host_array(d.k_pool).tobytes() == rk.tobytes()
+
+
+# ------------------------------------------------- several query tokens ----
+@pytest.mark.parametrize("group,query_len", [(1, 3), (1, 16), (2, 5), (4, 2), (4, 4), (5, 3),
+                                             (8, 2)])
+def test_multi_query_tokens(nplib, group, query_len):
+    """Each row's last query_len positions attend causally (bf16, tensor cores),
+    with the new tokens appended fused or separately, split or not; includes
+    rows shorter than the query run and runs crossing split boundaries."""
+    ctx = [1, query_len, query_len + 1, 63, 64, 65, 700, 1500]
+    w = _custom(ctx, 2 * group, 2, 128, 16, "bf16", seed=90 + group * 7 + query_len,
+                query_len=query_len)
+    for s in (1, 5):
+        _full_parity(nplib, w, num_splits=s)
+    _full_parity(nplib, w, num_splits=5, fused=False)
+
+
+@pytest.mark.parametrize("head_dim,block_size", [(64, 8), (256, 32), (32, 16)])
+def test_multi_query_head_dims(nplib, head_dim, block_size):
+    w = _custom([5, 80, 300], 16, 8, head_dim, block_size, "bf16", seed=130 + head_dim,
+                query_len=2)
+    _full_parity(nplib, w)
+    _full_parity(nplib, w, num_splits=3)
+
+
+def test_multi_query_workload_sampled(nplib):
+    _sampled_rows(nplib, "bf16-gqa4-q4", 6, fused=True)
+
+
+def test_head_dim_256_with_eight_kv_heads(nplib):
+    w = _custom([10, 700, 2500], 64, 8, 256, 32, "bf16", seed=140)
+    _full_parity(nplib, w)
+    _full_parity(nplib, w, num_splits=4)
 
 
 # ---------------------------------------------------------- robustness ----

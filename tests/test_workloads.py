@@ -28,10 +28,12 @@ def test_metadata_is_a_valid_allocation(name):
         used.append(row[:n])
     used = torch.cat(used)
     assert used.unique().numel() == used.numel(), "a block is shared by two rows"
-    c = cl.to(torch.int64) - 1
     bt = md.block_tables.to(torch.int64)
-    expect = bt[torch.arange(w.rows), c // w.block_size] * w.block_size + c % w.block_size
-    assert torch.equal(md.slot_mapping, expect)
+    sm = md.slot_mapping.reshape(w.rows, w.query_len)
+    for j in range(w.query_len):  # new token j sits at position c - query_len + j
+        c = cl.to(torch.int64) - w.query_len + j
+        expect = bt[torch.arange(w.rows), c // w.block_size] * w.block_size + c % w.block_size
+        assert torch.equal(sm[:, j], expect)
 
 
 def test_pool_sizes_match_the_configs():

@@ -50,6 +50,7 @@ class Workload:
     scale: float | None = None  # None -> 1/sqrt(head_dim)
     description: str = ""
     table_capacity: int | None = None  # tokens a block table can hold (default: max context)
+    query_len: int = 1  # new (query) tokens per row: its last query_len positions
 
     @property
     def group(self) -> int:
@@ -114,6 +115,12 @@ WORKLOADS: dict[str, Workload] = {
                  ctx=("loguniform", 16, 16384), pool=("spare", 256), seed=4,
                  description="bf16 ragged batch, contexts log-uniform "
                              "[16, 16384], block 32, append then read"),
+        Workload("bf16-gqa4-q4", rows=64, q_heads=32, kv_heads=8, head_dim=128,
+                 block_size=16, dtype="bf16", ctx=("uniform", 1024, 8192),
+                 pool=("factor", 1.25), seed=2, query_len=4,
+                 description="bf16-gqa4 with 4 query tokens per row (speculative "
+                             "decode): 4 new tokens appended, each attending "
+                             "causally"),
     ]
 }
 
@@ -167,7 +174,7 @@ def pool_blocks(w: Workload, needed_total: int) -> int:
 class Metadata:
     context_lens: torch.Tensor  # [rows] int32
     block_tables: torch.Tensor  # [rows, max_blocks_per_row] int32, unused = -1
-    slot_mapping: torch.Tensor  # [rows] int64: slot of each row's new token
+    slot_mapping: torch.Tensor  # [rows] (or [rows, query_len]) int64: new tokens' slots
     num_blocks: int
 
 
@@ -190,22 +197,24 @@ def metadata(w: Workload, context_lens: torch.Tensor | None = None,
     g = torch.Generator().manual_seed(w.seed * 104729 + 3)
     free_list = torch.randperm(nb, generator=g).to(torch.int32)
     bt = torch.full((w.rows, mb), unused_entry, dtype=torch.int32)
-    slots = torch.full((w.rows,), -1, dtype=torch.int64)
+    qn = w.query_len
+    slots = torch.full((w.rows, qn), -1, dtype=torch.int64)
     pos = 0
     for r, n in enumerate(needed):
         bt[r, :n] = free_list[pos:pos + n]
         pos += n
         c = int(cl[r])
-        if c > 0:
-            last = c - 1
-            slots[r] = int(bt[r, last // bs]) * bs + last % bs
-    return Metadata(cl, bt, slots, nb)
+        for j in range(qn):  # new token j is position c - qn + j
+            t = c - qn + j
+            if t >= 0:
+                slots[r, j] = int(bt[r, t // bs]) * bs + t % bs
+    return Metadata(cl, bt, slots[:, 0].clone() if qn == 1 else slots, nb)
 
 
 def history_slot_mask(w: Workload, md: Metadata, include_new: bool = False) -> torch.Tensor:
     """Bool [num_blocks * block_size]: True for slots holding a row's history.
 
-    Excludes each row's new-token slot unless ``include_new``.  Used only to
+    Excludes each row's new-token slots unless ``include_new``.  Used only to
     poison every other slot with NaN, so a read that touches a slot it should
     not shows up as a NaN in the output.
     """
@@ -213,7 +222,7 @@ def history_slot_mask(w: Workload, md: Metadata, include_new: bool = False) -> t
     mask = torch.zeros(md.num_blocks * bs, dtype=torch.bool)
     for r in range(w.rows):
         c = int(md.context_lens[r])
-        n = c if include_new else c - 1
+        n = c if include_new else c - w.query_len
         if n <= 0:
             continue
         nblk = -(-n // bs)
@@ -274,9 +283,10 @@ def make_inputs(w: Workload, device="cpu", *, poison: bool = True,
     dev = torch.device(device)
     gen = torch.Generator(device=dev).manual_seed(w.seed * 1000003 + 17)
     dt = w.torch_dtype
-    q = _normal((w.rows, w.q_heads, w.head_dim), gen, dev, dt)
-    k_new = _normal((w.rows, w.kv_heads, w.head_dim), gen, dev, dt)
-    v_new = _normal((w.rows, w.kv_heads, w.head_dim), gen, dev, dt)
+    lead = (w.rows,) if w.query_len == 1 else (w.rows, w.query_len)
+    q = _normal(lead + (w.q_heads, w.head_dim), gen, dev, dt)
+    k_new = _normal(lead + (w.kv_heads, w.head_dim), gen, dev, dt)
+    v_new = _normal(lead + (w.kv_heads, w.head_dim), gen, dev, dt)
     shape = (md.num_blocks, w.block_size, w.kv_heads, w.head_dim)
     k_pool = _normal(shape, gen, dev, dt)
     v_pool = _normal(shape, gen, dev, dt)
@@ -310,15 +320,20 @@ def row_subproblem(inp: Inputs, rows: list[int]) -> dict:
     cl = md.context_lens[rows]
     mb = max(1, max((-(-int(c) // bs)) for c in cl.tolist()))
     bt = torch.full((len(rows), mb), -1, dtype=torch.int32)
-    slots = torch.full((len(rows),), -1, dtype=torch.int64)
+    qn = w.query_len
+    slots = torch.full((len(rows), qn), -1, dtype=torch.int64)
     for i, r in enumerate(rows):
         c = int(md.context_lens[r])
         n = -(-c // bs)
         ids.append(md.block_tables[r, :n].to(torch.int64))
         bt[i, :n] = torch.arange(offs, offs + n, dtype=torch.int32)
-        if c > 0:
-            slots[i] = (offs + (c - 1) // bs) * bs + (c - 1) % bs
+        for j in range(qn):
+            t = c - qn + j
+            if t >= 0:
+                slots[i, j] = (offs + t // bs) * bs + t % bs
         offs += n
+    if qn == 1:
+        slots = slots[:, 0].clone()
     idx = torch.cat(ids) if ids else torch.zeros(0, dtype=torch.int64)
     if idx.numel() == 0:
         idx = torch.zeros(1, dtype=torch.int64)
