@@ -280,7 +280,7 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
     inp = wl.make_inputs(w, device=dev, poison=False)
     md = inp.md
     bt, cl, sm = (t.to(dev) for t in (md.block_tables, md.context_lens, md.slot_mapping))
-    S = args.splits or npg.np_paged_decode_plan(w.rows, w.q_heads, w.kv_heads, w.head_dim,
+    S = args.splits if args.splits is not None else npg.np_paged_decode_plan(w.rows, w.q_heads, w.kv_heads, w.head_dim,
                                                 w.block_size, bt.shape[1], w.torch_dtype)
     ws = npg.workspace(w.rows, w.q_heads, w.head_dim, S, device=dev, query_len=w.query_len)
     out = torch.empty_like(inp.q)
@@ -298,12 +298,12 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
         launches = 0
         if rec is not None:
             rec[0].record(stream)
-        npg.np_paged_append_decode(out if S == 1 else None, inp.q, inp.k_new, inp.v_new, sm,
+        npg.np_paged_append_decode(out if S <= 1 else None, inp.q, inp.k_new, inp.v_new, sm,
                                    inp.k_pool, inp.v_pool, bt, cl, w.softmax_scale, S, ws, err,
                                    stream)
         if rec is not None:
             rec[1].record(stream)
-        launches += 1
+        launches += 2 if S == 0 else 1  # the balanced read adds its merge launch
         if S > 1:
             npg.np_paged_decode_reduce(out, ws, S, stream)
             launches += 1
@@ -359,7 +359,7 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
     def e2e_step():
         for k in pin:
             dbuf[k].copy_(pin[k], non_blocking=True)
-        npg.np_paged_append_decode(out if S == 1 else None, dbuf["q"], dbuf["k_new"],
+        npg.np_paged_append_decode(out if S <= 1 else None, dbuf["q"], dbuf["k_new"],
                                    dbuf["v_new"], dbuf["sm"], inp.k_pool, inp.v_pool,
                                    dbuf["bt"], dbuf["cl"], w.softmax_scale, S, ws, err, stream)
         if S > 1:
@@ -407,7 +407,10 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
             "query_len": w.query_len,
             "block_size": w.block_size, "max_blocks_per_row": bt.shape[1],
             "num_blocks": md.num_blocks, "num_splits": S,
-            "split_len": npg.np_paged_decode_split_len(w.block_size, bt.shape[1], S),
+            "schedule": "balanced stream (one CTA per SM, equal token shares)" if S == 0
+            else f"split-K x{S}",
+            "split_len": npg.np_paged_decode_split_len(w.block_size, bt.shape[1], S) if S > 0
+            else None,
             "mean_context": float(md.context_lens.double().mean()),
             "kv_bytes_per_step": nbytes["kv"],
             "l2": ("inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2"
@@ -417,7 +420,9 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "paged_decode_mma_kernel" if w.dtype == "bf16" else "paged_decode_kernel",
+            "kernel": ("paged_decode_stream_kernel + its merge launch (timed together)"
+                       if S == 0 else "paged_decode_mma_kernel" if w.dtype == "bf16"
+                       else "paged_decode_kernel"),
             "achieved": achieved,
             "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
             if peak_kind == "measured" else "fallback 6.8 TB/s",

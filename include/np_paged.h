@@ -122,11 +122,12 @@ np_status np_kv_append(void* k_pool, void* v_pool, np_dtype dtype,
                        np_stream_t stream);
 
 /*
- * np_paged_decode_plan -- how many context splits the library recommends.
- * Pure host arithmetic on STATIC shapes only (never on context_lens, so the
- * choice needs no device read and a step stays graph-capturable).
- * num_sms <= 0 queries the current device's SM count.
- * Writes the split count (>= 1) to *num_splits.
+ * np_paged_decode_plan -- the schedule the library recommends, as a
+ * num_splits value for np_paged_decode.  Pure host arithmetic on STATIC
+ * shapes only (never on context_lens, so the choice needs no device read and
+ * a step stays graph-capturable).  num_sms <= 0 queries the current device's
+ * SM count.  Writes 0 (the balanced read) when the shapes allow it, else a
+ * split count >= 1 sized to about 2 MB of K+V per thread block.
  */
 np_status np_paged_decode_plan(int32_t rows, int32_t q_heads, int32_t kv_heads,
                                int32_t head_dim, int32_t block_size,
@@ -144,12 +145,16 @@ int64_t np_paged_decode_split_len(int32_t block_size,
                                   int32_t num_splits);
 
 /*
- * np_paged_decode_workspace_bytes -- workspace a split read needs:
- *   partial outputs  [rows, q_heads, num_splits, head_dim] fp32 at offset 0,
- *   partial lse      [rows, q_heads, num_splits] fp32 at the next 256-byte
- *                    boundary (natural log; -inf for an empty split).
- * For query_len > 1 pass rows * query_len as `rows`.
- * 0 when num_splits <= 1.
+ * np_paged_decode_workspace_bytes -- workspace a read needs:
+ *   num_splits > 1: partial outputs [rows, q_heads, num_splits, head_dim]
+ *                   fp32 at offset 0, partial lse [rows, q_heads,
+ *                   num_splits] fp32 at the next 256-byte boundary (natural
+ *                   log; -inf for an empty split).  For query_len > 1 pass
+ *                   rows * query_len as `rows`.
+ *   num_splits == 0 (balanced read): a fixed size that depends on head_dim
+ *                   only (partials of the rows cut between thread blocks);
+ *                   its layout is private to the library.
+ *   0 when num_splits == 1.  No read needs the workspace initialised.
  */
 size_t np_paged_decode_workspace_bytes(int32_t rows, int32_t q_heads,
                                        int32_t head_dim, int32_t num_splits);
@@ -168,13 +173,23 @@ size_t np_paged_decode_workspace_bytes(int32_t rows, int32_t q_heads,
  *   context_lens   [rows] int32: history length of each row (including any
  *                  token appended this step); 0 gives an all-zero output
  *   scale          softmax scale applied to q.k (finite)
- *   num_splits     >= 1.  1: out is written directly.  > 1: split s of row r
+ *   num_splits     >= 0.  1: out is written directly.  > 1: split s of row r
  *                  (tokens [s*split_len, (s+1)*split_len), see
  *                  np_paged_decode_split_len) writes its normalised partial
  *                  output and lse into `workspace`; call
  *                  np_paged_decode_reduce next to produce out.
+ *                  0: the balanced read -- one thread block per SM (at most
+ *                  256), each taking an equal, chunk-aligned share of all
+ *                  rows' history laid end to end (computed on the device
+ *                  from context_lens); rows cut between blocks are merged
+ *                  by a second launch on `stream`, in block order (results
+ *                  are deterministic).  out is written; no reduce call.
+ *                  Needs bf16, head_dim a multiple of 64, kv_heads a
+ *                  multiple of 8, rows * kv_heads / 8 <= 4096 and a workspace
+ *                  (else NP_ERR_UNSUPPORTED / NP_ERR_WORKSPACE).
+ *                  Results equal the split read's up to fp32 rounding order.
  *   workspace      device buffer of >= np_paged_decode_workspace_bytes(...)
- *                  bytes (may be NULL when num_splits == 1)
+ *                  bytes, 256-byte aligned (may be NULL when num_splits == 1)
  *   err_word       device int32 or NULL (NP_FLAG_BLOCK_ID, NP_FLAG_CONTEXT,
  *                  NP_FLAG_TIMEOUT)
  * Memory traffic: each history token's K and V rows are read once from HBM;

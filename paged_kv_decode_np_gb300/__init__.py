@@ -12,12 +12,15 @@ Typical decode step::
     import paged_kv_decode_np_gb300 as npg
     S = npg.np_paged_decode_plan(rows, q_heads, kv_heads, head_dim, block_size,
                                  max_blocks_per_row, torch.bfloat16)
-    ws = npg.workspace(rows, q_heads, head_dim, S, device="cuda")
-    npg.np_kv_append(k_pool, v_pool, k_new, v_new, slot_mapping)
-    npg.np_paged_decode(out, q, k_pool, v_pool, block_tables, context_lens,
-                        scale, num_splits=S, workspace=ws)
+    ws = npg.workspace(rows, q_heads, head_dim, S, device="cuda")   # zeroed
+    npg.np_paged_append_decode(out if S <= 1 else None, q, k_new, v_new,
+                               slot_mapping, k_pool, v_pool, block_tables,
+                               context_lens, scale, num_splits=S, workspace=ws)
     if S > 1:
         npg.np_paged_decode_reduce(out, ws, num_splits=S)
+
+S == 0 (the balanced read) writes ``out`` itself; S > 1 leaves split
+partials for np_paged_decode_reduce.
 """
 from __future__ import annotations
 
@@ -211,11 +214,12 @@ def np_paged_decode_workspace_bytes(rows, q_heads, head_dim, num_splits) -> int:
 
 def workspace(rows, q_heads, head_dim, num_splits, device="cuda",
               query_len: int = 1) -> torch.Tensor | None:
-    """A torch-allocated workspace of the size the library asks for (None if unsplit)."""
+    """A workspace of the size the library asks for (None if unsplit).  No
+    call needs its contents initialised; zero-filled only to be reproducible."""
     n = np_paged_decode_workspace_bytes(rows * query_len, q_heads, head_dim, num_splits)
     if n == 0:
         return None
-    return torch.empty(n, dtype=torch.uint8, device=device)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
 def _check_read_args(call, out, q, k_pool, v_pool, block_tables, context_lens):
@@ -321,7 +325,7 @@ def decode_step(out, q, k_pool, v_pool, block_tables, context_lens, scale, *, k_
     np_kv_append runs first.  Returns the number of library kernels launched.
     """
     launches = 0
-    o = out if num_splits == 1 else None
+    o = out if num_splits <= 1 else None  # 0: the balanced read writes out itself
     if k_new is not None and fused and k_new.shape[0] == q.shape[0] and \
             k_new.dim() == q.dim():
         np_paged_append_decode(o, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables,

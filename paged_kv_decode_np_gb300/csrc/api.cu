@@ -12,6 +12,7 @@
 
 #include "decode_kernel.cuh"
 #include "decode_launch.h"
+#include "decode_stream.cuh"
 #include "np_paged.h"
 
 #ifndef NPK_SPLIT_BYTES
@@ -78,6 +79,16 @@ np_status device_info(int* sms, int* smem) {
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Shapes the balanced streamed read (num_splits == 0) handles: bf16 pools,
+// head_dim a multiple of 64, kv heads in groups of 8, at most
+// kStreamMaxVRows (row, head group) pairs, contexts that fit int32.
+bool stream_ok(np_dtype dtype, int32_t head_dim, int32_t kv_heads, int32_t rows,
+               int32_t max_blocks_per_row, int32_t block_size) {
+  return dtype == NP_BF16 && head_dim % 64 == 0 && kv_heads % 8 == 0 &&
+         (int64_t)rows * (kv_heads / 8) <= npk::kStreamMaxVRows &&
+         (int64_t)max_blocks_per_row * block_size <= INT32_MAX;
+}
 
 // ---- tiled TMA maps of the pools (bf16, head_dim a multiple of 64)
 // The driver's encoder is reached through the runtime (no libcuda link).
@@ -239,6 +250,10 @@ np_status np_paged_decode_plan(int32_t rows, int32_t q_heads, int32_t kv_heads,
   if (rows < 0 || q_heads <= 0 || kv_heads <= 0 || q_heads % kv_heads != 0 || head_dim <= 0 ||
       block_size <= 0 || max_blocks_per_row <= 0)
     return NP_ERR_INVALID_ARG;
+  if (stream_ok(dtype, head_dim, kv_heads, rows, max_blocks_per_row, block_size)) {
+    *num_splits = 0;  // the balanced streamed read
+    return NP_OK;
+  }
   if (num_sms <= 0) {
     int smem = 0;
     np_status st = device_info(&num_sms, &smem);
@@ -269,7 +284,10 @@ np_status np_paged_decode_plan(int32_t rows, int32_t q_heads, int32_t kv_heads,
 
 size_t np_paged_decode_workspace_bytes(int32_t rows, int32_t q_heads, int32_t head_dim,
                                        int32_t num_splits) {
-  if (num_splits <= 1 || rows <= 0 || q_heads <= 0 || head_dim <= 0) return 0;
+  if (rows <= 0 || q_heads <= 0 || head_dim <= 0 || num_splits < 0) return 0;
+  if (num_splits == 0)  // balanced streamed read
+    return round_up(npk::StreamWs::bytes(head_dim), 256);
+  if (num_splits == 1) return 0;
   const size_t units = (size_t)rows * q_heads * num_splits;
   return round_up(units * head_dim * sizeof(float), 256) + round_up(units * sizeof(float), 256);
 }
@@ -289,7 +307,7 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
   const int es = elem_size(dtype);
   if (es == 0) return NP_ERR_UNSUPPORTED;
   if (rows < 0 || query_len <= 0 || q_heads <= 0 || kv_heads <= 0 || q_heads % kv_heads != 0 ||
-      num_blocks <= 0 || block_size <= 0 || max_blocks_per_row <= 0 || num_splits <= 0 ||
+      num_blocks <= 0 || block_size <= 0 || max_blocks_per_row <= 0 || num_splits < 0 ||
       num_splits > 65535 || !isfinite(scale))
     return NP_ERR_INVALID_ARG;
   if (!head_dim_supported(head_dim) || !group_supported(q_heads / kv_heads))
@@ -306,14 +324,24 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
   if (rows > 65535) return NP_ERR_UNSUPPORTED;  // grid.y
   if (rows == 0) return NP_OK;
   if (!q || !k_pool || !v_pool || !block_tables || !context_lens) return NP_ERR_INVALID_ARG;
-  if (num_splits == 1 && !out) return NP_ERR_INVALID_ARG;
+  if (num_splits <= 1 && !out) return NP_ERR_INVALID_ARG;
+  const bool streamed = num_splits == 0;
+  if (streamed && !stream_ok(dtype, head_dim, kv_heads, rows, max_blocks_per_row, block_size))
+    return NP_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
       (out && !aligned(out, 16)) || !aligned(block_tables, 4) || !aligned(context_lens, 4) ||
       (err_word && !aligned(err_word, 4)))
     return NP_ERR_INVALID_ARG;
   float* ws_o = nullptr;
   float* ws_lse = nullptr;
-  if (num_splits > 1) {
+  int64_t* st_pts = nullptr;
+  if (streamed) {
+    const size_t need = npk::StreamWs::bytes(head_dim);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return NP_ERR_WORKSPACE;
+    ws_o = static_cast<float*>(workspace);
+    st_pts = reinterpret_cast<int64_t*>(static_cast<char*>(workspace) +
+                                        npk::StreamWs::parts_bytes(head_dim));
+  } else if (num_splits > 1) {
     const int32_t units_rows = rows * query_len;  // rows of the partial layout
     const size_t need =
         np_paged_decode_workspace_bytes(units_rows, q_heads, head_dim, num_splits);
@@ -339,7 +367,8 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
   p.context_lens = context_lens;
   p.err = err_word;
   p.num_blocks = num_blocks;
-  p.split_len = np_paged_decode_split_len(block_size, max_blocks_per_row, num_splits);
+  p.split_len =
+      streamed ? 0 : np_paged_decode_split_len(block_size, max_blocks_per_row, num_splits);
   p.block_size = block_size;
   p.kv_heads = kv_heads;
   p.head_group = hg;
@@ -353,6 +382,8 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
   p.v_new = v_new;
   p.slot_mapping = slot_mapping;
   p.query_len = query_len;
+  p.rows = rows;
+  p.st_pts = st_pts;
   // bf16 pools with head_dim a multiple of 64 stage K/V through tiled TMA
   // boxes of box_tokens tokens: the largest power of two dividing the block
   // size, at most the stage's token count, with box_tokens * head_group a
@@ -379,6 +410,11 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
   L.rows = rows;
   L.splits = num_splits;
   L.head_groups = kv_heads / hg;
+  L.streamed = streamed;
+  if (streamed) {
+    if (!p.use_tmap) return NP_ERR_UNSUPPORTED;  // the streamed read stages through TMA maps
+    L.splits = sms < npk::kStreamMaxCtas ? sms : npk::kStreamMaxCtas;
+  }
   L.smem_budget = NPK_SMEM_BUDGET > 0 && NPK_SMEM_BUDGET < smem_optin ? NPK_SMEM_BUDGET
                                                                       : (size_t)smem_optin;
   L.stream = reinterpret_cast<cudaStream_t>(stream);

@@ -4,6 +4,7 @@
 #include "decode_kernel.cuh"
 #include "decode_launch.h"
 #include "decode_mma.cuh"
+#include "decode_stream.cuh"
 
 #ifndef NPK_BF16
 #error "define NPK_BF16"
@@ -77,10 +78,61 @@ np_status launch_variant(DecodeLaunch& L, DecodeParams& p) {
   return cudaGetLastError() == cudaSuccess ? NP_OK : NP_ERR_CUDA;
 }
 
+#if NPK_BF16 && (NPK_D % 64 == 0)
+// The balanced streamed read: grid = L.splits CTAs (one per SM), 8 kv heads
+// per CTA, the virtual-row prefix in shared memory after the ring.
+template <int G, bool TWO>
+np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
+  using SS = StreamSmem<NPK_D, G>;
+  using SM = MmaSmem<NPK_D, G, true>;
+  const int vrows = p.rows * (p.kv_heads / 8);
+  // static shared memory of the kernel (scan scratch) comes off the budget
+  const size_t budget = L.smem_budget - 4096;
+  size_t stages = 8;
+  while (stages >= 2 && SS::total((int)stages, vrows) > budget) --stages;
+  if (stages < 2) return NP_ERR_UNSUPPORTED;
+  (void)sizeof(SM);
+  const size_t smem = SS::total((int)stages, vrows);
+  p.stages = (int)stages;
+  L.stages = (int)stages;
+  L.smem_bytes = smem;
+  auto kern = paged_decode_stream_kernel<NPK_D, G, TWO>;
+  static unsigned long long configured = 0;  // bit d: attribute set on device d
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NP_ERR_CUDA;
+  if (dev >= 64 || !((__atomic_load_n(&configured, __ATOMIC_ACQUIRE) >> dev) & 1ull)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget) !=
+        cudaSuccess)
+      return NP_ERR_CUDA;
+    if (dev < 64) __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
+  }
+  kern<<<L.splits, 32 * (8 + 1), smem, L.stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return NP_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.splits, G * p.query_len);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = NPK_STREAM_PDL;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, paged_decode_stream_merge_kernel<NPK_D, G>, p) != cudaSuccess)
+    return NP_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? NP_OK : NP_ERR_CUDA;
+}
+#endif
+
 // bf16: TWO when the (query token, head) rows spill past the first 8 mma
 // rows (G * query_len > 8).  fp32: one query token only (host-checked).
 template <int G>
 np_status launch_one(DecodeLaunch& L, DecodeParams& p) {
+#if NPK_BF16 && (NPK_D % 64 == 0)
+  if (L.streamed)
+    return G * p.query_len > 8 ? launch_stream<G, true>(L, p) : launch_stream<G, false>(L, p);
+#endif
+  if (L.streamed) return NP_ERR_UNSUPPORTED;
 #if NPK_BF16
   const bool two = G * p.query_len > 8;
 #if NPK_D % 64 == 0

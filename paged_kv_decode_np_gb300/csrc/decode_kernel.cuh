@@ -76,6 +76,10 @@ struct DecodeParams {
   const void* k_new;     // [R, Q, Hk, D] T
   const void* v_new;
   const int64_t* slot_mapping;  // [R, Q]
+  // Balanced streamed read (num_splits == 0; decode_stream.cuh): partials
+  // go to ws_o, each CTA's start point to st_pts ([P + 1][2]).
+  int32_t rows;
+  int64_t* st_pts;
 };
 
 // Fused append, run by every thread of the CTA before its pipeline starts.

@@ -19,6 +19,7 @@ struct DecodeLaunch {
   int head_group;              // HG
   int token_warps;             // TW
   int rows, splits, head_groups;
+  bool streamed;               // balanced streamed read: grid = `splits` CTAs
   size_t smem_budget;          // bytes of dynamic shared memory available
   cudaStream_t stream;
   // filled by the launcher

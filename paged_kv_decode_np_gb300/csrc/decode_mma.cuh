@@ -133,6 +133,294 @@ __device__ __forceinline__ float softmax_row(float (&sc)[4], float& m_run, float
   return alpha;
 }
 
+// Where one kv head's rows of a stage live in shared memory, and the address
+// of the 16-byte chunk of dims [16*ks + 8*ld_c, +8) of a token row.
+template <int D, bool TMAP>
+struct StageLayout {
+  int BT;               // tokens per TMA box
+  uint32_t half_bytes;  // one 64-dim slab of a chunk (TMAP)
+  uint32_t box_bytes;   // one box within a slab (TMAP)
+  uint32_t RS;          // token-row stride (per-token copies)
+  int hl;               // kv head within the CTA's group
+
+  __device__ __forceinline__ void row(int tok, uint32_t& off, uint32_t& swz) const {
+    if constexpr (TMAP) {
+      const int bx = tok / BT, tr = tok - bx * BT;
+      off = bx * box_bytes + (hl * BT + tr) * 128;
+      swz = (off >> 7) & 7;
+    } else {
+      off = tok * RS + hl * D * 2;
+      swz = 0;
+    }
+  }
+  __device__ __forceinline__ uint32_t chunk(uint32_t base, int ks, uint32_t off, uint32_t swz,
+                                            int ld_c) const {
+    if constexpr (TMAP) {
+      const uint32_t cidx = ((2 * ks) & 7) + ld_c;  // chunk within the 128-byte row
+      return base + (ks >> 2) * half_bytes + off + ((cidx ^ swz) << 4);
+    } else {
+      return base + off + ks * 32 + ld_c * 16;
+    }
+  }
+};
+
+// Producer: issue the copies of one chunk -- tokens [cb, cb + n) of row r,
+// kv heads [hgi*HG, (hgi+1)*HG) -- completing on `fb`.  The row's block ids
+// are fetched 32 at a time into `my_id` (window starting at logical block
+// `win`; win < 0 forces a fetch) and broadcast with shuffles.
+template <int D, bool TMAP>
+__device__ __forceinline__ void produce_chunk(const DecodeParams& p, const StageLayout<D, TMAP>& L,
+                                              int64_t r, int hgi, int HG, int64_t cb, int n,
+                                              int64_t nblk, uint32_t kdst, uint32_t vdst,
+                                              uint32_t fb, uint64_t pol, int64_t& win,
+                                              int32_t& my_id, int lane) {
+  constexpr unsigned FULL = 0xffffffffu;
+  const int64_t bs = p.block_size;
+  const uint32_t row_bytes = (uint32_t)HG * D * 2;
+  const int64_t jfirst = cb / bs;
+  const int64_t jlast = (cb + n - 1) / bs;
+  if (win < 0 || jfirst < win || jlast >= win + 32) {
+    win = jfirst;
+    const int64_t jj = win + lane;
+    my_id = jj < nblk ? p.block_tables[r * p.max_blocks_per_row + jj] : 0;
+  }
+  if constexpr (TMAP) {
+    // boxes of BT tokens; each lies inside one block (BT divides the block
+    // size and the chunk start) and is copied whole (rows past the history
+    // are masked by the consumers)
+    const int nbox = (n + L.BT - 1) / L.BT;
+    if (lane == 0) mbar_arrive_expect_tx(fb, 2u * (D / 64) * nbox * L.box_bytes);
+    const int items = nbox * (D / 64) * 2;  // (box, slab, K|V)
+    const int rounds = (items + 31) / 32;
+    for (int rd = 0; rd < rounds; ++rd) {
+      const int it = rd * 32 + lane;
+      const int bx = (it < items ? it : 0) / ((D / 64) * 2);
+      const int64_t t = cb + (int64_t)bx * L.BT;
+      const int64_t j = t / bs;
+      int64_t b = __shfl_sync(FULL, my_id, (int)(j - win));
+      if (it < items) {
+        const int slab = (it >> 1) % (D / 64);
+        const bool isv = (it & 1) != 0;
+        if (b < 0 || b >= p.num_blocks) {
+          set_flag(p.err, NP_FLAG_BLOCK_ID);
+          b = 0;
+        }
+        const int64_t slot = b * bs + (t - j * bs);
+        const uint32_t dst = (isv ? vdst : kdst) + slab * L.half_bytes + bx * L.box_bytes;
+        tma_load_3d(dst, isv ? &p.tm_v : &p.tm_k, slab * 64, (int32_t)slot, hgi * HG, fb, pol);
+      }
+    }
+  } else {
+    if (lane == 0) mbar_arrive_expect_tx(fb, 2u * (uint32_t)n * row_bytes);
+    const int64_t t = cb + (lane < n ? lane : 0);
+    const int64_t j = t / bs;
+    int64_t b = __shfl_sync(FULL, my_id, (int)(j - win));
+    if (b < 0 || b >= p.num_blocks) {
+      if (lane < n) set_flag(p.err, NP_FLAG_BLOCK_ID);
+      b = 0;
+    }
+    if (lane < n) {
+      const int64_t slot = b * bs + (t - j * bs);
+      const int64_t pool_row = (int64_t)p.kv_heads * D * 2;
+      const char* kp = static_cast<const char*>(p.k_pool) + (int64_t)hgi * row_bytes;
+      const char* vp = static_cast<const char*>(p.v_pool) + (int64_t)hgi * row_bytes;
+      bulk_g2s(kdst + lane * L.RS, kp + slot * pool_row, row_bytes, fb, pol);
+      bulk_g2s(vdst + lane * L.RS, vp + slot * pool_row, row_bytes, fb, pol);
+    }
+  }
+}
+
+// One consumer warp's read of one kv head: q fragments, the running softmax
+// of its two fragment rows (g4 and g4 + 8) and the O^T accumulators.
+template <int D, int G, bool TWO>
+struct MmaWarp {
+  static constexpr int KS = D / 16;
+  uint32_t qa0[KS], qa2[KS], qa1[TWO ? KS : 1], qa3[TWO ? KS : 1];
+  float mA, lA, mB, lB;
+  // O^T fragments: rows d = 16*mi + lane/4 (+8); columns = mma rows
+  // 2*(lane%4) (+1) in oA, 8 + 2*(lane%4) (+1) in oB
+  float oA[KS][4];
+  float oB[TWO ? KS : 1][4];
+  int64_t limA, limB;  // last position each row may see (-1: a padding row)
+
+  // q of row r, kv head kvh: mma row qi*G + h is query token qi, head
+  // kvh*G + h; rows >= G*Q are zero.  Resets the softmax state.
+  __device__ __forceinline__ void begin(const DecodeParams& p, int64_t r, int kvh, int64_t c,
+                                        int lane) {
+    const int Q = p.query_len, MR = G * Q;
+    const int g4 = lane >> 2, c4 = lane & 3;
+    auto qrow = [&](int row) -> const __nv_bfloat16* {
+      const int qi = row / G, h = row - (row / G) * G;
+      return static_cast<const __nv_bfloat16*>(p.q) +
+             ((r * Q + qi) * p.q_heads + kvh * G + h) * D;
+    };
+    const bool liveA = g4 < MR, liveB = g4 + 8 < MR;
+    limA = liveA ? c - Q + g4 / G : -1;
+    limB = liveB ? c - Q + (g4 + 8) / G : -1;
+    const __nv_bfloat16* qa = liveA ? qrow(g4) : nullptr;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qa0[ks] = liveA ? *reinterpret_cast<const uint32_t*>(qa + 16 * ks + 2 * c4) : 0u;
+      qa2[ks] = liveA ? *reinterpret_cast<const uint32_t*>(qa + 16 * ks + 8 + 2 * c4) : 0u;
+    }
+    if constexpr (TWO) {
+      const __nv_bfloat16* qb = liveB ? qrow(g4 + 8) : nullptr;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qa1[ks] = liveB ? *reinterpret_cast<const uint32_t*>(qb + 16 * ks + 2 * c4) : 0u;
+        qa3[ks] = liveB ? *reinterpret_cast<const uint32_t*>(qb + 16 * ks + 8 + 2 * c4) : 0u;
+      }
+    }
+    mA = mB = -INFINITY;
+    lA = lB = 0.f;
+#pragma unroll
+    for (int mi = 0; mi < KS; ++mi)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        oA[mi][e] = 0.f;
+        if constexpr (TWO) oB[mi][e] = 0.f;
+      }
+  }
+
+  // One tile: up to 16 tokens from tile-local token sb of a staged chunk
+  // (K rows at kst, V rows at vst) whose first token is position tch and
+  // whose first nvalid tokens are valid.
+  template <bool TMAP>
+  __device__ __forceinline__ void tile(const StageLayout<D, TMAP>& L, uint32_t kst, uint32_t vst,
+                                       int sb, int nvalid, int64_t tch, float qscale, int lane) {
+    constexpr unsigned FULL = 0xffffffffu;
+    const int c4 = lane & 3;
+    // ldmatrix lane addressing: matrix (lane/8) covers tokens 8*(lane/16) +
+    // (0..7) and the 8-dim column chunk (lane/8)%2 of a 16-dim step; the same
+    // pattern serves K (B of QK) and V (A of PV, transposed load).  Rows past
+    // the valid tokens read row sb instead (finite data; probability 0).
+    const int ld_tok = ((lane >> 4) << 3) + (lane & 7);
+    const int ld_c = (lane >> 3) & 1;
+    const int tok = (sb + ld_tok < nvalid) ? sb + ld_tok : sb;
+    uint32_t off, swz;
+    L.row(tok, off, swz);
+    // ---- S^T = q K^T for 16 tokens (two n-tiles of 8)
+    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(L.chunk(kst, ks, off, swz, ld_c), b0, b1, b2, b3);
+      if constexpr (TWO) {
+        mma_bf16(s0, qa0[ks], qa1[ks], qa2[ks], qa3[ks], b0, b1);
+        mma_bf16(s1, qa0[ks], qa1[ks], qa2[ks], qa3[ks], b2, b3);
+      } else {
+        mma_bf16(s0, qa0[ks], 0u, qa2[ks], 0u, b0, b1);
+        mma_bf16(s1, qa0[ks], 0u, qa2[ks], 0u, b2, b3);
+      }
+    }
+    // ---- masks: token (tile-local) 2*c4 + {0, 1, 8, 9} must be a valid
+    // token of the chunk and at or before the row's own position
+    const int lt = sb + 2 * c4;
+    const int64_t pos = tch + lt;
+    const bool v0 = lt < nvalid, v1 = lt + 1 < nvalid, v8 = lt + 8 < nvalid, v9 = lt + 9 < nvalid;
+    float sa[4] = {s0[0] * qscale, s0[1] * qscale, s1[0] * qscale, s1[1] * qscale};
+    if (!(v0 && pos <= limA)) sa[0] = -INFINITY;
+    if (!(v1 && pos + 1 <= limA)) sa[1] = -INFINITY;
+    if (!(v8 && pos + 8 <= limA)) sa[2] = -INFINITY;
+    if (!(v9 && pos + 9 <= limA)) sa[3] = -INFINITY;
+    const float alphaA = softmax_row(sa, mA, lA);
+    const uint32_t pa0 = pack_bf16(sa[0], sa[1]);
+    const uint32_t pa1 = pack_bf16(sa[2], sa[3]);
+    float alphaB = 1.f;
+    uint32_t pb0 = 0u, pb1 = 0u;
+    if constexpr (TWO) {
+      float sbv[4] = {s0[2] * qscale, s0[3] * qscale, s1[2] * qscale, s1[3] * qscale};
+      if (!(v0 && pos <= limB)) sbv[0] = -INFINITY;
+      if (!(v1 && pos + 1 <= limB)) sbv[1] = -INFINITY;
+      if (!(v8 && pos + 8 <= limB)) sbv[2] = -INFINITY;
+      if (!(v9 && pos + 9 <= limB)) sbv[3] = -INFINITY;
+      alphaB = softmax_row(sbv, mB, lB);
+      pb0 = pack_bf16(sbv[0], sbv[1]);
+      pb1 = pack_bf16(sbv[2], sbv[3]);
+    }
+    // ---- rescale O^T columns (mma rows 2*c4, 2*c4+1 and +8) when a max moved
+    if (__any_sync(FULL, alphaA != 1.f || alphaB != 1.f)) {
+      const float a_lo = __shfl_sync(FULL, alphaA, 8 * c4);
+      const float a_hi = __shfl_sync(FULL, alphaA, 8 * c4 + 4);
+#pragma unroll
+      for (int mi = 0; mi < KS; ++mi) {
+        oA[mi][0] *= a_lo;
+        oA[mi][1] *= a_hi;
+        oA[mi][2] *= a_lo;
+        oA[mi][3] *= a_hi;
+      }
+      if constexpr (TWO) {
+        const float b_lo = __shfl_sync(FULL, alphaB, 8 * c4);
+        const float b_hi = __shfl_sync(FULL, alphaB, 8 * c4 + 4);
+#pragma unroll
+        for (int mi = 0; mi < KS; ++mi) {
+          oB[mi][0] *= b_lo;
+          oB[mi][1] *= b_hi;
+          oB[mi][2] *= b_lo;
+          oB[mi][3] *= b_hi;
+        }
+      }
+    }
+    // ---- O^T += V^T P^T
+#pragma unroll
+    for (int mi = 0; mi < KS; ++mi) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(L.chunk(vst, mi, off, swz, ld_c), a0, a1, a2, a3);
+      mma_bf16(oA[mi], a0, a1, a2, a3, pa0, pa1);
+      if constexpr (TWO) mma_bf16(oB[mi], a0, a1, a2, a3, pb0, pb1);
+    }
+  }
+
+  // each row's sum over its 4 lanes
+  __device__ __forceinline__ void finish() {
+    constexpr unsigned FULL = 0xffffffffu;
+    lA += __shfl_xor_sync(FULL, lA, 1);
+    lA += __shfl_xor_sync(FULL, lA, 2);
+    lB += __shfl_xor_sync(FULL, lB, 1);
+    lB += __shfl_xor_sync(FULL, lB, 2);
+  }
+
+  // Unnormalised result rows into a [16 rows][D] fp32 array plus m and l
+  // ([16] each); rows >= MR are skipped.
+  __device__ __forceinline__ void store_rows(float* m_out, float* l_out, float* o_out, int MR,
+                                             int lane) const {
+    const int g4 = lane >> 2;
+    if ((lane & 3) == 0) {
+      if (g4 < MR) {
+        m_out[g4] = mA;
+        l_out[g4] = lA;
+      }
+      if (TWO && g4 + 8 < MR) {
+        m_out[g4 + 8] = mB;
+        l_out[g4 + 8] = lB;
+      }
+    }
+    const int c0 = 2 * (lane & 3);  // mma rows of this lane's O^T columns
+#pragma unroll
+    for (int mi = 0; mi < KS; ++mi) {
+      const int d = 16 * mi + g4;
+      if (c0 < MR) {
+        o_out[c0 * D + d] = oA[mi][0];
+        o_out[c0 * D + d + 8] = oA[mi][2];
+      }
+      if (c0 + 1 < MR) {
+        o_out[(c0 + 1) * D + d] = oA[mi][1];
+        o_out[(c0 + 1) * D + d + 8] = oA[mi][3];
+      }
+      if constexpr (TWO) {
+        if (c0 + 8 < MR) {
+          o_out[(c0 + 8) * D + d] = oB[mi][0];
+          o_out[(c0 + 8) * D + d + 8] = oB[mi][2];
+        }
+        if (c0 + 9 < MR) {
+          o_out[(c0 + 9) * D + d] = oB[mi][1];
+          o_out[(c0 + 9) * D + d + 8] = oB[mi][3];
+        }
+      }
+    }
+  }
+};
+
 template <int D, int G, bool TMAP, bool TWO>
 __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
     paged_decode_mma_kernel(const __grid_constant__ DecodeParams p) {
@@ -199,35 +487,28 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
   __syncthreads();
 
   const int64_t nch = (t1 - t0 + C::CT - 1) / C::CT;
-  const uint32_t row_bytes = (uint32_t)HG * D * 2;  // one token, HG kv heads
   // TMAP layout of a stage: [K | V] x [D/64 slabs of 64 dims] x [CT/B boxes]
   //                         x [HG heads] x [B token rows of 128 bytes]
-  const int BT = TMAP ? p.box_tokens : 1;
-  if (TMAP && (BT < 1 || BT > C::CT || C::CT % BT != 0)) {
+  StageLayout<D, TMAP> L;
+  L.BT = TMAP ? p.box_tokens : 1;
+  L.half_bytes = (uint32_t)C::CT * HG * 128;
+  L.box_bytes = (uint32_t)L.BT * HG * 128;
+  L.RS = (uint32_t)S::row_stride(HG);
+  L.hl = warp % HG;
+  if (TMAP && (L.BT < 1 || L.BT > C::CT || C::CT % L.BT != 0)) {
     // a box must fit its stage; the host never launches otherwise
     if (threadIdx.x == 0) set_flag(p.err, NP_FLAG_CONFIG);
     return;
   }
-  const uint32_t half_bytes = (uint32_t)C::CT * HG * 128;  // one 64-dim slab of a chunk
-  const uint32_t box_bytes = (uint32_t)BT * HG * 128;      // one box within a slab
-  const uint32_t RS = (uint32_t)S::row_stride(HG);         // padded layout
 
-  // running softmax state of this lane's two fragment rows (g4 and g4 + 8)
-  float mA = -INFINITY, lA = 0.f, mB = -INFINITY, lB = 0.f;
-  // O^T fragments: rows d = 16*mi + lane/4 (+8); columns = mma rows
-  // 2*(lane%4) (+1) in oA, 8 + 2*(lane%4) (+1) in oB
-  float oA[C::KS][4];
-  float oB[TWO ? C::KS : 1][4];
+  MmaWarp<D, G, TWO> W;
+  W.mA = W.mB = -INFINITY;
+  W.lA = W.lB = 0.f;
 
   if (warp == NC) {
     // ======================= producer warp
     const uint64_t pol = policy_evict_first();
-    const int64_t bs = p.block_size;
-    const int64_t tab0 = (int64_t)r * p.max_blocks_per_row;
-    const int64_t nblk = (c + bs - 1) / bs;
-    const int64_t pool_row = (int64_t)p.kv_heads * D * 2;
-    const char* kpool = static_cast<const char*>(p.k_pool) + (int64_t)hgi * row_bytes;
-    const char* vpool = static_cast<const char*>(p.v_pool) + (int64_t)hgi * row_bytes;
+    const int64_t nblk = (c + p.block_size - 1) / p.block_size;
     int64_t win = -1;
     int32_t my_id = 0;
     int64_t issued = 0;
@@ -239,58 +520,10 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
       }
       const int64_t cb = t0 + ch * C::CT;
       const int n = (int)min((int64_t)C::CT, t1 - cb);
-      const uint32_t fb = smem_u32(&full_bar[st]);
       const uint32_t kdst = smem_u32(smem + st * stage_bytes);
-      const uint32_t vdst = kdst + (uint32_t)(stage_bytes / 2);
-      const int64_t jfirst = cb / bs;
-      const int64_t jlast = (cb + n - 1) / bs;
-      if (win < 0 || jlast >= win + 32) {
-        win = jfirst;
-        const int64_t jj = win + lane;
-        my_id = jj < nblk ? p.block_tables[tab0 + jj] : 0;
-      }
-      if constexpr (TMAP) {
-        // boxes of BT tokens; each lies inside one block (BT divides the block
-        // size and the chunk start) and is copied whole (rows past the
-        // history are masked by the consumers)
-        const int nbox = (n + BT - 1) / BT;
-        if (lane == 0) mbar_arrive_expect_tx(fb, 2u * (D / 64) * nbox * box_bytes);
-        const int items = nbox * (D / 64) * 2;  // (box, slab, K|V)
-        const int rounds = (items + 31) / 32;
-        for (int rd = 0; rd < rounds; ++rd) {
-          const int it = rd * 32 + lane;
-          const int bx = (it < items ? it : 0) / ((D / 64) * 2);
-          const int64_t t = cb + (int64_t)bx * BT;
-          const int64_t j = t / bs;
-          int64_t b = __shfl_sync(FULL, my_id, (int)(j - win));
-          if (it < items) {
-            const int slab = (it >> 1) % (D / 64);
-            const bool isv = (it & 1) != 0;
-            if (b < 0 || b >= p.num_blocks) {
-              set_flag(p.err, NP_FLAG_BLOCK_ID);
-              b = 0;
-            }
-            const int64_t slot = b * bs + (t - j * bs);
-            const uint32_t dst = (isv ? vdst : kdst) + slab * half_bytes + bx * box_bytes;
-            tma_load_3d(dst, isv ? &p.tm_v : &p.tm_k, slab * 64, (int32_t)slot, hgi * HG, fb,
-                        pol);
-          }
-        }
-      } else {
-        if (lane == 0) mbar_arrive_expect_tx(fb, 2u * (uint32_t)n * row_bytes);
-        const int64_t t = cb + (lane < n ? lane : 0);
-        const int64_t j = t / bs;
-        int64_t b = __shfl_sync(FULL, my_id, (int)(j - win));
-        if (b < 0 || b >= p.num_blocks) {
-          if (lane < n) set_flag(p.err, NP_FLAG_BLOCK_ID);
-          b = 0;
-        }
-        if (lane < n) {
-          const int64_t slot = b * bs + (t - j * bs);
-          bulk_g2s(kdst + lane * RS, kpool + slot * pool_row, row_bytes, fb, pol);
-          bulk_g2s(vdst + lane * RS, vpool + slot * pool_row, row_bytes, fb, pol);
-        }
-      }
+      produce_chunk<D, TMAP>(p, L, r, hgi, HG, cb, n, nblk, kdst,
+                             kdst + (uint32_t)(stage_bytes / 2), smem_u32(&full_bar[st]), pol,
+                             win, my_id, lane);
       issued = ch + 1;
     }
     if (*abort) {  // never leave copies in flight (bounded)
@@ -299,53 +532,8 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
     }
   } else {
     // ======================= consumer warp: kv head hl, chunks tw, tw+TW, ...
-    const int hl = warp % HG;
     const int tw = warp / HG;
-    const int kvh = hgi * HG + hl;
-    const int g4 = lane >> 2;  // fragment row group: mma rows g4 and g4 + 8
-    const int c4 = lane & 3;   // fragment column pair
-
-    // q as mma A fragments; row = qi*G + h, rows >= MR zero.  The last
-    // position row `row` may see: c - Q + qi.
-    uint32_t qa0[C::KS], qa2[C::KS], qa1[TWO ? C::KS : 1], qa3[TWO ? C::KS : 1];
-    auto qrow = [&](int row) -> const __nv_bfloat16* {
-      const int qi = row / G, h = row - (row / G) * G;
-      return static_cast<const __nv_bfloat16*>(p.q) +
-             (((int64_t)r * Q + qi) * p.q_heads + kvh * G + h) * D;
-    };
-    const bool liveA = g4 < MR, liveB = g4 + 8 < MR;
-    const int64_t limA = liveA ? c - Q + g4 / G : -1;
-    const int64_t limB = liveB ? c - Q + (g4 + 8) / G : -1;
-    {
-      const __nv_bfloat16* qa = liveA ? qrow(g4) : nullptr;
-#pragma unroll
-      for (int ks = 0; ks < C::KS; ++ks) {
-        qa0[ks] = liveA ? *reinterpret_cast<const uint32_t*>(qa + 16 * ks + 2 * c4) : 0u;
-        qa2[ks] = liveA ? *reinterpret_cast<const uint32_t*>(qa + 16 * ks + 8 + 2 * c4) : 0u;
-      }
-      if constexpr (TWO) {
-        const __nv_bfloat16* qb = liveB ? qrow(g4 + 8) : nullptr;
-#pragma unroll
-        for (int ks = 0; ks < C::KS; ++ks) {
-          qa1[ks] = liveB ? *reinterpret_cast<const uint32_t*>(qb + 16 * ks + 2 * c4) : 0u;
-          qa3[ks] = liveB ? *reinterpret_cast<const uint32_t*>(qb + 16 * ks + 8 + 2 * c4) : 0u;
-        }
-      }
-    }
-#pragma unroll
-    for (int mi = 0; mi < C::KS; ++mi)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        oA[mi][e] = 0.f;
-        if constexpr (TWO) oB[mi][e] = 0.f;
-      }
-
-    // ldmatrix lane addressing: matrix (lane/8) covers tokens 8*(lane/16) +
-    // (0..7) and the 8-dim column chunk (lane/8)%2 of a 16-dim step; the same
-    // pattern serves K (B of QK) and V (A of PV, transposed load)
-    const int ld_tok = ((lane >> 4) << 3) + (lane & 7);
-    const int ld_c = (lane >> 3) & 1;
-
+    W.begin(p, r, hgi * HG + L.hl, c, lane);
     for (int64_t ch = tw; ch < nch; ch += TW) {
       const int st = (int)(ch % stages);
       bool ok = mbar_wait(smem_u32(&full_bar[st]), (uint32_t)((ch / stages) & 1), abort);
@@ -356,111 +544,13 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
       const int64_t tch = t0 + ch * C::CT;  // position of the chunk's first token
       const int nvalid = (int)min((int64_t)C::CT, t1 - tch);
       const uint32_t kst = smem_u32(smem + st * stage_bytes);
-      const uint32_t vst = kst + (uint32_t)(stage_bytes / 2);
-
-      for (int sb = 0; sb < nvalid; sb += C::ST) {
-        // rows past the valid tokens read row sb instead (finite data; their
-        // probabilities are exactly 0)
-        const int tok = (sb + ld_tok < nvalid) ? sb + ld_tok : sb;
-        // this lane's row within a slab, and its swizzle
-        uint32_t row_off, swz = 0;
-        if constexpr (TMAP) {
-          const int bx = tok / BT, tr = tok - bx * BT;
-          row_off = bx * box_bytes + (hl * BT + tr) * 128;
-          swz = (row_off >> 7) & 7;
-        } else {
-          row_off = tok * RS + hl * D * 2;
-        }
-        // address of this lane's 16-byte chunk of dims [16*ks + 8*ld_c, +8)
-        auto chunk_addr = [&](uint32_t base, int ks) -> uint32_t {
-          if constexpr (TMAP) {
-            const uint32_t cidx = ((2 * ks) & 7) + ld_c;  // chunk within the 128-byte row
-            return base + (ks >> 2) * half_bytes + row_off + ((cidx ^ swz) << 4);
-          } else {
-            return base + row_off + ks * 32 + ld_c * 16;
-          }
-        };
-        // ---- S^T = q K^T for 16 tokens (two n-tiles of 8)
-        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < C::KS; ++ks) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(chunk_addr(kst, ks), b0, b1, b2, b3);
-          if constexpr (TWO) {
-            mma_bf16(s0, qa0[ks], qa1[ks], qa2[ks], qa3[ks], b0, b1);
-            mma_bf16(s1, qa0[ks], qa1[ks], qa2[ks], qa3[ks], b2, b3);
-          } else {
-            mma_bf16(s0, qa0[ks], 0u, qa2[ks], 0u, b0, b1);
-            mma_bf16(s1, qa0[ks], 0u, qa2[ks], 0u, b2, b3);
-          }
-        }
-        // ---- masks: token (tile-local) 2*c4 + {0, 1, 8, 9} must be a valid
-        // token of the chunk and at or before the row's own position
-        const int lt = sb + 2 * c4;
-        const int64_t pos = tch + lt;
-        const bool v0 = lt < nvalid, v1 = lt + 1 < nvalid, v8 = lt + 8 < nvalid,
-                   v9 = lt + 9 < nvalid;
-        float sa[4] = {s0[0] * p.qscale, s0[1] * p.qscale, s1[0] * p.qscale, s1[1] * p.qscale};
-        if (!(v0 && pos <= limA)) sa[0] = -INFINITY;
-        if (!(v1 && pos + 1 <= limA)) sa[1] = -INFINITY;
-        if (!(v8 && pos + 8 <= limA)) sa[2] = -INFINITY;
-        if (!(v9 && pos + 9 <= limA)) sa[3] = -INFINITY;
-        const float alphaA = softmax_row(sa, mA, lA);
-        const uint32_t pa0 = pack_bf16(sa[0], sa[1]);
-        const uint32_t pa1 = pack_bf16(sa[2], sa[3]);
-        float alphaB = 1.f;
-        uint32_t pb0 = 0u, pb1 = 0u;
-        if constexpr (TWO) {
-          float sbv[4] = {s0[2] * p.qscale, s0[3] * p.qscale, s1[2] * p.qscale,
-                          s1[3] * p.qscale};
-          if (!(v0 && pos <= limB)) sbv[0] = -INFINITY;
-          if (!(v1 && pos + 1 <= limB)) sbv[1] = -INFINITY;
-          if (!(v8 && pos + 8 <= limB)) sbv[2] = -INFINITY;
-          if (!(v9 && pos + 9 <= limB)) sbv[3] = -INFINITY;
-          alphaB = softmax_row(sbv, mB, lB);
-          pb0 = pack_bf16(sbv[0], sbv[1]);
-          pb1 = pack_bf16(sbv[2], sbv[3]);
-        }
-        // ---- rescale O^T columns (mma rows 2*c4, 2*c4+1 and +8) when a max moved
-        if (__any_sync(FULL, alphaA != 1.f || alphaB != 1.f)) {
-          const float a_lo = __shfl_sync(FULL, alphaA, 8 * c4);
-          const float a_hi = __shfl_sync(FULL, alphaA, 8 * c4 + 4);
-#pragma unroll
-          for (int mi = 0; mi < C::KS; ++mi) {
-            oA[mi][0] *= a_lo;
-            oA[mi][1] *= a_hi;
-            oA[mi][2] *= a_lo;
-            oA[mi][3] *= a_hi;
-          }
-          if constexpr (TWO) {
-            const float b_lo = __shfl_sync(FULL, alphaB, 8 * c4);
-            const float b_hi = __shfl_sync(FULL, alphaB, 8 * c4 + 4);
-#pragma unroll
-            for (int mi = 0; mi < C::KS; ++mi) {
-              oB[mi][0] *= b_lo;
-              oB[mi][1] *= b_hi;
-              oB[mi][2] *= b_lo;
-              oB[mi][3] *= b_hi;
-            }
-          }
-        }
-        // ---- O^T += V^T P^T
-#pragma unroll
-        for (int mi = 0; mi < C::KS; ++mi) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(chunk_addr(vst, mi), a0, a1, a2, a3);
-          mma_bf16(oA[mi], a0, a1, a2, a3, pa0, pa1);
-          if constexpr (TWO) mma_bf16(oB[mi], a0, a1, a2, a3, pb0, pb1);
-        }
-      }
+      for (int sb = 0; sb < nvalid; sb += C::ST)
+        W.template tile<TMAP>(L, kst, kst + (uint32_t)(stage_bytes / 2), sb, nvalid, tch,
+                              p.qscale, lane);
       __syncwarp();  // every lane's reads of this stage are done
       if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
     }
-    // each row's sum over its 4 lanes
-    lA += __shfl_xor_sync(FULL, lA, 1);
-    lA += __shfl_xor_sync(FULL, lA, 2);
-    lB += __shfl_xor_sync(FULL, lB, 1);
-    lB += __shfl_xor_sync(FULL, lB, 2);
+    W.finish();
   }
 
   // ======================= epilogue: stage (m, l, O) per warp, merge, store
@@ -470,40 +560,7 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
   const int stride_w = RW * (D + 2);
   if (warp < NC) {
     float* mg = merge + warp * stride_w;
-    const int g4 = lane >> 2;
-    if ((lane & 3) == 0) {
-      if (g4 < MR) {
-        mg[g4] = mA;
-        mg[RW + g4] = lA;
-      }
-      if (TWO && g4 + 8 < MR) {
-        mg[g4 + 8] = mB;
-        mg[RW + g4 + 8] = lB;
-      }
-    }
-    const int c0 = 2 * (lane & 3);  // mma rows of this lane's O^T columns
-#pragma unroll
-    for (int mi = 0; mi < C::KS; ++mi) {
-      const int d = 16 * mi + g4;
-      if (c0 < MR) {
-        mg[2 * RW + c0 * D + d] = oA[mi][0];
-        mg[2 * RW + c0 * D + d + 8] = oA[mi][2];
-      }
-      if (c0 + 1 < MR) {
-        mg[2 * RW + (c0 + 1) * D + d] = oA[mi][1];
-        mg[2 * RW + (c0 + 1) * D + d + 8] = oA[mi][3];
-      }
-      if constexpr (TWO) {
-        if (c0 + 8 < MR) {
-          mg[2 * RW + (c0 + 8) * D + d] = oB[mi][0];
-          mg[2 * RW + (c0 + 8) * D + d + 8] = oB[mi][2];
-        }
-        if (c0 + 9 < MR) {
-          mg[2 * RW + (c0 + 9) * D + d] = oB[mi][1];
-          mg[2 * RW + (c0 + 9) * D + d + 8] = oB[mi][3];
-        }
-      }
-    }
+    W.store_rows(mg, mg + RW, mg + 2 * RW, MR, lane);
   }
   __syncthreads();  // (B)
   if (warp >= NC || warp / HG != 0) return;

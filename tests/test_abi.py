@@ -73,7 +73,10 @@ def test_decode_validation(lib):
     assert _decode(lib, hk=1, hq=3, **ok_ptrs) == 2    # group 3 not compiled
     assert _decode(lib, dtype=7, **ok_ptrs) == 2       # dtype
     assert _decode(lib, scale=float("nan"), **ok_ptrs) == 1
-    assert _decode(lib, splits=0, **ok_ptrs) == 1
+    assert _decode(lib, splits=-1, **ok_ptrs) == 1
+    assert _decode(lib, splits=0, **ok_ptrs) == 2            # balanced read: bf16 only
+    assert _decode(lib, splits=0, dtype=1, hk=4, hq=8, **ok_ptrs) == 2  # kv heads % 8
+    assert _decode(lib, splits=0, dtype=1, hk=8, hq=16, nb=16, **ok_ptrs) == 3  # no workspace
     assert _decode(lib, bs=0, **ok_ptrs) == 1
     assert _decode(lib, nb=0, **ok_ptrs) == 1
     assert _decode(lib, rows=-1, **ok_ptrs) == 1
@@ -114,6 +117,7 @@ def test_reduce_validation(lib):
 def test_workspace_bytes(lib):
     f = lib.np_paged_decode_workspace_bytes
     assert f(4, 8, 128, 1) == 0
+    assert f(4, 8, 128, 0) > 0  # the balanced read's partials and counters
     n_o = 4 * 8 * 3 * 128 * 4
     n_l = 4 * 8 * 3 * 4
     assert f(4, 8, 128, 3) == (n_o + 255) // 256 * 256 + (n_l + 255) // 256 * 256
@@ -136,6 +140,9 @@ def test_plan_is_static_and_sane(lib):
         s = npg.np_paged_decode_plan(w.rows, w.q_heads, w.kv_heads, w.head_dim, w.block_size,
                                      w.max_blocks_per_row, w.torch_dtype, num_sms=152)
         cap = w.max_blocks_per_row * w.block_size
+        if s == 0:  # the balanced read: bf16, head_dim % 64, kv heads % 8
+            assert w.dtype == "bf16" and w.head_dim % 64 == 0 and w.kv_heads % 8 == 0
+            continue
         sl = npg.np_paged_decode_split_len(w.block_size, w.max_blocks_per_row, s)
         assert s >= 1 and sl * s >= cap
         if s > 1:  # each split reads at least 64 tokens' worth of every head group

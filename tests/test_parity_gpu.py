@@ -364,6 +364,70 @@ def test_head_dim_256_with_eight_kv_heads(nplib):
     _full_parity(nplib, w, num_splits=4)
 
 
+# ------------------------------------------- the balanced streamed read ----
+@pytest.mark.parametrize("kv_heads,group,head_dim,block_size,query_len", [
+    (8, 4, 128, 16, 1), (8, 8, 128, 32, 1), (8, 5, 128, 8, 1), (16, 1, 64, 16, 1),
+    (8, 2, 256, 32, 1), (8, 4, 128, 16, 3), (8, 8, 64, 64, 2), (16, 4, 128, 4, 1)])
+def test_balanced_read(nplib, kv_heads, group, head_dim, block_size, query_len):
+    """num_splits = 0: one CTA per SM, equal token shares; rows cut between
+    CTAs are merged by the second kernel.  Small totals spread over 152
+    CTAs cut most rows, so the merge path is exercised heavily."""
+    ctx = [0, 1, 5, 16, 17, 300, 2049, 64, 0, 4000, 31, 7]
+    ctx = [max(c, query_len if c else 0) for c in ctx]
+    w = _custom(ctx, kv_heads * group, kv_heads, head_dim, block_size, "bf16",
+                seed=150 + kv_heads + group + head_dim + block_size + query_len,
+                query_len=query_len)
+    _full_parity(nplib, w, num_splits=0)
+    _full_parity(nplib, w, num_splits=0, fused=False)
+
+
+def test_balanced_read_two_calls_one_workspace(nplib):
+    """The workspace needs no zeroing: a NaN-filled one, reused by a second
+    call with other lengths, must not leak stale partials."""
+    ws = None
+    for seed, ctx in ((160, [3000, 17, 900, 64, 1]), (161, [5, 5000, 2500, 0, 130])):
+        w = _custom(ctx, 32, 8, 128, 16, "bf16", seed=seed)
+        inp = wl.make_inputs(w)
+        host = wl.full_host(inp)
+        if ws is None:
+            ws = nplib.workspace(w.rows, w.q_heads, w.head_dim, 0)
+            ws.view(torch.float32).fill_(float("nan"))
+        dev = [t.to(DEV) for t in (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new)]
+        bt, cl, sm = (t.to(DEV) for t in (inp.block_tables, inp.context_lens, inp.slot_mapping))
+        out = torch.full_like(dev[0], float("nan"))
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        nplib.np_paged_append_decode(out, dev[0], dev[3], dev[4], sm, dev[1], dev[2], bt, cl,
+                                     w.softmax_scale, 0, ws, err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        ref, _ = oracle_step(host, w.softmax_scale)
+        assert_parity(out, ref, "bf16", f"balanced call seed={seed}")
+
+
+def test_balanced_read_graph_replay(nplib):
+    w = _custom([700, 4096, 33, 1200, 2], 40, 8, 128, 32, "bf16", seed=170)
+    inp = wl.make_inputs(w)
+    host = wl.full_host(inp)
+    q, kp, vp, kn, vn = (t.to(DEV) for t in (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new))
+    bt, cl, sm = (t.to(DEV) for t in (inp.block_tables, inp.context_lens, inp.slot_mapping))
+    ws = nplib.workspace(w.rows, w.q_heads, w.head_dim, 0)
+    out = torch.empty_like(q)
+    nplib.np_paged_append_decode(out, q, kn, vn, sm, kp, vp, bt, cl, w.softmax_scale, 0, ws)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        nplib.np_paged_append_decode(out, q, kn, vn, sm, kp, vp, bt, cl, w.softmax_scale, 0, ws)
+    for _ in range(3):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+    ref, _ = oracle_step(host, w.softmax_scale)
+    assert_parity(out, ref, "bf16", "balanced graph replay")
+
+
 # ---------------------------------------------------------- robustness ----
 def test_bad_block_id_is_flagged_not_faulted(nplib):
     w = _custom([40, 40], 8, 2, 128, 16, "f32", seed=50)
