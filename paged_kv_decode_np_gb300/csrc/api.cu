@@ -334,13 +334,13 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
     return NP_ERR_INVALID_ARG;
   float* ws_o = nullptr;
   float* ws_lse = nullptr;
-  int64_t* st_pts = nullptr;
+  int32_t* st_desc = nullptr;
   if (streamed) {
     const size_t need = npk::StreamWs::bytes(head_dim);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return NP_ERR_WORKSPACE;
     ws_o = static_cast<float*>(workspace);
-    st_pts = reinterpret_cast<int64_t*>(static_cast<char*>(workspace) +
-                                        npk::StreamWs::parts_bytes(head_dim));
+    st_desc = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) +
+                                         npk::StreamWs::parts_bytes(head_dim));
   } else if (num_splits > 1) {
     const int32_t units_rows = rows * query_len;  // rows of the partial layout
     const size_t need =
@@ -383,7 +383,7 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
   p.slot_mapping = slot_mapping;
   p.query_len = query_len;
   p.rows = rows;
-  p.st_pts = st_pts;
+  p.st_desc = st_desc;
   // bf16 pools with head_dim a multiple of 64 stage K/V through tiled TMA
   // boxes of box_tokens tokens: the largest power of two dividing the block
   // size, at most the stage's token count, with box_tokens * head_group a

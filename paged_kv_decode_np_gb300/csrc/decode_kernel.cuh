@@ -77,9 +77,9 @@ struct DecodeParams {
   const void* v_new;
   const int64_t* slot_mapping;  // [R, Q]
   // Balanced streamed read (num_splits == 0; decode_stream.cuh): partials
-  // go to ws_o, each CTA's start point to st_pts ([P + 1][2]).
+  // go to ws_o, each CTA's merge descriptor to st_desc ([P][4]).
   int32_t rows;
-  int64_t* st_pts;
+  int32_t* st_desc;
 };
 
 // Fused append, run by every thread of the CTA before its pipeline starts.

@@ -41,7 +41,8 @@ constexpr int kStreamMaxCtas = 256;    // grid cap (the workspace is sized for i
 // Workspace of the streamed read (host and device agree on this):
 //   parts  [kStreamMaxCtas][2 slots][8 kv heads] entries of
 //          m[16] l[16] o[16][D] fp32 (16 = mma rows)
-//   pts    [kStreamMaxCtas + 1] longlong2: CTA b's start point (v, t)
+//   desc   [kStreamMaxCtas] int4: CTA b's merge descriptor {v, c, bl, slot}
+//          for the cut row it owns (v = -1: none)
 // Nothing in it needs to start zeroed.
 struct StreamWs {
   __host__ __device__ static constexpr size_t entry_floats(int d) {
@@ -51,13 +52,10 @@ struct StreamWs {
     return (size_t)kStreamMaxCtas * 2 * 8 * entry_floats(d) * sizeof(float);
   }
   __host__ __device__ static constexpr size_t bytes(int d) {
-    return parts_bytes(d) + (size_t)(kStreamMaxCtas + 1) * 2 * sizeof(int64_t);
+    return parts_bytes(d) + (size_t)kStreamMaxCtas * 4 * sizeof(int32_t);
   }
 };
 
-__device__ __forceinline__ bool point_before(int64_t v1, int64_t t1, int64_t v2, int64_t t2) {
-  return v1 < v2 || (v1 == v2 && t1 < t2);
-}
 
 template <int D, int G>
 struct StreamSmem {
@@ -99,7 +97,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   uint64_t* empty_bar = full_bar + stages;
   volatile int* abort = reinterpret_cast<volatile int*>(empty_bar + stages);
   int64_t* pre = reinterpret_cast<int64_t*>(smem + ring + 16ull * stages + 16);
-  __shared__ int64_t tsum[kMaxThreads];
+  __shared__ int64_t wsum[32];
   __shared__ int64_t range[4];  // vb, tb, ve, te
 
   auto row_len = [&](int v) -> int64_t {
@@ -107,33 +105,43 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     return c < 0 ? 0 : (c > cap ? cap : c);
   };
 
-  // ---- prefix of the virtual rows' lengths (two-level block scan)
+  // ---- prefix of the virtual rows' lengths: each thread sums a run of
+  // rows, warps scan the run sums with shuffles, warp 0 scans the warp sums
   {
     const int nt = blockDim.x;
     const int per = (V + nt - 1) / nt;
     const int v0 = threadIdx.x * per, v1 = min(V, v0 + per);
     int64_t sum = 0;
-    for (int v = v0; v < v1; ++v) sum += row_len(v);
-    tsum[threadIdx.x] = sum;
+    for (int v = v0; v < v1; ++v) {
+      sum += row_len(v);
+      if (b == 0 && v < R && (p.context_lens[v] < 0 || p.context_lens[v] > cap))
+        set_flag(p.err, NP_FLAG_CONTEXT);  // clamped above
+    }
+    int64_t x = sum;  // inclusive scan within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(FULL, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int64_t run = 0;
-      for (int t = 0; t < nt; ++t) {
-        const int64_t x = tsum[t];
-        tsum[t] = run;
-        run += x;
+    if (warp == 0) {
+      const int nw = nt / 32;
+      int64_t t = lane < nw ? wsum[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(FULL, t, o);
+        if (lane >= o) t += y;
       }
-      pre[V] = run;
+      if (lane < nw) wsum[lane] = t;
+      if (lane == nw - 1) pre[V] = t;
     }
     __syncthreads();
-    int64_t run = tsum[threadIdx.x];
+    int64_t run = x - sum + (warp > 0 ? wsum[warp - 1] : 0);
     for (int v = v0; v < v1; ++v) {
       pre[v] = run;
       run += row_len(v);
     }
-    if (threadIdx.x == 0 && b == 0)  // out-of-range contexts were clamped
-      for (int r = 0; r < R; ++r)
-        if (p.context_lens[r] < 0 || p.context_lens[r] > cap) set_flag(p.err, NP_FLAG_CONTEXT);
   }
   __syncthreads();
 
@@ -157,15 +165,25 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     point(b, pv, pt);
     range[0] = pv;
     range[1] = pt;
-    p.st_pts[2 * b] = pv;  // for the merge kernel
-    p.st_pts[2 * b + 1] = pt;
+    const int vb0 = pv;
+    const int64_t tb0 = pt;
     point(b + 1, pv, pt);
     range[2] = pv;
     range[3] = pt;
-    if (b == P - 1) {
-      p.st_pts[2 * P] = pv;
-      p.st_pts[2 * P + 1] = pt;
+    // Merge descriptor.  CTA b owns the row its range ends inside, v, if v
+    // began here ((vb, tb) <= (v, 0)).  The covering CTAs are b .. bl, bl
+    // the last whose stream position floor(bb*total/P) lies before the
+    // row's end pre[v+1]; CTAs after b hold v as their first row (slot 0),
+    // b holds it in slot 0 if it is b's first row, else in slot 1.
+    int4 d = make_int4(-1, 0, 0, 0);
+    if (pt > 0 && pv < V && (vb0 < pv || tb0 == 0)) {
+      const int64_t x = pre[pv + 1];
+      d.x = pv;
+      d.y = (int)(x - pre[pv]);
+      d.z = (int)min((int64_t)P - 1, (x * P - 1) / total);
+      d.w = vb0 == pv ? 0 : 1;
     }
+    reinterpret_cast<int4*>(p.st_desc)[b] = d;
   }
   __syncthreads();
   const int vb = (int)range[0], ve = (int)range[2];
@@ -218,34 +236,112 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
   if (warp == HG) {
     // ======================= producer warp: every chunk of every segment
+    // Block-table entries come in windows of 32 blocks of one row, aligned
+    // to multiples of 32 blocks; a chunk never straddles two (chunk starts
+    // and 32-block spans are both multiples of CT tokens).  Lane j holds
+    // entry j of the current window (cur) and of the window after it (nxt:
+    // the row's next window, or the next segment's first), loaded one window
+    // ahead so that issuing never waits on the table.  Positions fit int32
+    // (the host admits tables of at most INT32_MAX tokens).
     const uint64_t pol = policy_evict_first();
-    int64_t gch = 0, issued = 0;
+    const int32_t bs = p.block_size;
+    auto next_seg = [&](int v, int64_t& ts, int64_t& tend) -> int {  // first non-empty >= v
+      for (; v <= ve && v < V; ++v) {
+        seg_bounds(v, ts, tend);
+        if (ts < tend) return v;
+      }
+      ts = tend = 0;
+      return -1;
+    };
+    auto load_window = [&](int v, int32_t w) -> int32_t {
+      if (v < 0) return 0;
+      const int32_t j = w + lane;
+      return j < (int32_t)((row_len(v) + bs - 1) / bs)
+                 ? p.block_tables[(int64_t)(v % R) * p.max_blocks_per_row + j]
+                 : 0;
+    };
+    int64_t ts64, te64;
+    int v = next_seg(vb, ts64, te64);
+    int32_t ts = (int32_t)ts64, tend = (int32_t)te64;
+    int32_t ww = v >= 0 ? ts / bs / 32 * 32 : 0;  // current window: row v, first block ww
+    int32_t cur = load_window(v, ww), nxt = 0;
+    int nv = -1;  // the window after it: row nv, first block nw
+    int32_t nw = 0;
+    int64_t gch = 0;
+    int st = 0;
+    uint32_t ph = 1;  // parity of stage st's empty barrier: (gch / stages - 1) & 1
     bool stop = false;
-    for (int v = vb; v <= ve && v < V && !stop; ++v) {
-      int64_t ts, tend;
-      seg_bounds(v, ts, tend);
+    while (v >= 0 && !stop) {
       const int r = v % R, hgi = v / R;
-      const int64_t nblk = (row_len(v) + p.block_size - 1) / p.block_size;
-      int64_t win = -1;
-      int32_t my_id = 0;
-      for (int64_t cb = ts; cb < tend; cb += C::CT, ++gch) {
-        const int st = (int)(gch % stages);
+      const int32_t lastw = (tend - 1) / bs / 32 * 32;
+      int64_t nts, nte;
+      const int vn = next_seg(v + 1, nts, nte);
+      auto set_next = [&]() {  // the window after (v, ww), loaded now
+        if (ww < lastw) {
+          nv = v;
+          nw = ww + 32;
+        } else {
+          nv = vn;
+          nw = vn >= 0 ? (int32_t)nts / bs / 32 * 32 : 0;
+        }
+        nxt = load_window(nv, nw);
+      };
+      set_next();
+      for (int32_t cb = ts; cb < tend; cb += C::CT, ++gch) {
         if (gch >= stages) {
-          bool ok =
-              mbar_wait(smem_u32(&empty_bar[st]), (uint32_t)((gch / stages - 1) & 1), abort);
+          bool ok = mbar_wait(smem_u32(&empty_bar[st]), ph, abort);
           if (!__all_sync(FULL, ok)) {
             stop = true;
             break;
           }
         }
-        const int n = (int)min((int64_t)C::CT, tend - cb);
+        const int32_t w = cb / bs / 32 * 32;
+        if (w != ww) {  // into the row's next window
+          ww = w;
+          cur = (nv == v && nw == w) ? nxt : load_window(v, w);
+          set_next();
+        }
+        const int n = min(C::CT, tend - cb);
         const uint32_t kdst = smem_u32(smem + st * stage_bytes);
-        produce_chunk<D, true>(p, L, r, hgi, HG, cb, n, nblk, kdst,
-                               kdst + (uint32_t)(stage_bytes / 2), smem_u32(&full_bar[st]), pol,
-                               win, my_id, lane);
-        issued = gch + 1;
+        const uint32_t fb = smem_u32(&full_bar[st]);
+        const int nbox = (n + L.BT - 1) / L.BT;
+        if (lane == 0) mbar_arrive_expect_tx(fb, 2u * (D / 64) * nbox * L.box_bytes);
+        const int items = nbox * (D / 64) * 2;  // (box, slab, K|V)
+        for (int it0 = 0; it0 < items; it0 += 32) {
+          const int it = it0 + lane;
+          const int bx = (it < items ? it : 0) / ((D / 64) * 2);
+          const int32_t t = cb + bx * L.BT;
+          const int32_t j = t / bs;
+          int32_t blk = __shfl_sync(FULL, cur, j - ww);
+          if (it < items) {
+            if (blk < 0 || blk >= p.num_blocks) {
+              set_flag(p.err, NP_FLAG_BLOCK_ID);
+              blk = 0;
+            }
+            const int slab = (it >> 1) % (D / 64);
+            const bool isv = (it & 1) != 0;
+            const int32_t slot = blk * bs + (t - j * bs);
+            tma_load_3d(kdst + (isv ? (uint32_t)(stage_bytes / 2) : 0u) + slab * L.half_bytes +
+                            bx * L.box_bytes,
+                        isv ? &p.tm_v : &p.tm_k, slab * 64, slot, hgi * HG, fb, pol);
+          }
+        }
+        if (++st == stages) {
+          st = 0;
+          ph ^= 1u;
+        }
+      }
+      // into the next segment: its first window was loaded as nxt
+      v = vn;
+      ts = (int32_t)nts;
+      tend = (int32_t)nte;
+      if (v >= 0) {
+        const int32_t w = ts / bs / 32 * 32;
+        cur = (nv == v && nw == w) ? nxt : load_window(v, w);
+        ww = w;
       }
     }
+    const int64_t issued = gch;
     if (*abort) {  // never leave copies in flight (bounded)
       for (int64_t ch = max((int64_t)0, issued - stages); ch < issued; ++ch)
         mbar_wait_drain(smem_u32(&full_bar[ch % stages]), (uint32_t)((ch / stages) & 1));
@@ -255,6 +351,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
   // ======================= consumer warp hl: its kv head of every segment
   const int hl = warp;
+  if (vb == ve && tb == te && vb < V && lane < kMmaRows) {
+    // an empty range inside row vb: an empty partial (m = -inf, l = 0) in
+    // slot 0 for the merge of that row (its o is never read)
+    float* ent = p.ws_o + ((int64_t)b * 2 * HG + hl) * (int64_t)StreamWs::entry_floats(D);
+    ent[lane] = -INFINITY;
+    ent[kMmaRows + lane] = 0.f;
+  }
   const int g4 = lane >> 2, c4 = lane & 3;
   MmaWarp<D, G, TWO> W;
   int64_t gch = 0;
@@ -326,15 +429,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 }
 
 // Merge of the cut rows.  Grid (the read's CTAs, G*Q mma rows); CTA b of
-// the read is blockIdx.x here, and 8 warps = 8 kv heads.  CTA b owns the
-// row its read range ends inside if that row also begins inside it
-// (point(b) <= (v, 0) < point(b+1) < (v, c)); the row's partials are those
-// of CTAs b, b+1, ... while they start before the row's end, each in slot 0
-// when the row is that CTA's first and slot 1 otherwise.  Warp hl merges
-// mma row blockIdx.y of its kv head: lanes take the covering CTAs for the
-// max and the weights, then head_dim for the weighted sum of the partials,
-// which runs over the CTAs in ascending order (a fixed order: results are
-// deterministic).
+// the read is blockIdx.x here, and 8 warps = 8 kv heads.  The read left
+// CTA b's descriptor {v, c, bl, slot}: the row v it owns, cut between CTAs
+// b .. bl.  Warp hl merges mma row blockIdx.y of its kv head: lanes take
+// the covering CTAs for the max and the weights, then head_dim for the
+// weighted sum of the partials, which runs over the CTAs in ascending order
+// (a fixed order: results are deterministic).
 template <int D, int G>
 __global__ void __launch_bounds__(256) paged_decode_stream_merge_kernel(
     const __grid_constant__ DecodeParams p) {
@@ -344,61 +444,27 @@ __global__ void __launch_bounds__(256) paged_decode_stream_merge_kernel(
   constexpr int UNROLL = 8;
   const int b = blockIdx.x;
   const int row = blockIdx.y;
-  const int P = gridDim.x;
   const int hl = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 #if NPK_STREAM_PDL
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the read is complete
 #endif
-  const int64_t* pts = p.st_pts;
-  const int64_t vb = pts[2 * b], tb = pts[2 * b + 1];
-  const int64_t v = pts[2 * b + 2], te = pts[2 * b + 3];
-  const int R = p.rows;
-  if (te == 0 || v >= (int64_t)R * (p.kv_heads / HG)) return;  // b's range ends at a row boundary
-  if (!point_before(vb, tb, v, 0) && !(vb == v && tb == 0)) return;  // v began before b
-  const int64_t cap = (int64_t)p.max_blocks_per_row * p.block_size;
-  int64_t c = p.context_lens[v % R];
-  c = c < 0 ? 0 : (c > cap ? cap : c);
-  const int r = (int)(v % R), hgi = (int)(v / R);
-  const int kvh = hgi * HG + hl;
+  const int4 d = reinterpret_cast<const int4*>(p.st_desc)[b];
   const int Q = p.query_len;
-  if (row >= G * Q) return;
+  if (d.x < 0 || row >= G * Q) return;
+  const int v = d.x, bl = d.z, slot_b = d.w;
+  const int R = p.rows;
+  const int r = v % R, hgi = v / R;
+  const int kvh = hgi * HG + hl;
   const int64_t ent_floats = (int64_t)StreamWs::entry_floats(D);
-
-  // the covering CTAs b..bl: those that start before (v, c)
-  int bl = b;
-  for (int base = b + 1; base < P; base += 32) {
-    const int j = base + lane;
-    const bool cov = j < P && point_before(pts[2 * j], pts[2 * j + 1], v, c);
-    const unsigned m = __ballot_sync(FULL, cov);
-    const int n = __ffs(~m) - 1;  // leading covering lanes (-1: all 32)
-    if (n < 0) {
-      bl = base + 31;
-      continue;
-    }
-    bl = base + n - 1;
-    break;
-  }
-  // lane j's partial of CTA base + j: entry offset (-1 for none), m and l
-  auto load_ml = [&](int base, int64_t& off, float& mj, float& lj) {
-    const int j = base + lane;
-    off = -1;
-    mj = -INFINITY;
-    lj = 0.f;
-    if (j > bl) return;
-    const int64_t v0 = pts[2 * j], t0 = pts[2 * j + 1];
-    if (!point_before(v0, t0, pts[2 * j + 2], pts[2 * j + 3])) return;  // an empty range
-    const int sl = (v0 == v) ? 0 : 1;
-    off = (((int64_t)j * 2 + sl) * HG + hl) * ent_floats;
-    mj = p.ws_o[off + row];
-    lj = p.ws_o[off + kMmaRows + row];
+  auto entry = [&](int j) -> int64_t {  // CTA j's partial of row v, kv head hl
+    return (((int64_t)j * 2 + (j == b ? slot_b : 0)) * HG + hl) * ent_floats;
   };
+
   float mm = -INFINITY;
   for (int base = b; base <= bl; base += 32) {
-    int64_t off;
-    float mj, lj;
-    load_ml(base, off, mj, lj);
-    mm = fmaxf(mm, mj);
+    const int j = base + lane;
+    if (j <= bl) mm = fmaxf(mm, p.ws_o[entry(j) + row]);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(FULL, mm, o));
@@ -408,11 +474,15 @@ __global__ void __launch_bounds__(256) paged_decode_stream_merge_kernel(
 #pragma unroll
   for (int e2 = 0; e2 < DL; ++e2) acc[e2] = 0.f;
   for (int base = b; base <= bl; base += 32) {
-    int64_t off;
-    float mj, lj;
-    load_ml(base, off, mj, lj);
-    const float aj = (off < 0 || mj == -INFINITY) ? 0.f : ex2(mj - mm);
-    lsum = fmaf(aj, lj, lsum);
+    const int j = base + lane;
+    int64_t off = 0;
+    float aj = 0.f;
+    if (j <= bl) {
+      off = entry(j);
+      const float mj = p.ws_o[off + row];
+      aj = mj == -INFINITY ? 0.f : ex2(mj - mm);
+      lsum = fmaf(aj, p.ws_o[off + kMmaRows + row], lsum);
+    }
     const int n = min(32, bl - base + 1);
     for (int k = 0; k < n; k += UNROLL) {
       float ak[UNROLL], ok[UNROLL][DL];
