@@ -80,12 +80,14 @@ np_status device_info(int* sms, int* smem) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Shapes the balanced streamed read (num_splits == 0) handles: bf16 pools,
-// head_dim a multiple of 64, kv heads in groups of 8, at most
-// kStreamMaxVRows (row, head group) pairs, contexts that fit int32.
+// Shapes the balanced streamed read (num_splits == 0) handles: bf16 pools
+// with head_dim a multiple of 64 or fp32 pools with head_dim a multiple of
+// 32, kv heads in groups of 8, at most kStreamMaxVRows (row, head group)
+// pairs, contexts that fit int32.
 bool stream_ok(np_dtype dtype, int32_t head_dim, int32_t kv_heads, int32_t rows,
                int32_t max_blocks_per_row, int32_t block_size) {
-  return dtype == NP_BF16 && head_dim % 64 == 0 && kv_heads % 8 == 0 &&
+  const bool dim_ok = dtype == NP_BF16 ? head_dim % 64 == 0 : head_dim % 32 == 0;
+  return dim_ok && head_dim <= 256 && kv_heads % 8 == 0 &&
          (int64_t)rows * (kv_heads / 8) <= npk::kStreamMaxVRows &&
          (int64_t)max_blocks_per_row * block_size <= INT32_MAX;
 }
@@ -412,7 +414,8 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
   L.head_groups = kv_heads / hg;
   L.streamed = streamed;
   if (streamed) {
-    if (!p.use_tmap) return NP_ERR_UNSUPPORTED;  // the streamed read stages through TMA maps
+    // bf16: the streamed read stages through the TMA maps
+    if (dtype == NP_BF16 && !p.use_tmap) return NP_ERR_UNSUPPORTED;
     L.splits = sms < npk::kStreamMaxCtas ? sms : npk::kStreamMaxCtas;
   }
   L.smem_budget = NPK_SMEM_BUDGET > 0 && NPK_SMEM_BUDGET < smem_optin ? NPK_SMEM_BUDGET

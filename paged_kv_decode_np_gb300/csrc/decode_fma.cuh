@@ -1,0 +1,233 @@
+// decode_fma.cuh -- the fp32 consumer warp of the balanced read: one kv
+// head, its G query heads, full fp32 products on the FMA pipes.
+//
+// What it computes is the read of decode_kernel.cuh (scores q.K in log2
+// units, a running max and sum per head, the accumulator rescaled when the
+// max grows).  The work layout is chosen for instruction count and
+// independent chains on the FMA pipes:
+//   * QK: lane (dl, tg) owns head_dim slice dl (DPL dims) of the chunk's
+//     token group tg (NT tokens); it forms the partial dot products of all
+//     NT tokens x G heads -- NT*GP independent FMA chains of DPL terms.
+//   * The LD lanes of a token group sum those partials with a shuffle
+//     reduce-scatter (each level keeps half of the values and adds the
+//     partner's other half), so every score is finished by one lane with
+//     NT*GP - 1 shuffles in all rather than log2(LD) per score.
+//   * Softmax: finished scores go through a small per-warp tile into a
+//     (token, head) lane layout; lanes of one head reduce the chunk max and
+//     sum with xor-shuffles, write the probabilities and each head's
+//     rescale factor back to the tile.
+//   * PV: lane (dl, tg) again owns head_dim slice dl and accumulates
+//     p[t][h] * V[t][dl] over its token group; token groups are summed at the
+//     end.
+// Stage layout (written by the producer's bulk copies): K rows [token][8 kv
+// heads][D] fp32, then V rows the same.
+#pragma once
+
+#include "decode_kernel.cuh"
+
+namespace npk {
+
+template <int D, int G>
+struct FmaCfg {
+  static constexpr int LD = D / 4 < 32 ? D / 4 : 32;  // lanes across head_dim
+  static constexpr int DPL = D / LD;                   // dims per lane: 4 (8 at D = 256)
+  static constexpr int LT = 32 / LD;                   // token groups
+  static constexpr int CT = 1024 / D;                  // tokens per stage: 64 KB of K+V at 8 heads
+  static constexpr int NT = CT / LT;                   // tokens per lane per chunk
+  static constexpr int GP = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;  // heads, power of two
+  static constexpr int NV = NT * GP;                   // partial scores per lane
+  static constexpr int LOG_LD = LD >= 32 ? 5 : LD >= 16 ? 4 : LD >= 8 ? 3 : LD >= 4 ? 2 : 1;
+  static constexpr int NE = (CT * GP + 31) / 32;       // tile entries per lane in the softmax
+  static constexpr int TILE = CT * GP + 8;             // floats per warp: p[CT][GP], alpha[GP]
+  static_assert(D % 32 == 0 && D <= 256, "fp32 balanced read: head_dim 32..256");
+  static_assert(DPL % 4 == 0 && 32 % LD == 0 && CT % LT == 0 && NT >= 1, "fp32 layout");
+  static_assert(G <= 8, "fp32 balanced read: at most 8 query heads per kv head");
+};
+
+template <int D, int G>
+struct FmaWarp {
+  using C = FmaCfg<D, G>;
+  float q[G][C::DPL];    // this lane's head_dim slice of each head's q (log2 units)
+  float acc[G][C::DPL];  // unnormalised output slice
+  float m, l;            // running max and sum of head (lane % GP)
+
+  __device__ __forceinline__ void begin(const DecodeParams& p, int64_t r, int kvh, int64_t,
+                                        int lane) {
+    const int dl = lane % C::LD;
+    const float* qr = static_cast<const float*>(p.q) + (r * p.q_heads + (int64_t)kvh * G) * D;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      Storage<float>::template load<C::DPL>(qr + h * D + dl * C::DPL, q[h]);
+#pragma unroll
+      for (int e = 0; e < C::DPL; ++e) {
+        q[h][e] *= p.qscale;
+        acc[h][e] = 0.f;
+      }
+    }
+    m = -INFINITY;
+    l = 0.f;
+  }
+
+  // One staged chunk: K rows at ks, V rows at vs ([token][8][D] floats, this
+  // warp's kv head hl), the first nvalid tokens valid; tile = the warp's
+  // scratch of C::TILE floats.
+  __device__ __forceinline__ void consume(const float* ks, const float* vs, int hl, int nvalid,
+                                          float* tile, int lane) {
+    constexpr unsigned FULL = 0xffffffffu;
+    constexpr int GP = C::GP, NT = C::NT, DPL = C::DPL;
+    const int dl = lane % C::LD, tg = lane / C::LD;
+    const int t0 = tg * NT;  // this lane's first token of the chunk
+    const int rowf = 8 * D;  // floats per token row of a stage
+
+    // ---- partial scores x[j*GP + h] over this lane's head_dim slice
+    float x[C::NV];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      float kv[DPL];
+      Storage<float>::template load<DPL>(ks + (t0 + j) * rowf + hl * D + dl * DPL, kv);
+#pragma unroll
+      for (int h = 0; h < GP; ++h) {
+        float a = 0.f;
+        if (h < G) {
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) a = fmaf(q[h][e], kv[e], a);
+        }
+        x[j * GP + h] = a;
+      }
+    }
+    // ---- reduce-scatter over the LD lanes of the token group
+    int base = 0;  // index of x[0] after the scatter levels
+#pragma unroll
+    for (int k = 0; k < C::LOG_LD; ++k) {
+      const int msk = 1 << k;
+      const int n = C::NV >> k;  // values still held
+      if (n >= 2) {
+        const bool up = (lane & msk) != 0;
+        const int half = n / 2;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+          const float send = up ? x[i] : x[i + half];
+          const float keep = up ? x[i + half] : x[i];
+          x[i] = keep + __shfl_xor_sync(FULL, send, msk);
+        }
+        if (up) base += half;
+      } else {
+        x[0] += __shfl_xor_sync(FULL, x[0], msk);
+      }
+    }
+    constexpr int NF = C::NV >= C::LD ? C::NV / C::LD : 1;  // finished scores per lane
+    constexpr int SCAT = C::NV >= C::LD ? C::LOG_LD
+                         : (C::NV >= 32 ? 5 : C::NV >= 16 ? 4 : C::NV >= 8 ? 3
+                            : C::NV >= 4 ? 2 : C::NV >= 2 ? 1 : 0);
+    if ((dl >> SCAT) == 0) {  // one writer per finished score
+#pragma unroll
+      for (int i = 0; i < NF; ++i) tile[t0 * GP + base + i] = x[i];
+    }
+    __syncwarp();
+
+    // ---- softmax in the (token, head) layout: entry e = t*GP + h
+    const int hme = lane % GP;  // every entry of this lane has head hme
+    float s[C::NE];
+    float mt = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < C::NE; ++k) {
+      const int e = lane + 32 * k;
+      const bool ok = e < C::CT * GP && e / GP < nvalid && hme < G;
+      s[k] = ok ? tile[e] : -INFINITY;
+      mt = fmaxf(mt, s[k]);
+    }
+#pragma unroll
+    for (int o = GP; o < 32; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, o));
+    const float mn = fmaxf(m, mt);
+    const float msub = mn == -INFINITY ? 0.f : mn;
+    const float alpha = ex2(m - msub);  // m = -inf: 0 (nothing accumulated yet)
+    float ls = 0.f;
+#pragma unroll
+    for (int k = 0; k < C::NE; ++k) {
+      s[k] = ex2(s[k] - msub);  // -inf: 0
+      ls += s[k];
+    }
+#pragma unroll
+    for (int o = GP; o < 32; o <<= 1) ls += __shfl_xor_sync(FULL, ls, o);
+    l = fmaf(l, alpha, ls);
+    m = mn;
+    __syncwarp();  // every score has been read
+#pragma unroll
+    for (int k = 0; k < C::NE; ++k) {
+      const int e = lane + 32 * k;
+      if (e < C::CT * GP) tile[e] = s[k];
+    }
+    if (lane < GP) tile[C::CT * GP + lane] = alpha;
+    __syncwarp();
+
+    // ---- PV over this lane's tokens and head_dim slice
+    float al[GP];
+#pragma unroll
+    for (int h = 0; h < GP; ++h) al[h] = tile[C::CT * GP + h];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) acc[h][e] *= al[h];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int t = t0 + j;
+      if (t < nvalid) {
+        float pj[GP], vv[DPL];
+#pragma unroll
+        for (int h = 0; h < GP; ++h) pj[h] = tile[t * GP + h];
+        Storage<float>::template load<DPL>(vs + t * rowf + hl * D + dl * DPL, vv);
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) acc[h][e] = fmaf(pj[h], vv[e], acc[h][e]);
+      }
+    }
+    __syncwarp();  // the tile is free for the next chunk
+  }
+
+  // token groups' partial outputs summed (lanes tg == 0 end with the result)
+  __device__ __forceinline__ void finish() {
+    constexpr unsigned FULL = 0xffffffffu;
+#pragma unroll
+    for (int o = C::LD; o < 32; o <<= 1)
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int e = 0; e < C::DPL; ++e) acc[h][e] += __shfl_xor_sync(FULL, acc[h][e], o);
+  }
+
+  // The whole row's normalised output for this kv head's G query heads.
+  __device__ __forceinline__ void store_out(const DecodeParams& p, int64_t r, int kvh,
+                                            int lane) const {
+    constexpr unsigned FULL = 0xffffffffu;
+    const int dl = lane % C::LD;
+    float* o = static_cast<float*>(p.out) + (r * p.q_heads + (int64_t)kvh * G) * D;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float lh = __shfl_sync(FULL, l, h);  // lane h holds head h's sum
+      const float inv = lh > 0.f ? 1.f / lh : 0.f;
+      float v[C::DPL];
+#pragma unroll
+      for (int e = 0; e < C::DPL; ++e) v[e] = acc[h][e] * inv;
+      if (lane < C::LD) Storage<float>::template store<C::DPL>(o + h * D + dl * C::DPL, v);
+    }
+  }
+
+  // Unnormalised rows (one per head) into a [16 rows][D] fp32 array plus m
+  // and l ([16] each), as the merge of cut rows reads them.
+  __device__ __forceinline__ void store_rows(float* m_out, float* l_out, float* o_out, int,
+                                             int lane) const {
+    const int dl = lane % C::LD;
+    if (lane < G) {
+      m_out[lane] = m;
+      l_out[lane] = l;
+    }
+    if (lane < C::LD) {
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        Storage<float>::template store<C::DPL>(o_out + h * D + dl * C::DPL, acc[h]);
+    }
+  }
+};
+
+}  // namespace npk

@@ -78,25 +78,24 @@ np_status launch_variant(DecodeLaunch& L, DecodeParams& p) {
   return cudaGetLastError() == cudaSuccess ? NP_OK : NP_ERR_CUDA;
 }
 
-#if NPK_BF16 && (NPK_D % 64 == 0)
+#if (NPK_BF16 && NPK_D % 64 == 0) || (!NPK_BF16 && NPK_D % 32 == 0)
+#define NPK_HAS_STREAM 1
 // The balanced streamed read: grid = L.splits CTAs (one per SM), 8 kv heads
 // per CTA, the virtual-row prefix in shared memory after the ring.
 template <int G, bool TWO>
 np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
-  using SS = StreamSmem<NPK_D, G>;
-  using SM = MmaSmem<NPK_D, G, true>;
+  using SS = StreamSmem<StorageT, NPK_D, G, TWO>;
   const int vrows = p.rows * (p.kv_heads / 8);
   // static shared memory of the kernel (scan scratch) comes off the budget
   const size_t budget = L.smem_budget - 4096;
   size_t stages = 8;
   while (stages >= 2 && SS::total((int)stages, vrows) > budget) --stages;
   if (stages < 2) return NP_ERR_UNSUPPORTED;
-  (void)sizeof(SM);
   const size_t smem = SS::total((int)stages, vrows);
   p.stages = (int)stages;
   L.stages = (int)stages;
   L.smem_bytes = smem;
-  auto kern = paged_decode_stream_kernel<NPK_D, G, TWO>;
+  auto kern = paged_decode_stream_kernel<StorageT, NPK_D, G, TWO>;
   static unsigned long long configured = 0;  // bit d: attribute set on device d
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return NP_ERR_CUDA;
@@ -118,7 +117,8 @@ np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
   attr[0].val.programmaticStreamSerializationAllowed = NPK_STREAM_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, paged_decode_stream_merge_kernel<NPK_D, G>, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, paged_decode_stream_merge_kernel<StorageT, NPK_D, G>, p) !=
+      cudaSuccess)
     return NP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? NP_OK : NP_ERR_CUDA;
 }
@@ -128,9 +128,11 @@ np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
 // rows (G * query_len > 8).  fp32: one query token only (host-checked).
 template <int G>
 np_status launch_one(DecodeLaunch& L, DecodeParams& p) {
-#if NPK_BF16 && (NPK_D % 64 == 0)
+#if defined(NPK_HAS_STREAM) && NPK_BF16
   if (L.streamed)
     return G * p.query_len > 8 ? launch_stream<G, true>(L, p) : launch_stream<G, false>(L, p);
+#elif defined(NPK_HAS_STREAM)
+  if (L.streamed) return launch_stream<G, false>(L, p);
 #endif
   if (L.streamed) return NP_ERR_UNSUPPORTED;
 #if NPK_BF16

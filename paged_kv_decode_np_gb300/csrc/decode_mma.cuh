@@ -380,6 +380,38 @@ struct MmaWarp {
     lB += __shfl_xor_sync(FULL, lB, 2);
   }
 
+  // The whole row's normalised output: mma row qi*G + h to out[r, qi,
+  // kvh*G + h] (bf16), rows >= G*Q skipped.  After finish().
+  __device__ __forceinline__ void store_out(const DecodeParams& p, int64_t r, int kvh,
+                                            int lane) const {
+    constexpr unsigned FULL = 0xffffffffu;
+    const int Q = p.query_len, MR = G * Q;
+    const int g4 = lane >> 2, c4 = lane & 3;
+    const float l_lo = __shfl_sync(FULL, lA, 8 * c4), l_hi = __shfl_sync(FULL, lA, 8 * c4 + 4);
+    const float lb_lo = __shfl_sync(FULL, lB, 8 * c4), lb_hi = __shfl_sync(FULL, lB, 8 * c4 + 4);
+    auto put = [&](int row, int d, float x, float l) {
+      if (row >= MR) return;
+      const int qi = row / G, h = row - qi * G;
+      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) +
+                         ((r * Q + qi) * p.q_heads + (int64_t)kvh * G + h) * D;
+      o[d] = __float2bfloat16_rn(l > 0.f ? x / l : 0.f);
+    };
+#pragma unroll
+    for (int mi = 0; mi < KS; ++mi) {
+      const int d = 16 * mi + g4;
+      put(2 * c4, d, oA[mi][0], l_lo);
+      put(2 * c4 + 1, d, oA[mi][1], l_hi);
+      put(2 * c4, d + 8, oA[mi][2], l_lo);
+      put(2 * c4 + 1, d + 8, oA[mi][3], l_hi);
+      if constexpr (TWO) {
+        put(8 + 2 * c4, d, oB[mi][0], lb_lo);
+        put(9 + 2 * c4, d, oB[mi][1], lb_hi);
+        put(8 + 2 * c4, d + 8, oB[mi][2], lb_lo);
+        put(9 + 2 * c4, d + 8, oB[mi][3], lb_hi);
+      }
+    }
+  }
+
   // Unnormalised result rows into a [16 rows][D] fp32 array plus m and l
   // ([16] each); rows >= MR are skipped.
   __device__ __forceinline__ void store_rows(float* m_out, float* l_out, float* o_out, int MR,

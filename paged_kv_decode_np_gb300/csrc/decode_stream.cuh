@@ -1,7 +1,9 @@
-// decode_stream.cuh -- the balanced streamed read (bf16 pools, head_dim a
-// multiple of 64, kv heads in groups of 8): the same arithmetic as the split
-// read (decode_mma.cuh), with the work laid out so that every SM gets the same
-// number of history tokens and no thread block is launched for nothing.
+// decode_stream.cuh -- the balanced streamed read (kv heads in groups of 8;
+// bf16 pools with head_dim a multiple of 64 on the tensor cores, through
+// tiled TMA boxes, or fp32 pools with head_dim a multiple of 32 on the FMA
+// pipes, through 1-D bulk copies): the same arithmetic as the split read,
+// with the work laid out so that every SM gets the same number of history
+// tokens and no thread block is launched for nothing.
 //
 // Partition (computed on the device from context_lens; no host sync, so the
 // step stays graph-capturable).  Virtual rows v = hgi*rows + r (row r, kv
@@ -23,6 +25,7 @@
 // and no thread block ever waits for another.
 #pragma once
 
+#include "decode_fma.cuh"
 #include "decode_mma.cuh"
 
 namespace npk {
@@ -57,20 +60,54 @@ struct StreamWs {
 };
 
 
-template <int D, int G>
-struct StreamSmem {
-  using S = MmaSmem<D, G, true>;
-  // ring (1024-aligned) | barriers | abort | virtual-row prefix (int64, V + 1)
-  __host__ __device__ static constexpr size_t total(int stages, int vrows) {
-    return S::total(8, stages, 8) + 16 + (size_t)(vrows + 1) * sizeof(int64_t);
+// Per storage type: tokens per stage, the stage size and the consumer warp.
+template <typename T, int D, int G, bool TWO>
+struct StreamKind;
+
+template <int D, int G, bool TWO>
+struct StreamKind<__nv_bfloat16, D, G, TWO> {  // tensor cores, tiled TMA boxes
+  static constexpr bool kTmap = true;
+  using Warp = MmaWarp<D, G, TWO>;
+  static constexpr int CT = MmaCfg<D, G, true>::CT;
+  static constexpr int ST = MmaCfg<D, G, true>::ST;
+  __host__ __device__ static constexpr size_t stage_bytes() {
+    return MmaSmem<D, G, true>::stage_bytes(8);
   }
+  __host__ __device__ static constexpr size_t tile_floats() { return 0; }
 };
 
 template <int D, int G, bool TWO>
+struct StreamKind<float, D, G, TWO> {  // FMA pipes, 1-D bulk copies of token rows
+  static_assert(!TWO, "fp32 pools: one query token per row");
+  static constexpr bool kTmap = false;
+  using Warp = FmaWarp<D, G>;
+  static constexpr int CT = FmaCfg<D, G>::CT;
+  static constexpr int ST = CT;
+  __host__ __device__ static constexpr size_t stage_bytes() {
+    return 2ull * CT * 8 * D * sizeof(float);
+  }
+  __host__ __device__ static constexpr size_t tile_floats() { return FmaCfg<D, G>::TILE; }
+};
+
+// Shared memory: ring (1024-aligned) | full, empty barriers | abort |
+// virtual-row prefix (int64, V + 1) | consumer tiles (16-aligned).
+template <typename T, int D, int G, bool TWO>
+struct StreamSmem {
+  using K = StreamKind<T, D, G, TWO>;
+  __host__ __device__ static constexpr size_t tiles_offset(int stages, int vrows) {
+    return (K::stage_bytes() * stages + 16ull * stages + 16 +
+            (size_t)(vrows + 1) * sizeof(int64_t) + 15) / 16 * 16;
+  }
+  __host__ __device__ static constexpr size_t total(int stages, int vrows) {
+    return 1024 + tiles_offset(stages, vrows) + 8 * K::tile_floats() * sizeof(float);
+  }
+};
+
+template <typename T, int D, int G, bool TWO>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     paged_decode_stream_kernel(const __grid_constant__ DecodeParams p) {
-  using C = MmaCfg<D, G, true>;
-  using S = MmaSmem<D, G, true>;
+  using K = StreamKind<T, D, G, TWO>;
+  using C = K;  // chunk geometry (CT, ST)
   constexpr unsigned FULL = 0xffffffffu;
   constexpr int HG = 8;
 
@@ -91,12 +128,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int stages = p.stages;
-  const size_t stage_bytes = S::stage_bytes(HG);
-  const size_t ring = S::ring_bytes(HG, stages, HG);
+  const size_t stage_bytes = K::stage_bytes();
+  const size_t ring = stage_bytes * stages;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + ring);
   uint64_t* empty_bar = full_bar + stages;
   volatile int* abort = reinterpret_cast<volatile int*>(empty_bar + stages);
   int64_t* pre = reinterpret_cast<int64_t*>(smem + ring + 16ull * stages + 16);
+  float* tiles =
+      reinterpret_cast<float*>(smem + StreamSmem<T, D, G, TWO>::tiles_offset(stages, V));
   __shared__ int64_t wsum[32];
   __shared__ int64_t range[4];  // vb, tb, ve, te
 
@@ -200,9 +239,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     if (row_len(v) != 0) continue;
     const int r = v % R, hgi = v / R;
     for (int qi = 0; qi < Q; ++qi) {
-      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) +
-                         (((int64_t)r * Q + qi) * p.q_heads + hgi * HG * G) * D;
-      for (int i = threadIdx.x; i < HG * G * D; i += blockDim.x) o[i] = __float2bfloat16_rn(0.f);
+      T* o = static_cast<T*>(p.out) + (((int64_t)r * Q + qi) * p.q_heads + hgi * HG * G) * D;
+      for (int i = threadIdx.x; i < HG * G * D; i += blockDim.x) o[i] = T(0.f);
     }
   }
 
@@ -210,7 +248,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   for (int v = vb; v <= ve && v < V; ++v) {
     int64_t ts, tend;
     seg_bounds(v, ts, tend);
-    if (ts < tend) fused_append<D, 2>(p, v % R, v / R, HG, row_len(v), ts, tend);
+    if (ts < tend) fused_append<D, (int)sizeof(T)>(p, v % R, v / R, HG, row_len(v), ts, tend);
   }
 
   if (threadIdx.x == 0) {
@@ -229,7 +267,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   L.box_bytes = (uint32_t)L.BT * HG * 128;
   L.RS = 0;
   L.hl = warp % HG;
-  if (L.BT < 1 || L.BT > C::CT || C::CT % L.BT != 0) {
+  if (K::kTmap && (L.BT < 1 || L.BT > C::CT || C::CT % L.BT != 0)) {
     if (threadIdx.x == 0) set_flag(p.err, NP_FLAG_CONFIG);
     return;
   }
@@ -272,7 +310,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     uint32_t ph = 1;  // parity of stage st's empty barrier: (gch / stages - 1) & 1
     bool stop = false;
     while (v >= 0 && !stop) {
-      const int r = v % R, hgi = v / R;
+      const int hgi = v / R;
       const int32_t lastw = (tend - 1) / bs / 32 * 32;
       int64_t nts, nte;
       const int vn = next_seg(v + 1, nts, nte);
@@ -303,27 +341,61 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
         const int n = min(C::CT, tend - cb);
         const uint32_t kdst = smem_u32(smem + st * stage_bytes);
+        const uint32_t vdst = kdst + (uint32_t)(stage_bytes / 2);
         const uint32_t fb = smem_u32(&full_bar[st]);
-        const int nbox = (n + L.BT - 1) / L.BT;
-        if (lane == 0) mbar_arrive_expect_tx(fb, 2u * (D / 64) * nbox * L.box_bytes);
-        const int items = nbox * (D / 64) * 2;  // (box, slab, K|V)
-        for (int it0 = 0; it0 < items; it0 += 32) {
-          const int it = it0 + lane;
-          const int bx = (it < items ? it : 0) / ((D / 64) * 2);
-          const int32_t t = cb + bx * L.BT;
-          const int32_t j = t / bs;
-          int32_t blk = __shfl_sync(FULL, cur, j - ww);
-          if (it < items) {
+        if constexpr (K::kTmap) {
+          const int nbox = (n + L.BT - 1) / L.BT;
+          if (lane == 0) mbar_arrive_expect_tx(fb, 2u * (D / 64) * nbox * L.box_bytes);
+          const int items = nbox * (D / 64) * 2;  // (box, slab, K|V)
+          for (int it0 = 0; it0 < items; it0 += 32) {
+            const int it = it0 + lane;
+            const int bx = (it < items ? it : 0) / ((D / 64) * 2);
+            const int32_t t = cb + bx * L.BT;
+            const int32_t j = t / bs;
+            int32_t blk = __shfl_sync(FULL, cur, j - ww);
+            if (it < items) {
+              if (blk < 0 || blk >= p.num_blocks) {
+                set_flag(p.err, NP_FLAG_BLOCK_ID);
+                blk = 0;
+              }
+              const int slab = (it >> 1) % (D / 64);
+              const bool isv = (it & 1) != 0;
+              const int32_t slot = blk * bs + (t - j * bs);
+              tma_load_3d((isv ? vdst : kdst) + slab * L.half_bytes + bx * L.box_bytes,
+                          isv ? &p.tm_v : &p.tm_k, slab * 64, slot, hgi * HG, fb, pol);
+            }
+          }
+        } else {
+          // stage rows [token][8 kv heads][D]: with 8 kv heads in the pool a
+          // run of tokens inside one block is one contiguous copy (lane k:
+          // the chunk's k-th block); else one copy per token (lane = token).
+          // A chunk holds at most 32 tokens and lies in window ww.
+          const uint32_t row_b = 8u * D * (uint32_t)sizeof(T);
+          const int64_t pool_row = (int64_t)p.kv_heads * D * (int64_t)sizeof(T);
+          const char* kp = static_cast<const char*>(p.k_pool) + (int64_t)hgi * row_b;
+          const char* vp = static_cast<const char*>(p.v_pool) + (int64_t)hgi * row_b;
+          if (lane == 0) mbar_arrive_expect_tx(fb, 2u * (uint32_t)n * row_b);
+          const int32_t jf = cb / bs;
+          const bool whole = p.kv_heads == 8;
+          const int32_t j = whole ? jf + lane : (cb + min(lane, n - 1)) / bs;
+          int32_t blk = __shfl_sync(FULL, cur, (j - ww) & 31);
+          int64_t ta, tz;  // this lane's tokens [ta, tz)
+          if (whole) {
+            ta = max((int64_t)cb, (int64_t)j * bs);
+            tz = min((int64_t)cb + n, ((int64_t)j + 1) * bs);
+          } else {
+            ta = cb + lane;
+            tz = lane < n ? ta + 1 : ta;
+          }
+          if (ta < tz) {
             if (blk < 0 || blk >= p.num_blocks) {
               set_flag(p.err, NP_FLAG_BLOCK_ID);
               blk = 0;
             }
-            const int slab = (it >> 1) % (D / 64);
-            const bool isv = (it & 1) != 0;
-            const int32_t slot = blk * bs + (t - j * bs);
-            tma_load_3d(kdst + (isv ? (uint32_t)(stage_bytes / 2) : 0u) + slab * L.half_bytes +
-                            bx * L.box_bytes,
-                        isv ? &p.tm_v : &p.tm_k, slab * 64, slot, hgi * HG, fb, pol);
+            const int64_t slot = (int64_t)blk * bs + (ta - j * bs);
+            const uint32_t off = (uint32_t)(ta - cb) * row_b, bytes = (uint32_t)(tz - ta) * row_b;
+            bulk_g2s(kdst + off, kp + slot * pool_row, bytes, fb, pol);
+            bulk_g2s(vdst + off, vp + slot * pool_row, bytes, fb, pol);
           }
         }
         if (++st == stages) {
@@ -351,15 +423,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
   // ======================= consumer warp hl: its kv head of every segment
   const int hl = warp;
-  if (vb == ve && tb == te && vb < V && lane < kMmaRows) {
-    // an empty range inside row vb: an empty partial (m = -inf, l = 0) in
-    // slot 0 for the merge of that row (its o is never read)
+  if (vb == ve && tb == te && vb < V) {
+    // an empty range inside row vb: an empty partial (m = -inf, l = 0, o = 0)
+    // in slot 0 for the merge of that row
     float* ent = p.ws_o + ((int64_t)b * 2 * HG + hl) * (int64_t)StreamWs::entry_floats(D);
-    ent[lane] = -INFINITY;
-    ent[kMmaRows + lane] = 0.f;
+    if (lane < kMmaRows) {
+      ent[lane] = -INFINITY;
+      ent[kMmaRows + lane] = 0.f;
+    }
+    for (int i = lane; i < kMmaRows * D; i += 32) ent[2 * kMmaRows + i] = 0.f;
   }
-  const int g4 = lane >> 2, c4 = lane & 3;
-  MmaWarp<D, G, TWO> W;
+  typename K::Warp W;
+  float* tile = tiles + (size_t)hl * K::tile_floats();  // fp32 consumers' scratch
   int64_t gch = 0;
   bool first = true;
   for (int v = vb; v <= ve && v < V; ++v) {
@@ -380,41 +455,23 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         break;
       }
       const int nvalid = (int)min((int64_t)C::CT, tend - cb);
-      const uint32_t kst = smem_u32(smem + st * stage_bytes);
-      for (int sb = 0; sb < nvalid; sb += C::ST)
-        W.template tile<true>(L, kst, kst + (uint32_t)(stage_bytes / 2), sb, nvalid, cb,
-                              p.qscale, lane);
+      if constexpr (K::kTmap) {
+        const uint32_t kst = smem_u32(smem + st * stage_bytes);
+        for (int sb = 0; sb < nvalid; sb += C::ST)
+          W.template tile<true>(L, kst, kst + (uint32_t)(stage_bytes / 2), sb, nvalid, cb,
+                                p.qscale, lane);
+      } else {
+        const float* ks = reinterpret_cast<const float*>(smem + st * stage_bytes);
+        W.consume(ks, ks + stage_bytes / 8, hl, nvalid, tile, lane);
+      }
       __syncwarp();  // every lane's reads of this stage are done
       if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
     }
     if (!ok) return;
     W.finish();
 
-    if (ts == 0 && tend == c) {
-      // ---- the whole row is here: normalise and store
-      const float l_lo = __shfl_sync(FULL, W.lA, 8 * c4), l_hi = __shfl_sync(FULL, W.lA, 8 * c4 + 4);
-      const float lb_lo = __shfl_sync(FULL, W.lB, 8 * c4), lb_hi = __shfl_sync(FULL, W.lB, 8 * c4 + 4);
-      auto put = [&](int row, int d, float x, float l) {
-        if (row >= MR) return;
-        const int qi = row / G, h = row - qi * G;
-        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) +
-                           (((int64_t)r * Q + qi) * p.q_heads + kvh * G + h) * D;
-        o[d] = __float2bfloat16_rn(l > 0.f ? x / l : 0.f);
-      };
-#pragma unroll
-      for (int mi = 0; mi < C::KS; ++mi) {
-        const int d = 16 * mi + g4;
-        put(2 * c4, d, W.oA[mi][0], l_lo);
-        put(2 * c4 + 1, d, W.oA[mi][1], l_hi);
-        put(2 * c4, d + 8, W.oA[mi][2], l_lo);
-        put(2 * c4 + 1, d + 8, W.oA[mi][3], l_hi);
-        if constexpr (TWO) {
-          put(8 + 2 * c4, d, W.oB[mi][0], lb_lo);
-          put(9 + 2 * c4, d, W.oB[mi][1], lb_hi);
-          put(8 + 2 * c4, d + 8, W.oB[mi][2], lb_lo);
-          put(9 + 2 * c4, d + 8, W.oB[mi][3], lb_hi);
-        }
-      }
+    if (ts == 0 && tend == c) {  // the whole row is here: normalise and store
+      W.store_out(p, r, kvh, lane);
       first = false;
       continue;
     }
@@ -431,17 +488,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 // Merge of the cut rows.  Grid (the read's CTAs, G*Q mma rows); CTA b of
 // the read is blockIdx.x here, and 8 warps = 8 kv heads.  The read left
 // CTA b's descriptor {v, c, bl, slot}: the row v it owns, cut between CTAs
-// b .. bl.  Warp hl merges mma row blockIdx.y of its kv head: lanes take
-// the covering CTAs for the max and the weights, then head_dim for the
-// weighted sum of the partials, which runs over the CTAs in ascending order
-// (a fixed order: results are deterministic).
-template <int D, int G>
+// b .. bl.  Warp hl merges mma row blockIdx.y of its kv head over batches
+// of U covering CTAs in ascending order; each batch is one round of loads
+// (lane j: partial j's m and l; every lane: its head_dim slice of all U
+// partial rows), then a rescale of the running state to the batch's max
+// (a fixed order: results are deterministic).  Every partial the merge
+// reads is finite (an empty one is m = -inf, l = 0, o = 0), so the weighted
+// sum runs without branches and its loads all issue before the first use.
+template <typename T, int D, int G>
 __global__ void __launch_bounds__(256) paged_decode_stream_merge_kernel(
     const __grid_constant__ DecodeParams p) {
   constexpr unsigned FULL = 0xffffffffu;
   constexpr int HG = 8;
   constexpr int DL = D / 32;
-  constexpr int UNROLL = 8;
+  constexpr int U = DL >= 8 ? 8 : 16;
   const int b = blockIdx.x;
   const int row = blockIdx.y;
   const int hl = threadIdx.x >> 5;
@@ -457,62 +517,56 @@ __global__ void __launch_bounds__(256) paged_decode_stream_merge_kernel(
   const int r = v % R, hgi = v / R;
   const int kvh = hgi * HG + hl;
   const int64_t ent_floats = (int64_t)StreamWs::entry_floats(D);
-  auto entry = [&](int j) -> int64_t {  // CTA j's partial of row v, kv head hl
-    return (((int64_t)j * 2 + (j == b ? slot_b : 0)) * HG + hl) * ent_floats;
+  auto entry = [&](int j) -> const float* {  // CTA j's partial of row v, kv head hl
+    return p.ws_o + (((int64_t)j * 2 + (j == b ? slot_b : 0)) * HG + hl) * ent_floats;
   };
-
-  float mm = -INFINITY;
-  for (int base = b; base <= bl; base += 32) {
-    const int j = base + lane;
-    if (j <= bl) mm = fmaxf(mm, p.ws_o[entry(j) + row]);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(FULL, mm, o));
-
   const int d0 = lane * DL;
-  float lsum = 0.f, acc[DL];
+
+  float mm = -INFINITY, lsum = 0.f, acc[DL];
 #pragma unroll
   for (int e2 = 0; e2 < DL; ++e2) acc[e2] = 0.f;
-  for (int base = b; base <= bl; base += 32) {
-    const int j = base + lane;
-    int64_t off = 0;
-    float aj = 0.f;
-    if (j <= bl) {
-      off = entry(j);
-      const float mj = p.ws_o[off + row];
-      aj = mj == -INFINITY ? 0.f : ex2(mj - mm);
-      lsum = fmaf(aj, p.ws_o[off + kMmaRows + row], lsum);
+  for (int base = b; base <= bl; base += U) {
+    const int nb = min(U, bl - base + 1);
+    float mj = -INFINITY, lj = 0.f;
+    if (lane < nb) {
+      const float* e = entry(base + lane);
+      mj = e[row];
+      lj = e[kMmaRows + row];
     }
-    const int n = min(32, bl - base + 1);
-    for (int k = 0; k < n; k += UNROLL) {
-      float ak[UNROLL], ok[UNROLL][DL];
+    float ok[U][DL];
 #pragma unroll
-      for (int u = 0; u < UNROLL; ++u) {  // the loads of UNROLL partials first
-        const int src = (k + u) & 31;
-        ak[u] = __shfl_sync(FULL, aj, src);
-        const int64_t of = __shfl_sync(FULL, off, src);
-        const bool use = k + u < n && ak[u] != 0.f;
-        const float* e = p.ws_o + (use ? of : 0) + 2 * kMmaRows + row * D + d0;
-#pragma unroll
-        for (int e2 = 0; e2 < DL; ++e2) ok[u][e2] = use ? e[e2] : 0.f;
-        if (!use) ak[u] = 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < UNROLL; ++u)  // then their sum, in CTA order
-#pragma unroll
-        for (int e2 = 0; e2 < DL; ++e2) acc[e2] = fmaf(ok[u][e2], ak[u], acc[e2]);
+    for (int u = 0; u < U; ++u) {
+      const float* e = entry(u < nb ? base + u : base) + 2 * kMmaRows + row * D + d0;
+      Storage<float>::template load<DL>(e, ok[u]);
     }
+    float bm = mj;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(FULL, bm, o));
+    const float mn = fmaxf(mm, bm);
+    const float msub = mn == -INFINITY ? 0.f : mn;
+    const float sc = ex2(mm - msub);  // mm = -inf: 0 (nothing merged yet)
+    const float aj = ex2(mj - msub);  // an empty partial (m = -inf): 0
+    float ls = aj * lj;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(FULL, ls, o);
+    lsum = fmaf(lsum, sc, ls);
+#pragma unroll
+    for (int e2 = 0; e2 < DL; ++e2) acc[e2] *= sc;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {  // in CTA order; lanes >= nb hold aj = 0
+      const float au = __shfl_sync(FULL, aj, u);
+#pragma unroll
+      for (int e2 = 0; e2 < DL; ++e2) acc[e2] = fmaf(ok[u][e2], au, acc[e2]);
+    }
+    mm = mn;
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(FULL, lsum, o);
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
   float ov[DL];
 #pragma unroll
   for (int e2 = 0; e2 < DL; ++e2) ov[e2] = acc[e2] * inv;
   const int qi = row / G, h = row - qi * G;
-  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) +
-                     (((int64_t)r * Q + qi) * p.q_heads + kvh * G + h) * D;
-  Storage<__nv_bfloat16>::template store<DL>(o + d0, ov);
+  T* o = static_cast<T*>(p.out) + (((int64_t)r * Q + qi) * p.q_heads + kvh * G + h) * D;
+  Storage<T>::template store<DL>(o + d0, ov);
 }
 
 }  // namespace npk

@@ -137,10 +137,13 @@ template <>
 struct Storage<float> {
   static constexpr int kBytes = 4;
   static constexpr np_dtype kDtype = NP_F32;
-  // n elements (4 or 2) from a 16- or 8-byte aligned address
+  // n elements (8, 4 or 2) from a 16- or 8-byte aligned address
   template <int N>
   __device__ __forceinline__ static void load(const float* p, float* x) {
-    if constexpr (N == 4) {
+    if constexpr (N == 8) {
+      load<4>(p, x);
+      load<4>(p + 4, x + 4);
+    } else if constexpr (N == 4) {
       float4 v = *reinterpret_cast<const float4*>(p);
       x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
     } else if constexpr (N == 2) {
@@ -153,7 +156,10 @@ struct Storage<float> {
   }
   template <int N>
   __device__ __forceinline__ static void store(float* p, const float* x) {
-    if constexpr (N == 4) {
+    if constexpr (N == 8) {
+      store<4>(p, x);
+      store<4>(p + 4, x + 4);
+    } else if constexpr (N == 4) {
       *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
     } else if constexpr (N == 2) {
       *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);

@@ -381,6 +381,19 @@ def test_balanced_read(nplib, kv_heads, group, head_dim, block_size, query_len):
     _full_parity(nplib, w, num_splits=0, fused=False)
 
 
+@pytest.mark.parametrize("kv_heads,group,head_dim,block_size", [
+    (8, 4, 128, 16), (8, 1, 128, 32), (8, 2, 64, 8), (8, 8, 32, 3), (8, 5, 256, 16),
+    (16, 4, 128, 16), (16, 2, 256, 1), (8, 8, 128, 24), (8, 4, 32, 64)])
+def test_balanced_read_fp32(nplib, kv_heads, group, head_dim, block_size):
+    """fp32 pools on the balanced read (FMA consumers, 1-D bulk copies:
+    whole block runs at 8 kv heads, one copy per token at 16)."""
+    ctx = [0, 1, 5, 16, 17, 300, 2049, 64, 0, 4000, 31, 7]
+    w = _custom(ctx, kv_heads * group, kv_heads, head_dim, block_size, "f32",
+                seed=180 + kv_heads + group + head_dim + block_size)
+    _full_parity(nplib, w, num_splits=0)
+    _full_parity(nplib, w, num_splits=0, fused=False)
+
+
 def test_balanced_read_two_calls_one_workspace(nplib):
     """The workspace needs no zeroing: a NaN-filled one, reused by a second
     call with other lengths, must not leak stale partials."""
