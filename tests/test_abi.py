@@ -140,8 +140,9 @@ def test_plan_is_static_and_sane(lib):
         s = npg.np_paged_decode_plan(w.rows, w.q_heads, w.kv_heads, w.head_dim, w.block_size,
                                      w.max_blocks_per_row, w.torch_dtype, num_sms=152)
         cap = w.max_blocks_per_row * w.block_size
-        if s == 0:  # the balanced read: bf16, head_dim % 64, kv heads % 8
-            assert w.dtype == "bf16" and w.head_dim % 64 == 0 and w.kv_heads % 8 == 0
+        if s == 0:  # the balanced read: kv heads % 8, head_dim % 64 (bf16) or % 32 (fp32)
+            assert w.kv_heads % 8 == 0 and w.head_dim <= 256
+            assert w.head_dim % (64 if w.dtype == "bf16" else 32) == 0
             continue
         sl = npg.np_paged_decode_split_len(w.block_size, w.max_blocks_per_row, s)
         assert s >= 1 and sl * s >= cap
