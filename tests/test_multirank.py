@@ -62,7 +62,7 @@ def test_reference_arm_prints_on_rank_zero_only():
     assert rc0 == 0 and rc1 == 0, (e0, e1)
     line = json.loads(o0.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
     assert o1.strip() == ""
 
