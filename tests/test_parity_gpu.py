@@ -473,6 +473,70 @@ def test_context_past_table_is_clamped_and_flagged(nplib):
     assert_parity(out[1:], ref[1:], "f32", "the untouched row")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_balanced_bad_block_id_is_flagged_not_faulted(nplib, dtype):
+    """The balanced read walks several rows per thread block: a bad table
+    entry is flagged and read as block 0, and only its own row is affected."""
+    w = _custom([40, 300, 40, 1000], 32, 8, 128, 16, dtype, seed=53)
+    inp = wl.make_inputs(w, poison=False)
+    host = wl.full_host(inp)
+    bt = inp.block_tables.clone()
+    bt[0, 1] = inp.md.num_blocks + 1000                 # outside the pool
+    bt[2, 0] = -5
+    d = wl.Inputs(w, wl.Metadata(inp.context_lens, bt, inp.slot_mapping, inp.md.num_blocks),
+                  *(t.to(DEV) for t in (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new)))
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, s, _ = gpu_step(nplib, d, num_splits=0, err=err)
+    assert s == 0 and int(err.item()) & nplib.NP_FLAG_BLOCK_ID
+    assert torch.isfinite(out.float()).all()
+    ref, _ = oracle_step(host, w.softmax_scale)
+    for r in (1, 3):
+        assert_parity(out[r:r + 1], ref[r:r + 1], dtype, f"untouched row {r}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_balanced_context_out_of_range_is_clamped_and_flagged(nplib, dtype):
+    w = _custom([40, 64, 500, 7], 32, 8, 128, 16, dtype, seed=54)
+    inp = wl.make_inputs(w)
+    host = wl.full_host(inp)
+    cl = inp.context_lens.clone()
+    cl[0] = 10_000                                      # the table holds 512
+    cl[3] = -3                                          # read as empty
+    dmd = wl.Metadata(cl, inp.block_tables, inp.slot_mapping, inp.md.num_blocks)
+    d = wl.Inputs(w, dmd, *(t.to(DEV) for t in
+                            (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new)))
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, s, _ = gpu_step(nplib, d, num_splits=0, err=err)
+    assert s == 0 and int(err.item()) & nplib.NP_FLAG_CONTEXT
+    # row 0 reads table entries past its history (poisoned): its values are
+    # not checked; the others are untouched and row 3 is empty
+    assert torch.isfinite(out[1:].float()).all()
+    assert torch.count_nonzero(out[3]) == 0
+    ref, _ = oracle_step(host, w.softmax_scale)
+    assert_parity(out[1:3], ref[1:3], dtype, "the untouched rows")
+
+
+def test_balanced_read_at_the_row_limit(nplib):
+    """4096 (row, 8-head group) pairs: the largest balanced launch (its row
+    prefix takes 32 KB of shared memory, the ring drops to 2 stages); one more
+    row is refused with NP_ERR_UNSUPPORTED and the plan picks the split grid."""
+    g = torch.Generator().manual_seed(55)
+    ctx = torch.randint(1, 48, (4096,), generator=g).tolist()
+    w = _custom(ctx, 8, 8, 64, 16, "bf16", seed=55)
+    _full_parity(nplib, w, num_splits=0)
+    assert nplib.np_paged_decode_plan(4096, 8, 8, 64, 16, 3, "bf16") == 0
+    assert nplib.np_paged_decode_plan(4097, 8, 8, 64, 16, 3, "bf16") >= 1
+    w2 = _custom(ctx + [5], 8, 8, 64, 16, "bf16", seed=56)
+    inp = wl.make_inputs(w2)
+    d = [t.to(DEV) for t in (inp.q, inp.k_pool, inp.v_pool)]
+    bt, cl = inp.block_tables.to(DEV), inp.context_lens.to(DEV)
+    ws = nplib.workspace(w2.rows, w2.q_heads, w2.head_dim, 0)
+    with pytest.raises(nplib.NPError) as e:
+        nplib.np_paged_decode(torch.empty_like(d[0]), d[0], d[1], d[2], bt, cl, 0.1,
+                              num_splits=0, workspace=ws)
+    assert e.value.status == nplib.NP_ERR_UNSUPPORTED
+
+
 def test_validation_errors_return_before_launch(nplib):
     w = _custom([10], 8, 2, 128, 16, "f32", seed=52)
     inp = wl.make_inputs(w)
