@@ -93,7 +93,8 @@ struct DecodeParams {
 // reads by fence.proxy.async before the barrier that precedes the first copy.
 template <int D, int ES>
 __device__ __forceinline__ void fused_append(const DecodeParams& p, int r, int hgi, int HG,
-                                             int64_t c, int64_t t0, int64_t t1) {
+                                             int64_t c, int64_t t0, int64_t t1,
+                                             int tid = threadIdx.x, int nthreads = blockDim.x) {
   if (p.slot_mapping == nullptr) return;
   const int Q = p.query_len;
   bool wrote = false;
@@ -106,7 +107,7 @@ __device__ __forceinline__ void fused_append(const DecodeParams& p, int r, int h
     const int64_t bs = p.block_size;
     const int64_t b = p.block_tables[(int64_t)r * p.max_blocks_per_row + pos / bs];
     if (b < 0 || b >= p.num_blocks || s != b * bs + pos % bs) {
-      if (threadIdx.x == 0) set_flag(p.err, NP_FLAG_SLOT);
+      if (tid == 0) set_flag(p.err, NP_FLAG_SLOT);
       continue;
     }
     const int64_t nvec = (int64_t)HG * D * ES / 16;  // 16-byte vectors of the slice
@@ -116,7 +117,7 @@ __device__ __forceinline__ void fused_append(const DecodeParams& p, int r, int h
     const uint4* vn = static_cast<const uint4*>(p.v_new);
     uint4* kd = static_cast<uint4*>(const_cast<void*>(p.k_pool));
     uint4* vd = static_cast<uint4*>(const_cast<void*>(p.v_pool));
-    for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+    for (int64_t i = tid; i < nvec; i += nthreads) {
       kd[dst0 + i] = kn[src0 + i];
       vd[dst0 + i] = vn[src0 + i];
     }

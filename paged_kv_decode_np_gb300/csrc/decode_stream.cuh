@@ -144,6 +144,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     return c < 0 ? 0 : (c > cap ? cap : c);
   };
 
+  if (threadIdx.x == 0) {  // the ring's barriers (ordered by the scan's barriers)
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(smem_u32(&full_bar[i]), 1);
+      mbar_init(smem_u32(&empty_bar[i]), HG);  // one arrive per consumer warp
+    }
+    *abort = 0;
+    fence_mbar_init();
+  }
+
   // ---- prefix of the virtual rows' lengths: each thread sums a run of
   // rows, warps scan the run sums with shuffles, warp 0 scans the warp sums
   {
@@ -234,33 +243,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     tend = (v == ve) ? te : row_len(v);
   };
 
-  // ---- rows with no history: zeros (spread over the CTAs)
-  for (int v = b; v < V; v += P) {
-    if (row_len(v) != 0) continue;
-    const int r = v % R, hgi = v / R;
-    for (int qi = 0; qi < Q; ++qi) {
-      T* o = static_cast<T*>(p.out) + (((int64_t)r * Q + qi) * p.q_heads + hgi * HG * G) * D;
-      for (int i = threadIdx.x; i < HG * G * D; i += blockDim.x) o[i] = T(0.f);
-    }
-  }
-
-  // ---- fused append of the new tokens this CTA's segments hold
-  for (int v = vb; v <= ve && v < V; ++v) {
-    int64_t ts, tend;
-    seg_bounds(v, ts, tend);
-    if (ts < tend) fused_append<D, (int)sizeof(T)>(p, v % R, v / R, HG, row_len(v), ts, tend);
-  }
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < stages; ++i) {
-      mbar_init(smem_u32(&full_bar[i]), 1);
-      mbar_init(smem_u32(&empty_bar[i]), HG);  // one arrive per consumer warp
-    }
-    *abort = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-
   StageLayout<D, true> L;
   L.BT = p.box_tokens;
   L.half_bytes = (uint32_t)C::CT * HG * 128;
@@ -270,6 +252,30 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   if (K::kTmap && (L.BT < 1 || L.BT > C::CT || C::CT % L.BT != 0)) {
     if (threadIdx.x == 0) set_flag(p.err, NP_FLAG_CONFIG);
     return;
+  }
+
+  // The consumer warps write the zero rows and the fused append while the
+  // producer starts on the history; they signal named barrier 1 (after
+  // fence.proxy.async, so the appended rows are visible to TMA) and the
+  // producer waits on it before the first chunk that holds a new token.
+  constexpr int kAppendBar = 1;
+  if (warp < HG) {
+    const int tid = threadIdx.x, nthr = 32 * HG;
+    for (int v = b; v < V; v += P) {  // rows with no history: zeros
+      if (row_len(v) != 0) continue;
+      const int r = v % R, hgi = v / R;
+      for (int qi = 0; qi < Q; ++qi) {
+        T* o = static_cast<T*>(p.out) + (((int64_t)r * Q + qi) * p.q_heads + hgi * HG * G) * D;
+        for (int i = tid; i < HG * G * D; i += nthr) o[i] = T(0.f);
+      }
+    }
+    for (int v = vb; v <= ve && v < V; ++v) {  // the new tokens of this CTA's segments
+      int64_t ts, tend;
+      seg_bounds(v, ts, tend);
+      if (ts < tend)
+        fused_append<D, (int)sizeof(T)>(p, v % R, v / R, HG, row_len(v), ts, tend, tid, nthr);
+    }
+    asm volatile("bar.arrive %0, %1;" ::"r"(kAppendBar), "r"(blockDim.x) : "memory");
   }
 
   if (warp == HG) {
@@ -309,9 +315,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     int st = 0;
     uint32_t ph = 1;  // parity of stage st's empty barrier: (gch / stages - 1) & 1
     bool stop = false;
+    const bool fused = p.slot_mapping != nullptr;
+    bool appended = false;  // past named barrier 1 (exactly once)
     while (v >= 0 && !stop) {
       const int hgi = v / R;
       const int32_t lastw = (tend - 1) / bs / 32 * 32;
+      const int32_t first_new = (int32_t)row_len(v) - Q;  // the row's first new position
       int64_t nts, nte;
       const int vn = next_seg(v + 1, nts, nte);
       auto set_next = [&]() {  // the window after (v, ww), loaded now
@@ -340,6 +349,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           set_next();
         }
         const int n = min(C::CT, tend - cb);
+        if (fused && !appended && cb + n > first_new) {
+          asm volatile("bar.sync %0, %1;" ::"r"(kAppendBar), "r"(blockDim.x) : "memory");
+          appended = true;
+        }
         const uint32_t kdst = smem_u32(smem + st * stage_bytes);
         const uint32_t vdst = kdst + (uint32_t)(stage_bytes / 2);
         const uint32_t fb = smem_u32(&full_bar[st]);
@@ -413,6 +426,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         ww = w;
       }
     }
+    if (!appended)  // complete the barrier the consumers signalled
+      asm volatile("bar.sync %0, %1;" ::"r"(kAppendBar), "r"(blockDim.x) : "memory");
     const int64_t issued = gch;
     if (*abort) {  // never leave copies in flight (bounded)
       for (int64_t ch = max((int64_t)0, issued - stages); ch < issued; ++ch)
