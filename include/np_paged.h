@@ -46,9 +46,10 @@
  *     [num_blocks, block_size, kv_heads, head_dim] of `dtype`.
  *   - Supported: dtype NP_F32 or NP_BF16; head_dim in {16, 32, 64, 128, 256};
  *     group g = q_heads/kv_heads in {1, 2, 4, 5, 8}; any block_size >= 1;
- *     any kv_heads >= 1; query_len 1, or (bf16 pools) any query_len with
- *     g * query_len <= 16.  Arithmetic is fp32 in every case (bf16 is
- *     widened exactly); q and out have the pool dtype.
+ *     any kv_heads >= 1; query_len 1, or any query_len with g * query_len
+ *     <= 16 on bf16 pools, or <= 8 on fp32 pools through the balanced read
+ *     (num_splits == 0).  Arithmetic is fp32 in every case (bf16 is widened
+ *     exactly); q and out have the pool dtype.
  *   - Several query tokens per row (query_len Q > 1, speculative or chunked
  *     decode): the row's Q query tokens are its last Q positions
  *     c - Q .. c - 1 (c = context_lens[r], counting them); query token i
@@ -184,9 +185,10 @@ size_t np_paged_decode_workspace_bytes(int32_t rows, int32_t q_heads,
  *                  from context_lens); rows cut between blocks are merged
  *                  by a second launch on `stream`, in block order (results
  *                  are deterministic).  out is written; no reduce call.
- *                  Needs bf16, head_dim a multiple of 64, kv_heads a
- *                  multiple of 8, rows * kv_heads / 8 <= 4096 and a workspace
- *                  (else NP_ERR_UNSUPPORTED / NP_ERR_WORKSPACE).
+ *                  Needs head_dim a multiple of 64 (bf16) or 32 (fp32, up
+ *                  to 256), kv_heads a multiple of 8, rows * kv_heads / 8
+ *                  <= 4096, tables of at most 2^31 - 1 tokens and a
+ *                  workspace (else NP_ERR_UNSUPPORTED / NP_ERR_WORKSPACE).
  *                  Results equal the split read's up to fp32 rounding order.
  *   workspace      device buffer of >= np_paged_decode_workspace_bytes(...)
  *                  bytes, 256-byte aligned (may be NULL when num_splits == 1)

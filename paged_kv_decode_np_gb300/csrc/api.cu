@@ -314,9 +314,13 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
     return NP_ERR_INVALID_ARG;
   if (!head_dim_supported(head_dim) || !group_supported(q_heads / kv_heads))
     return NP_ERR_UNSUPPORTED;
-  // several query tokens: bf16 pools, (query token, head) rows of a group <= 16
-  if (query_len > 1 && (dtype != NP_BF16 || (q_heads / kv_heads) * query_len > 16))
-    return NP_ERR_UNSUPPORTED;
+  // several query tokens: (query token, head) rows of a group <= 16 on bf16
+  // pools; <= 8 on fp32 pools, through the balanced read only
+  if (query_len > 1) {
+    const int64_t mrows = (int64_t)(q_heads / kv_heads) * query_len;
+    if (dtype == NP_BF16 ? mrows > 16 : (mrows > 8 || num_splits != 0))
+      return NP_ERR_UNSUPPORTED;
+  }
   int64_t slots = 0, pool_elems = 0, pool_bytes = 0, tab = 0;
   if (!mul_ok(num_blocks, block_size, &slots) ||
       !mul_ok(slots, (int64_t)kv_heads * head_dim, &pool_elems) ||

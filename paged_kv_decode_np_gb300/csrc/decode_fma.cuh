@@ -1,5 +1,6 @@
 // decode_fma.cuh -- the fp32 consumer warp of the balanced read: one kv
-// head, its G query heads, full fp32 products on the FMA pipes.
+// head, its G query heads (times the row's query tokens), full fp32 products
+// on the FMA pipes.
 //
 // What it computes is the read of decode_kernel.cuh (scores q.K in log2
 // units, a running max and sum per head, the accumulator rescaled when the
@@ -19,6 +20,10 @@
 //   * PV: lane (dl, tg) again owns head_dim slice dl and accumulates
 //     p[t][h] * V[t][dl] over its token group; token groups are summed at the
 //     end.
+// Rows: with one query token per row, the G heads (padded to a power of two);
+// with several (MQ), rows qi*G + h for query token qi and head h, up to 8,
+// each masked to the positions at or before its own (c - Q + qi), as in the
+// tensor-core warp.
 // Stage layout (written by the producer's bulk copies): K rows [token][8 kv
 // heads][D] fp32, then V rows the same.
 #pragma once
@@ -27,14 +32,15 @@
 
 namespace npk {
 
-template <int D, int G>
+template <int D, int G, bool MQ = false>
 struct FmaCfg {
   static constexpr int LD = D / 4 < 32 ? D / 4 : 32;  // lanes across head_dim
   static constexpr int DPL = D / LD;                   // dims per lane: 4 (8 at D = 256)
   static constexpr int LT = 32 / LD;                   // token groups
   static constexpr int CT = 1024 / D;                  // tokens per stage: 64 KB of K+V at 8 heads
   static constexpr int NT = CT / LT;                   // tokens per lane per chunk
-  static constexpr int GP = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;  // heads, power of two
+  static constexpr int NR = MQ ? 8 : G;                // rows computed
+  static constexpr int GP = MQ ? 8 : (G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8);  // padded rows
   static constexpr int NV = NT * GP;                   // partial scores per lane
   static constexpr int LOG_LD = LD >= 32 ? 5 : LD >= 16 ? 4 : LD >= 8 ? 3 : LD >= 4 ? 2 : 1;
   static constexpr int NE = (CT * GP + 31) / 32;       // tile entries per lane in the softmax
@@ -44,35 +50,45 @@ struct FmaCfg {
   static_assert(G <= 8, "fp32 balanced read: at most 8 query heads per kv head");
 };
 
-template <int D, int G>
+template <int D, int G, bool MQ = false>
 struct FmaWarp {
-  using C = FmaCfg<D, G>;
-  float q[G][C::DPL];    // this lane's head_dim slice of each head's q (log2 units)
-  float acc[G][C::DPL];  // unnormalised output slice
-  float m, l;            // running max and sum of head (lane % GP)
+  using C = FmaCfg<D, G, MQ>;
+  static constexpr int NR = C::NR;
+  float q[NR][C::DPL];    // this lane's head_dim slice of each row's q (log2 units)
+  float acc[NR][C::DPL];  // unnormalised output slice
+  float m, l;             // running max and sum of row (lane % GP)
+  int32_t lim;            // last position row (lane % GP) may see (-1: a padding row);
+                          // positions fit int32 on the balanced read
 
-  __device__ __forceinline__ void begin(const DecodeParams& p, int64_t r, int kvh, int64_t,
+  __device__ __forceinline__ void begin(const DecodeParams& p, int64_t r, int kvh, int64_t c,
                                         int lane) {
+    const int Q = p.query_len, MR = G * Q;
     const int dl = lane % C::LD;
-    const float* qr = static_cast<const float*>(p.q) + (r * p.q_heads + (int64_t)kvh * G) * D;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      Storage<float>::template load<C::DPL>(qr + h * D + dl * C::DPL, q[h]);
+    for (int row = 0; row < NR; ++row) {
+      const int qi = row / G, h = row - (row / G) * G;
+      if (row < MR) {
+        const float* qr = static_cast<const float*>(p.q) +
+                          ((r * Q + qi) * p.q_heads + (int64_t)kvh * G + h) * D;
+        Storage<float>::template load<C::DPL>(qr + dl * C::DPL, q[row]);
+      }
 #pragma unroll
       for (int e = 0; e < C::DPL; ++e) {
-        q[h][e] *= p.qscale;
-        acc[h][e] = 0.f;
+        q[row][e] = row < MR ? q[row][e] * p.qscale : 0.f;
+        acc[row][e] = 0.f;
       }
     }
+    const int rme = lane % C::GP;
+    lim = rme < MR ? (int32_t)(c - Q + rme / G) : -1;
     m = -INFINITY;
     l = 0.f;
   }
 
   // One staged chunk: K rows at ks, V rows at vs ([token][8][D] floats, this
-  // warp's kv head hl), the first nvalid tokens valid; tile = the warp's
-  // scratch of C::TILE floats.
+  // warp's kv head hl), its first token at position cb and the first nvalid
+  // tokens valid; tile = the warp's scratch of C::TILE floats.
   __device__ __forceinline__ void consume(const float* ks, const float* vs, int hl, int nvalid,
-                                          float* tile, int lane) {
+                                          int64_t cb, float* tile, int lane) {
     constexpr unsigned FULL = 0xffffffffu;
     constexpr int GP = C::GP, NT = C::NT, DPL = C::DPL;
     const int dl = lane % C::LD, tg = lane / C::LD;
@@ -88,7 +104,7 @@ struct FmaWarp {
 #pragma unroll
       for (int h = 0; h < GP; ++h) {
         float a = 0.f;
-        if (h < G) {
+        if (h < NR) {
 #pragma unroll
           for (int e = 0; e < DPL; ++e) a = fmaf(q[h][e], kv[e], a);
         }
@@ -125,14 +141,15 @@ struct FmaWarp {
     }
     __syncwarp();
 
-    // ---- softmax in the (token, head) layout: entry e = t*GP + h
-    const int hme = lane % GP;  // every entry of this lane has head hme
+    // ---- softmax in the (token, row) layout: entry e = t*GP + row; every
+    // entry of this lane belongs to row lane % GP, which may see positions
+    // up to lim
     float s[C::NE];
     float mt = -INFINITY;
 #pragma unroll
     for (int k = 0; k < C::NE; ++k) {
       const int e = lane + 32 * k;
-      const bool ok = e < C::CT * GP && e / GP < nvalid && hme < G;
+      const bool ok = e < C::CT * GP && e / GP < nvalid && (int32_t)cb + e / GP <= lim;
       s[k] = ok ? tile[e] : -INFINITY;
       mt = fmaxf(mt, s[k]);
     }
@@ -165,7 +182,7 @@ struct FmaWarp {
 #pragma unroll
     for (int h = 0; h < GP; ++h) al[h] = tile[C::CT * GP + h];
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int h = 0; h < NR; ++h)
 #pragma unroll
       for (int e = 0; e < DPL; ++e) acc[h][e] *= al[h];
 #pragma unroll
@@ -177,7 +194,7 @@ struct FmaWarp {
         for (int h = 0; h < GP; ++h) pj[h] = tile[t * GP + h];
         Storage<float>::template load<DPL>(vs + t * rowf + hl * D + dl * DPL, vv);
 #pragma unroll
-        for (int h = 0; h < G; ++h)
+        for (int h = 0; h < NR; ++h)
 #pragma unroll
           for (int e = 0; e < DPL; ++e) acc[h][e] = fmaf(pj[h], vv[e], acc[h][e]);
       }
@@ -191,41 +208,43 @@ struct FmaWarp {
 #pragma unroll
     for (int o = C::LD; o < 32; o <<= 1)
 #pragma unroll
-      for (int h = 0; h < G; ++h)
+      for (int h = 0; h < NR; ++h)
 #pragma unroll
         for (int e = 0; e < C::DPL; ++e) acc[h][e] += __shfl_xor_sync(FULL, acc[h][e], o);
   }
 
-  // The whole row's normalised output for this kv head's G query heads.
+  // The whole row's normalised output: row qi*G + h to out[r, qi, kvh*G + h].
   __device__ __forceinline__ void store_out(const DecodeParams& p, int64_t r, int kvh,
                                             int lane) const {
     constexpr unsigned FULL = 0xffffffffu;
+    const int Q = p.query_len, MR = G * Q;
     const int dl = lane % C::LD;
-    float* o = static_cast<float*>(p.out) + (r * p.q_heads + (int64_t)kvh * G) * D;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float lh = __shfl_sync(FULL, l, h);  // lane h holds head h's sum
+    for (int row = 0; row < NR; ++row) {
+      const float lh = __shfl_sync(FULL, l, row);  // lane `row` holds that row's sum
       const float inv = lh > 0.f ? 1.f / lh : 0.f;
       float v[C::DPL];
 #pragma unroll
-      for (int e = 0; e < C::DPL; ++e) v[e] = acc[h][e] * inv;
-      if (lane < C::LD) Storage<float>::template store<C::DPL>(o + h * D + dl * C::DPL, v);
+      for (int e = 0; e < C::DPL; ++e) v[e] = acc[row][e] * inv;
+      const int qi = row / G, h = row - (row / G) * G;
+      float* o = static_cast<float*>(p.out) + ((r * Q + qi) * p.q_heads + (int64_t)kvh * G + h) * D;
+      if (lane < C::LD && row < MR) Storage<float>::template store<C::DPL>(o + dl * C::DPL, v);
     }
   }
 
-  // Unnormalised rows (one per head) into a [16 rows][D] fp32 array plus m
-  // and l ([16] each), as the merge of cut rows reads them.
-  __device__ __forceinline__ void store_rows(float* m_out, float* l_out, float* o_out, int,
+  // Unnormalised rows into a [16 rows][D] fp32 array plus m and l ([16]
+  // each), as the merge of cut rows reads them; rows >= MR are skipped.
+  __device__ __forceinline__ void store_rows(float* m_out, float* l_out, float* o_out, int MR,
                                              int lane) const {
     const int dl = lane % C::LD;
-    if (lane < G) {
+    if (lane < MR && lane < NR) {
       m_out[lane] = m;
       l_out[lane] = l;
     }
     if (lane < C::LD) {
 #pragma unroll
-      for (int h = 0; h < G; ++h)
-        Storage<float>::template store<C::DPL>(o_out + h * D + dl * C::DPL, acc[h]);
+      for (int row = 0; row < NR; ++row)
+        if (row < MR) Storage<float>::template store<C::DPL>(o_out + row * D + dl * C::DPL, acc[row]);
     }
   }
 };

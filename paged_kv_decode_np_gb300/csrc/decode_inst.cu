@@ -125,14 +125,19 @@ np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
 #endif
 
 // bf16: TWO when the (query token, head) rows spill past the first 8 mma
-// rows (G * query_len > 8).  fp32: one query token only (host-checked).
+// rows (G * query_len > 8).  fp32: several query tokens only on the balanced
+// read, at most 8 rows (host-checked).
 template <int G>
 np_status launch_one(DecodeLaunch& L, DecodeParams& p) {
 #if defined(NPK_HAS_STREAM) && NPK_BF16
   if (L.streamed)
     return G * p.query_len > 8 ? launch_stream<G, true>(L, p) : launch_stream<G, false>(L, p);
 #elif defined(NPK_HAS_STREAM)
-  if (L.streamed) return launch_stream<G, false>(L, p);
+  if (L.streamed) {  // fp32: several query tokens as (query token, head) rows, up to 8
+    if constexpr (G <= 4)
+      if (p.query_len > 1) return launch_stream<G, true>(L, p);
+    return launch_stream<G, false>(L, p);
+  }
 #endif
   if (L.streamed) return NP_ERR_UNSUPPORTED;
 #if NPK_BF16

@@ -76,17 +76,17 @@ struct StreamKind<__nv_bfloat16, D, G, TWO> {  // tensor cores, tiled TMA boxes
   __host__ __device__ static constexpr size_t tile_floats() { return 0; }
 };
 
-template <int D, int G, bool TWO>
-struct StreamKind<float, D, G, TWO> {  // FMA pipes, 1-D bulk copies of token rows
-  static_assert(!TWO, "fp32 pools: one query token per row");
+template <int D, int G, bool MQ>
+struct StreamKind<float, D, G, MQ> {  // FMA pipes, 1-D bulk copies of token rows
+  // MQ: several query tokens per row, (query token, head) rows up to 8
   static constexpr bool kTmap = false;
-  using Warp = FmaWarp<D, G>;
-  static constexpr int CT = FmaCfg<D, G>::CT;
+  using Warp = FmaWarp<D, G, MQ>;
+  static constexpr int CT = FmaCfg<D, G, MQ>::CT;
   static constexpr int ST = CT;
   __host__ __device__ static constexpr size_t stage_bytes() {
     return 2ull * CT * 8 * D * sizeof(float);
   }
-  __host__ __device__ static constexpr size_t tile_floats() { return FmaCfg<D, G>::TILE; }
+  __host__ __device__ static constexpr size_t tile_floats() { return FmaCfg<D, G, MQ>::TILE; }
 };
 
 // Shared memory: ring (1024-aligned) | full, empty barriers | abort |
@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                                 p.qscale, lane);
       } else {
         const float* ks = reinterpret_cast<const float*>(smem + st * stage_bytes);
-        W.consume(ks, ks + stage_bytes / 8, hl, nvalid, tile, lane);
+        W.consume(ks, ks + stage_bytes / 8, hl, nvalid, cb, tile, lane);
       }
       __syncwarp();  // every lane's reads of this stage are done
       if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));

@@ -74,7 +74,7 @@ def test_decode_validation(lib):
     assert _decode(lib, dtype=7, **ok_ptrs) == 2       # dtype
     assert _decode(lib, scale=float("nan"), **ok_ptrs) == 1
     assert _decode(lib, splits=-1, **ok_ptrs) == 1
-    assert _decode(lib, splits=0, **ok_ptrs) == 2            # balanced read: bf16 only
+    assert _decode(lib, splits=0, **ok_ptrs) == 2            # balanced read: kv heads % 8
     assert _decode(lib, splits=0, dtype=1, hk=4, hq=8, **ok_ptrs) == 2  # kv heads % 8
     assert _decode(lib, splits=0, dtype=1, hk=8, hq=16, nb=16, **ok_ptrs) == 3  # no workspace
     assert _decode(lib, bs=0, **ok_ptrs) == 1
@@ -88,7 +88,9 @@ def test_decode_validation(lib):
     assert _decode(lib, splits=4, ws=FAKE, wsb=100, **ok_ptrs) == 3
     assert _decode(lib, nb=2**62, **ok_ptrs) == 4            # pool bytes overflow
     assert _decode(lib, qlen=0, **ok_ptrs) == 1              # no query token
-    assert _decode(lib, qlen=2, **ok_ptrs) == 2              # fp32: one query token only
+    assert _decode(lib, qlen=2, **ok_ptrs) == 2              # fp32: several tokens, split grid
+    assert _decode(lib, qlen=2, splits=0, hk=8, hq=16, **ok_ptrs) == 3  # balanced: needs workspace
+    assert _decode(lib, qlen=5, splits=0, hk=8, hq=16, **ok_ptrs) == 2  # fp32: g*query_len > 8
     assert _decode(lib, qlen=9, dtype=1, **ok_ptrs) == 2     # bf16: g*query_len > 16
     assert _decode(lib, qlen=8, dtype=1, splits=4, **ok_ptrs) == 3   # workspace missing
 

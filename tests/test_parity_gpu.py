@@ -346,6 +346,29 @@ def test_multi_query_tokens(nplib, group, query_len):
     _full_parity(nplib, w, num_splits=5, fused=False)
 
 
+@pytest.mark.parametrize("group,query_len,head_dim", [(1, 3, 128), (1, 8, 64), (2, 4, 128),
+                                                       (4, 2, 128), (2, 3, 256), (1, 5, 32)])
+def test_multi_query_tokens_fp32(nplib, group, query_len, head_dim):
+    """fp32 pools: several query tokens per row on the balanced read (FMA
+    warps, (query token, head) rows up to 8), fused append or separate."""
+    ctx = [1, query_len, query_len + 1, 63, 64, 65, 700, 1500, 0]
+    w = _custom(ctx, 8 * group, 8, head_dim, 16, "f32", seed=200 + group * 7 + query_len,
+                query_len=query_len)
+    _full_parity(nplib, w, num_splits=0)
+    _full_parity(nplib, w, num_splits=0, fused=False)
+
+
+def test_multi_query_fp32_needs_the_balanced_read(nplib):
+    w = _custom([40, 70], 16, 8, 128, 16, "f32", seed=210, query_len=2)
+    inp = wl.make_inputs(w)
+    d = [t.to(DEV) for t in (inp.q, inp.k_pool, inp.v_pool)]
+    bt, cl = inp.block_tables.to(DEV), inp.context_lens.to(DEV)
+    with pytest.raises(nplib.NPError) as e:
+        nplib.np_paged_decode(torch.empty_like(d[0]), d[0], d[1], d[2], bt, cl, 0.1,
+                              num_splits=1)
+    assert e.value.status == nplib.NP_ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("head_dim,block_size", [(64, 8), (256, 32), (32, 16)])
 def test_multi_query_head_dims(nplib, head_dim, block_size):
     w = _custom([5, 80, 300], 16, 8, head_dim, block_size, "bf16", seed=130 + head_dim,
