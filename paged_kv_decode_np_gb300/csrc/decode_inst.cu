@@ -108,8 +108,8 @@ np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
   kern<<<L.splits, 32 * (8 + 1), smem, L.stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return NP_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(L.splits, G * p.query_len);
-  cfg.blockDim = dim3(256);
+  cfg.gridDim = dim3(L.splits, (G * p.query_len + kMergeRpb - 1) / kMergeRpb);
+  cfg.blockDim = dim3(256 * kMergeRpb);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = L.stream;
   cudaLaunchAttribute attr[1];

@@ -41,6 +41,13 @@ constexpr int kStreamMaxCtas = 256;    // grid cap (the workspace is sized for i
 #define NPK_STREAM_PDL 1
 #endif
 
+// mma rows per merge block (8 warps, one per kv head, for each): fewer,
+// larger blocks launch faster when a row group has many rows.
+#ifndef NPK_MERGE_RPB
+#define NPK_MERGE_RPB 2
+#endif
+constexpr int kMergeRpb = NPK_MERGE_RPB;
+
 // Workspace of the streamed read (host and device agree on this):
 //   parts  [kStreamMaxCtas][2 slots][8 kv heads] entries of
 //          m[16] l[16] o[16][D] fp32 (16 = mma rows)
@@ -511,15 +518,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 // reads is finite (an empty one is m = -inf, l = 0, o = 0), so the weighted
 // sum runs without branches and its loads all issue before the first use.
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(256) paged_decode_stream_merge_kernel(
+__global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_kernel(
     const __grid_constant__ DecodeParams p) {
   constexpr unsigned FULL = 0xffffffffu;
   constexpr int HG = 8;
   constexpr int DL = D / 32;
-  constexpr int U = DL >= 8 ? 8 : 16;
+  constexpr int U = kMergeRpb >= 4 ? (DL >= 8 ? 4 : 8) : (DL >= 8 ? 8 : 16);
   const int b = blockIdx.x;
-  const int row = blockIdx.y;
-  const int hl = threadIdx.x >> 5;
+  const int row = blockIdx.y * kMergeRpb + (threadIdx.x >> 8);
+  const int hl = (threadIdx.x >> 5) & 7;
   const int lane = threadIdx.x & 31;
 #if NPK_STREAM_PDL
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the read is complete
@@ -550,9 +557,13 @@ __global__ void __launch_bounds__(256) paged_decode_stream_merge_kernel(
     }
     float ok[U][DL];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const float* e = entry(u < nb ? base + u : base) + 2 * kMmaRows + row * D + d0;
-      Storage<float>::template load<DL>(e, ok[u]);
+    for (int u = 0; u < U; ++u) {  // the batch's partials only (nb is known before any load)
+      if (u < nb) {
+        Storage<float>::template load<DL>(entry(base + u) + 2 * kMmaRows + row * D + d0, ok[u]);
+      } else {
+#pragma unroll
+        for (int e2 = 0; e2 < DL; ++e2) ok[u][e2] = 0.f;
+      }
     }
     float bm = mj;
 #pragma unroll
