@@ -18,11 +18,11 @@
 // `out`.  Only the first and the last row of a CTA can be cut; for those the
 // consumer warp of each kv head stores its unnormalised partial (running max
 // m in log2 units, sum l, accumulator O) in the CTA's slot 0 (its first row)
-// or slot 1 (its last row), and the CTA records its start point.  A second,
-// small kernel then merges each cut row -- owned by the CTA where the row
-// begins, one warp per kv head -- over the covering CTAs in CTA order
-// (lse-weighted, the split read's combine), so results are deterministic
-// and no thread block ever waits for another.
+// or slot 1 (its last row), and the CTA that owns a cut row (the one where
+// the row begins) leaves a descriptor of it.  A second, small kernel then
+// merges each cut row -- one warp per (kv head, mma row) -- over the covering
+// CTAs in CTA order (the split read's max-and-weights combine), so results
+// are deterministic and no thread block ever waits for another.
 #pragma once
 
 #include "decode_fma.cuh"
