@@ -80,15 +80,24 @@ np_status device_info(int* sms, int* smem) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// kv heads per CTA of the balanced streamed read: 8, or 4 when the count is
+// a multiple of 4 but not of 8 (0: not a multiple of 4).
+int stream_head_group(int32_t kv_heads) {
+  return kv_heads % 8 == 0 ? 8 : (kv_heads % 4 == 0 ? 4 : 0);
+}
+
 // Shapes the balanced streamed read (num_splits == 0) handles: bf16 pools
 // with head_dim a multiple of 64 or fp32 pools with head_dim a multiple of
-// 32, kv heads in groups of 8, at most kStreamMaxVRows (row, head group)
-// pairs, contexts that fit int32.
+// 32, kv heads in groups of 8 or 4 (bf16 with 4: an even block size, so the
+// TMA boxes keep the swizzle alignment), at most kStreamMaxVRows (row, head
+// group) pairs, contexts that fit int32.
 bool stream_ok(np_dtype dtype, int32_t head_dim, int32_t kv_heads, int32_t rows,
                int32_t max_blocks_per_row, int32_t block_size) {
+  const int hg = stream_head_group(kv_heads);
   const bool dim_ok = dtype == NP_BF16 ? head_dim % 64 == 0 : head_dim % 32 == 0;
-  return dim_ok && head_dim <= 256 && kv_heads % 8 == 0 &&
-         (int64_t)rows * (kv_heads / 8) <= npk::kStreamMaxVRows &&
+  return hg > 0 && dim_ok && head_dim <= 256 &&
+         (dtype != NP_BF16 || hg == 8 || block_size % 2 == 0) &&
+         (int64_t)rows * (kv_heads / hg) <= npk::kStreamMaxVRows &&
          (int64_t)max_blocks_per_row * block_size <= INT32_MAX;
 }
 
@@ -361,7 +370,7 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
   np_status st = device_info(&sms, &smem_optin);
   if (st != NP_OK) return st;
 
-  const int hg = head_group_of(kv_heads);
+  const int hg = streamed ? stream_head_group(kv_heads) : head_group_of(kv_heads);
   DecodeParams p{};
   p.out = out;
   p.ws_o = ws_o;

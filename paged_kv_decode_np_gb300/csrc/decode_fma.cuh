@@ -24,7 +24,7 @@
 // with several (MQ), rows qi*G + h for query token qi and head h, up to 8,
 // each masked to the positions at or before its own (c - Q + qi), as in the
 // tensor-core warp.
-// Stage layout (written by the producer's bulk copies): K rows [token][8 kv
+// Stage layout (written by the producer's bulk copies): K rows [token][hg kv
 // heads][D] fp32, then V rows the same.
 #pragma once
 
@@ -84,16 +84,16 @@ struct FmaWarp {
     l = 0.f;
   }
 
-  // One staged chunk: K rows at ks, V rows at vs ([token][8][D] floats, this
+  // One staged chunk: K rows at ks, V rows at vs ([token][hg][D] floats, this
   // warp's kv head hl), its first token at position cb and the first nvalid
   // tokens valid; tile = the warp's scratch of C::TILE floats.
-  __device__ __forceinline__ void consume(const float* ks, const float* vs, int hl, int nvalid,
-                                          int64_t cb, float* tile, int lane) {
+  __device__ __forceinline__ void consume(const float* ks, const float* vs, int hl, int hg,
+                                          int nvalid, int64_t cb, float* tile, int lane) {
     constexpr unsigned FULL = 0xffffffffu;
     constexpr int GP = C::GP, NT = C::NT, DPL = C::DPL;
     const int dl = lane % C::LD, tg = lane / C::LD;
     const int t0 = tg * NT;  // this lane's first token of the chunk
-    const int rowf = 8 * D;  // floats per token row of a stage
+    const int rowf = hg * D;  // floats per token row of a stage
 
     // ---- partial scores x[j*GP + h] over this lane's head_dim slice
     float x[C::NV];

@@ -85,13 +85,14 @@ np_status launch_variant(DecodeLaunch& L, DecodeParams& p) {
 template <int G, bool TWO>
 np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
   using SS = StreamSmem<StorageT, NPK_D, G, TWO>;
-  const int vrows = p.rows * (p.kv_heads / 8);
+  const int hg = p.head_group;  // 8 or 4
+  const int vrows = p.rows * (p.kv_heads / hg);
   // static shared memory of the kernel (scan scratch) comes off the budget
   const size_t budget = L.smem_budget - 4096;
   size_t stages = 8;
-  while (stages >= 2 && SS::total((int)stages, vrows) > budget) --stages;
+  while (stages >= 2 && SS::total(hg, (int)stages, vrows) > budget) --stages;
   if (stages < 2) return NP_ERR_UNSUPPORTED;
-  const size_t smem = SS::total((int)stages, vrows);
+  const size_t smem = SS::total(hg, (int)stages, vrows);
   p.stages = (int)stages;
   L.stages = (int)stages;
   L.smem_bytes = smem;

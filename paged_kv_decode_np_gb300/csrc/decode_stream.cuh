@@ -1,4 +1,5 @@
-// decode_stream.cuh -- the balanced streamed read (kv heads in groups of 8;
+// decode_stream.cuh -- the balanced streamed read (kv heads in groups of 8,
+// or of 4 when the count is not a multiple of 8;
 // bf16 pools with head_dim a multiple of 64 on the tensor cores, through
 // tiled TMA boxes, or fp32 pools with head_dim a multiple of 32 on the FMA
 // pipes, through 1-D bulk copies): the same arithmetic as the split read,
@@ -77,8 +78,8 @@ struct StreamKind<__nv_bfloat16, D, G, TWO> {  // tensor cores, tiled TMA boxes
   using Warp = MmaWarp<D, G, TWO>;
   static constexpr int CT = MmaCfg<D, G, true>::CT;
   static constexpr int ST = MmaCfg<D, G, true>::ST;
-  __host__ __device__ static constexpr size_t stage_bytes() {
-    return MmaSmem<D, G, true>::stage_bytes(8);
+  __host__ __device__ static constexpr size_t stage_bytes(int hg) {
+    return MmaSmem<D, G, true>::stage_bytes(hg);
   }
   __host__ __device__ static constexpr size_t tile_floats() { return 0; }
 };
@@ -90,23 +91,24 @@ struct StreamKind<float, D, G, MQ> {  // FMA pipes, 1-D bulk copies of token row
   using Warp = FmaWarp<D, G, MQ>;
   static constexpr int CT = FmaCfg<D, G, MQ>::CT;
   static constexpr int ST = CT;
-  __host__ __device__ static constexpr size_t stage_bytes() {
-    return 2ull * CT * 8 * D * sizeof(float);
+  __host__ __device__ static constexpr size_t stage_bytes(int hg) {
+    return 2ull * CT * hg * D * sizeof(float);
   }
   __host__ __device__ static constexpr size_t tile_floats() { return FmaCfg<D, G, MQ>::TILE; }
 };
 
 // Shared memory: ring (1024-aligned) | full, empty barriers | abort |
-// virtual-row prefix (int64, V + 1) | consumer tiles (16-aligned).
+// virtual-row prefix (int64, V + 1) | consumer tiles (16-aligned).  hg = kv
+// heads per CTA (8 or 4).
 template <typename T, int D, int G, bool TWO>
 struct StreamSmem {
   using K = StreamKind<T, D, G, TWO>;
-  __host__ __device__ static constexpr size_t tiles_offset(int stages, int vrows) {
-    return (K::stage_bytes() * stages + 16ull * stages + 16 +
+  __host__ __device__ static constexpr size_t tiles_offset(int hg, int stages, int vrows) {
+    return (K::stage_bytes(hg) * stages + 16ull * stages + 16 +
             (size_t)(vrows + 1) * sizeof(int64_t) + 15) / 16 * 16;
   }
-  __host__ __device__ static constexpr size_t total(int stages, int vrows) {
-    return 1024 + tiles_offset(stages, vrows) + 8 * K::tile_floats() * sizeof(float);
+  __host__ __device__ static constexpr size_t total(int hg, int stages, int vrows) {
+    return 1024 + tiles_offset(hg, stages, vrows) + 8 * K::tile_floats() * sizeof(float);
   }
 };
 
@@ -116,7 +118,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   using K = StreamKind<T, D, G, TWO>;
   using C = K;  // chunk geometry (CT, ST)
   constexpr unsigned FULL = 0xffffffffu;
-  constexpr int HG = 8;
+  const int HG = p.head_group;  // kv heads per CTA: 8, or 4 (consumer warps 0 .. HG-1)
+  constexpr int kProducer = kMaxConsumerWarps;  // warp 8
 
   const int b = blockIdx.x;
   const int P = gridDim.x;
@@ -135,14 +138,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int stages = p.stages;
-  const size_t stage_bytes = K::stage_bytes();
+  const size_t stage_bytes = K::stage_bytes(HG);
   const size_t ring = stage_bytes * stages;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + ring);
   uint64_t* empty_bar = full_bar + stages;
   volatile int* abort = reinterpret_cast<volatile int*>(empty_bar + stages);
   int64_t* pre = reinterpret_cast<int64_t*>(smem + ring + 16ull * stages + 16);
   float* tiles =
-      reinterpret_cast<float*>(smem + StreamSmem<T, D, G, TWO>::tiles_offset(stages, V));
+      reinterpret_cast<float*>(smem + StreamSmem<T, D, G, TWO>::tiles_offset(HG, stages, V));
   __shared__ int64_t wsum[32];
   __shared__ int64_t range[4];  // vb, tb, ve, te
 
@@ -261,13 +264,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     return;
   }
 
-  // The consumer warps write the zero rows and the fused append while the
-  // producer starts on the history; they signal named barrier 1 (after
+  // Warps 0..7 write the zero rows and the fused append while the producer
+  // starts on the history; they signal named barrier 1 (after
   // fence.proxy.async, so the appended rows are visible to TMA) and the
   // producer waits on it before the first chunk that holds a new token.
+  // Warps HG..7 (when HG = 4) have no kv head and leave after that.
   constexpr int kAppendBar = 1;
-  if (warp < HG) {
-    const int tid = threadIdx.x, nthr = 32 * HG;
+  if (warp < kProducer) {
+    const int tid = threadIdx.x, nthr = 32 * kProducer;
     for (int v = b; v < V; v += P) {  // rows with no history: zeros
       if (row_len(v) != 0) continue;
       const int r = v % R, hgi = v / R;
@@ -283,9 +287,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         fused_append<D, (int)sizeof(T)>(p, v % R, v / R, HG, row_len(v), ts, tend, tid, nthr);
     }
     asm volatile("bar.arrive %0, %1;" ::"r"(kAppendBar), "r"(blockDim.x) : "memory");
+    if (warp >= HG) return;
   }
 
-  if (warp == HG) {
+  if (warp == kProducer) {
     // ======================= producer warp: every chunk of every segment
     // Block-table entries come in windows of 32 blocks of one row, aligned
     // to multiples of 32 blocks; a chunk never straddles two (chunk starts
@@ -386,17 +391,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             }
           }
         } else {
-          // stage rows [token][8 kv heads][D]: with 8 kv heads in the pool a
-          // run of tokens inside one block is one contiguous copy (lane k:
-          // the chunk's k-th block); else one copy per token (lane = token).
-          // A chunk holds at most 32 tokens and lies in window ww.
-          const uint32_t row_b = 8u * D * (uint32_t)sizeof(T);
+          // stage rows [token][HG kv heads][D]: when the pool has just HG kv
+          // heads a run of tokens inside one block is one contiguous copy
+          // (lane k: the chunk's k-th block); else one copy per token (lane =
+          // token).  A chunk holds at most 32 tokens and lies in window ww.
+          const uint32_t row_b = (uint32_t)HG * D * (uint32_t)sizeof(T);
           const int64_t pool_row = (int64_t)p.kv_heads * D * (int64_t)sizeof(T);
           const char* kp = static_cast<const char*>(p.k_pool) + (int64_t)hgi * row_b;
           const char* vp = static_cast<const char*>(p.v_pool) + (int64_t)hgi * row_b;
           if (lane == 0) mbar_arrive_expect_tx(fb, 2u * (uint32_t)n * row_b);
           const int32_t jf = cb / bs;
-          const bool whole = p.kv_heads == 8;
+          const bool whole = p.kv_heads == HG;
           const int32_t j = whole ? jf + lane : (cb + min(lane, n - 1)) / bs;
           int32_t blk = __shfl_sync(FULL, cur, (j - ww) & 31);
           int64_t ta, tz;  // this lane's tokens [ta, tz)
@@ -484,7 +489,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                                 p.qscale, lane);
       } else {
         const float* ks = reinterpret_cast<const float*>(smem + st * stage_bytes);
-        W.consume(ks, ks + stage_bytes / 8, hl, nvalid, cb, tile, lane);
+        W.consume(ks, ks + stage_bytes / 8, hl, HG, nvalid, cb, tile, lane);
       }
       __syncwarp();  // every lane's reads of this stage are done
       if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
@@ -521,7 +526,7 @@ template <typename T, int D, int G>
 __global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_kernel(
     const __grid_constant__ DecodeParams p) {
   constexpr unsigned FULL = 0xffffffffu;
-  constexpr int HG = 8;
+  const int HG = p.head_group;  // kv heads per row group: 8 or 4
   constexpr int DL = D / 32;
   constexpr int U = kMergeRpb >= 4 ? (DL >= 8 ? 4 : 8) : (DL >= 8 ? 8 : 16);
   const int b = blockIdx.x;
@@ -533,7 +538,7 @@ __global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_ker
 #endif
   const int4 d = reinterpret_cast<const int4*>(p.st_desc)[b];
   const int Q = p.query_len;
-  if (d.x < 0 || row >= G * Q) return;
+  if (d.x < 0 || row >= G * Q || hl >= HG) return;
   const int v = d.x, bl = d.z, slot_b = d.w;
   const int R = p.rows;
   const int r = v % R, hgi = v / R;

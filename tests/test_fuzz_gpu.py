@@ -24,11 +24,12 @@ def _draw(i: int):
     dtype = rnd.choice(["bf16", "f32"])
     head_dim = rnd.choice([16, 32, 64, 128, 256])
     group = rnd.choice([1, 2, 4, 5, 8])
-    kv_heads = rnd.choice([1, 2, 3, 8, 8, 16, 16])
+    kv_heads = rnd.choice([1, 2, 3, 4, 8, 8, 12, 16])
     block_size = rnd.choice([1, 3, 8, 16, 24, 32, 64])
     rows = rnd.randint(1, 12)
     # several query tokens: bf16 g*Q <= 16 anywhere; fp32 g*Q <= 8 on the balanced read
-    balanced_ok = kv_heads % 8 == 0 and head_dim % (64 if dtype == "bf16" else 32) == 0
+    balanced_ok = (kv_heads % 4 == 0 and head_dim % (64 if dtype == "bf16" else 32) == 0
+                   and (dtype == "f32" or kv_heads % 8 == 0 or block_size % 2 == 0))
     q_max = 16 // group if dtype == "bf16" else (8 // group if balanced_ok else 1)
     query_len = rnd.choice([1, 1, 1, max(1, min(q_max, rnd.randint(2, 5)))])
     budget = 60_000 // (kv_heads * max(head_dim, 32))  # keeps the oracle fast

@@ -390,7 +390,9 @@ def test_head_dim_256_with_eight_kv_heads(nplib):
 # ------------------------------------------- the balanced streamed read ----
 @pytest.mark.parametrize("kv_heads,group,head_dim,block_size,query_len", [
     (8, 4, 128, 16, 1), (8, 8, 128, 32, 1), (8, 5, 128, 8, 1), (16, 1, 64, 16, 1),
-    (8, 2, 256, 32, 1), (8, 4, 128, 16, 3), (8, 8, 64, 64, 2), (16, 4, 128, 4, 1)])
+    (8, 2, 256, 32, 1), (8, 4, 128, 16, 3), (8, 8, 64, 64, 2), (16, 4, 128, 4, 1),
+    (4, 4, 128, 16, 1), (4, 8, 128, 32, 2), (12, 2, 64, 8, 1), (4, 5, 256, 2, 1),
+    (20, 1, 128, 16, 4)])
 def test_balanced_read(nplib, kv_heads, group, head_dim, block_size, query_len):
     """num_splits = 0: one CTA per SM, equal token shares; rows cut between
     CTAs are merged by the second kernel.  Small totals spread over 152
@@ -406,10 +408,12 @@ def test_balanced_read(nplib, kv_heads, group, head_dim, block_size, query_len):
 
 @pytest.mark.parametrize("kv_heads,group,head_dim,block_size", [
     (8, 4, 128, 16), (8, 1, 128, 32), (8, 2, 64, 8), (8, 8, 32, 3), (8, 5, 256, 16),
-    (16, 4, 128, 16), (16, 2, 256, 1), (8, 8, 128, 24), (8, 4, 32, 64)])
+    (16, 4, 128, 16), (16, 2, 256, 1), (8, 8, 128, 24), (8, 4, 32, 64),
+    (4, 4, 128, 16), (12, 1, 256, 3), (4, 8, 64, 1)])
 def test_balanced_read_fp32(nplib, kv_heads, group, head_dim, block_size):
     """fp32 pools on the balanced read (FMA consumers, 1-D bulk copies:
-    whole block runs at 8 kv heads, one copy per token at 16)."""
+    whole block runs when the pool has just the CTA's 8 or 4 kv heads, one
+    copy per token otherwise)."""
     ctx = [0, 1, 5, 16, 17, 300, 2049, 64, 0, 4000, 31, 7]
     w = _custom(ctx, kv_heads * group, kv_heads, head_dim, block_size, "f32",
                 seed=180 + kv_heads + group + head_dim + block_size)
