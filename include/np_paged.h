@@ -295,6 +295,18 @@ np_status np_paged_decode_noalloc(void* out, const void* q, const void* k_pool,
                                   float scale, int32_t num_splits,
                                   int32_t* err_word, np_stream_t stream);
 
+/*
+ * np_selftest_bounded_wait -- checks, on the device, the failure path every
+ * pipeline wait of the read takes when its copies never land: one warp waits
+ * on an mbarrier that nothing completes, gives up after limit_cycles SM
+ * clock cycles (1 .. 2e9; 2e9 is the read's own limit, about 1 s), ORs
+ * NP_FLAG_TIMEOUT into *err_word (device int32, required) and returns; the
+ * context stays usable.  Nothing faults or traps.  For health checks and
+ * tests; not part of a decode step.
+ */
+np_status np_selftest_bounded_wait(int32_t* err_word, int64_t limit_cycles,
+                                   np_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -35,6 +35,7 @@ __all__ = [
     "np_paged_decode_plan", "np_paged_decode_split_len",
     "np_paged_decode_workspace_bytes", "np_paged_decode", "np_paged_decode_reduce",
     "np_paged_decode_noalloc", "NP_NOALLOC_SCRATCH_BYTES", "np_paged_append_decode",
+    "np_selftest_bounded_wait",
     "workspace", "decode_step", "NP_OK", "NP_ERR_INVALID_ARG", "NP_ERR_UNSUPPORTED",
     "NP_ERR_WORKSPACE", "NP_ERR_OUT_OF_RANGE", "NP_ERR_CUDA", "NP_F32", "NP_BF16",
     "NP_FLAG_BLOCK_ID", "NP_FLAG_CONTEXT", "NP_FLAG_SLOT", "NP_FLAG_TIMEOUT", "NP_FLAG_CONFIG",
@@ -113,6 +114,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.np_paged_decode_reduce.restype = ctypes.c_int
     lib.np_paged_decode_reduce.argtypes = [_P, ctypes.c_int, _P, ctypes.c_size_t, _I32, _I32,
                                            _I32, _I32, _P]
+    lib.np_selftest_bounded_wait.restype = ctypes.c_int
+    lib.np_selftest_bounded_wait.argtypes = [_P, _I64, _P]
     if path is None:
         _LIB = lib
     return lib
@@ -315,6 +318,15 @@ def np_paged_decode_noalloc(out, q, k_pool, v_pool, block_tables, context_lens, 
     _check(st, "np_paged_decode_noalloc")
 
 
+def np_selftest_bounded_wait(err_word, limit_cycles: int, stream=None):
+    """Device check of the read's wait-timeout path: a wait that nothing
+    completes gives up after ``limit_cycles`` and ORs NP_FLAG_TIMEOUT into
+    ``err_word`` (a device int32 tensor); see np_paged.h."""
+    st = load().np_selftest_bounded_wait(_dev(err_word, "err_word"), int(limit_cycles),
+                                         _stream(stream))
+    _check(st, "np_selftest_bounded_wait")
+
+
 def decode_step(out, q, k_pool, v_pool, block_tables, context_lens, scale, *, k_new=None,
                 v_new=None, slot_mapping=None, num_splits: int = 1, workspace=None,
                 err_word=None, stream=None, fused: bool = True) -> int:
@@ -330,14 +342,14 @@ def decode_step(out, q, k_pool, v_pool, block_tables, context_lens, scale, *, k_
             k_new.dim() == q.dim():
         np_paged_append_decode(o, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables,
                                context_lens, scale, num_splits, workspace, err_word, stream)
-        launches += 1 if q.shape[0] > 0 else 0
+        launches += (2 if num_splits == 0 else 1) if q.shape[0] > 0 else 0  # + the merge
     else:
         if k_new is not None:
             np_kv_append(k_pool, v_pool, k_new, v_new, slot_mapping, err_word, stream)
             launches += 1 if k_new.shape[0] > 0 else 0
         np_paged_decode(o, q, k_pool, v_pool, block_tables, context_lens, scale, num_splits,
                         workspace, err_word, stream)
-        launches += 1 if q.shape[0] > 0 else 0
+        launches += (2 if num_splits == 0 else 1) if q.shape[0] > 0 else 0
     if num_splits > 1:
         np_paged_decode_reduce(out, workspace, num_splits, stream)
         launches += 1 if q.shape[0] > 0 else 0

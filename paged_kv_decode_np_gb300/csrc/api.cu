@@ -496,4 +496,12 @@ np_status np_paged_decode_reduce(void* out, np_dtype out_dtype, const void* work
                             reinterpret_cast<cudaStream_t>(stream));
 }
 
+np_status np_selftest_bounded_wait(int32_t* err_word, int64_t limit_cycles, np_stream_t stream) {
+  if (!err_word || !aligned(err_word, 4) || limit_cycles < 1 ||
+      limit_cycles > npk::kWaitLimitCycles)
+    return NP_ERR_INVALID_ARG;
+  return npk::launch_bounded_wait_check(err_word, limit_cycles,
+                                        reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

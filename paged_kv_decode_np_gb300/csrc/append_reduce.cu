@@ -154,4 +154,27 @@ np_status launch_reduce(void* out, np_dtype out_dtype, const float* ws_o, const 
   return cudaGetLastError() == cudaSuccess ? NP_OK : NP_ERR_CUDA;
 }
 
+// ---------------------------------------------------- bounded-wait check --
+// One warp waits, with the pipeline's bounded wait, on an mbarrier that
+// nothing will ever complete: after `limit` cycles the wait gives up, the
+// kernel flags NP_FLAG_TIMEOUT and returns -- the path every pipeline wait
+// takes when its copies never land, exercised without any fault.
+__global__ void __launch_bounds__(32) bounded_wait_check_kernel(int32_t* err, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);  // expects one arrival; none comes
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(smem_u32(&bar), 0u, &abort_flag, limit);
+  if (!__all_sync(0xffffffffu, ok) && threadIdx.x == 0) set_flag(err, NP_FLAG_TIMEOUT);
+}
+
+np_status launch_bounded_wait_check(int32_t* err, long long limit, cudaStream_t stream) {
+  bounded_wait_check_kernel<<<1, 32, 0, stream>>>(err, limit);
+  return cudaGetLastError() == cudaSuccess ? NP_OK : NP_ERR_CUDA;
+}
+
 }  // namespace npk

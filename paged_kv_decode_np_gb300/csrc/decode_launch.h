@@ -46,6 +46,7 @@ np_status decode_bf16_d256(DecodeLaunch&, DecodeParams&);
 np_status launch_append(void* k_pool, void* v_pool, int64_t num_slots, int64_t row_bytes,
                         const void* k_new, const void* v_new, const int64_t* slot_mapping,
                         int32_t num_tokens, int32_t* err, cudaStream_t s);
+np_status launch_bounded_wait_check(int32_t* err, long long limit, cudaStream_t stream);
 np_status launch_reduce(void* out, np_dtype out_dtype, const float* ws_o, const float* ws_lse,
                         int32_t rows, int32_t q_heads, int32_t head_dim, int32_t num_splits,
                         cudaStream_t s);

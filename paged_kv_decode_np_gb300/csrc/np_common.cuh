@@ -62,17 +62,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity has completed.  Bounded: gives
-// up (returns false) when *abort becomes non-zero or after kWaitLimitCycles, in
-// which case it sets *abort itself so every other waiter in the block stops.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort) {
+// up (returns false) when *abort becomes non-zero or after `limit` cycles
+// (kWaitLimitCycles unless a self-test asks for less), in which case it sets
+// *abort itself so every other waiter in the block stops.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (clock64() - t0 > kWaitLimitCycles) {
+      if (clock64() - t0 > limit) {
         *abort = 1;
         return false;
       }

@@ -564,6 +564,20 @@ def test_balanced_read_at_the_row_limit(nplib):
     assert e.value.status == nplib.NP_ERR_UNSUPPORTED
 
 
+def test_bounded_wait_gives_up_and_the_context_stays_usable(nplib):
+    """The read's wait-timeout path, exercised without any fault: a wait that
+    nothing completes gives up after ~1 ms, flags NP_FLAG_TIMEOUT, and the
+    next read on the same context is correct."""
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    nplib.np_selftest_bounded_wait(err, 2_000_000)       # ~1 ms at 2 GHz
+    torch.cuda.synchronize()
+    assert int(err.item()) == nplib.NP_FLAG_TIMEOUT
+    with pytest.raises(nplib.NPError):
+        nplib.np_selftest_bounded_wait(err, 0)
+    w = _custom([300, 5, 2000], 32, 8, 128, 16, "bf16", seed=57)
+    _full_parity(nplib, w)
+
+
 def test_validation_errors_return_before_launch(nplib):
     w = _custom([10], 8, 2, 128, 16, "f32", seed=52)
     inp = wl.make_inputs(w)
