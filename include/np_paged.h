@@ -180,7 +180,7 @@ size_t np_paged_decode_workspace_bytes(int32_t rows, int32_t q_heads,
  *                  output and lse into `workspace`; call
  *                  np_paged_decode_reduce next to produce out.
  *                  0: the balanced read -- one thread block per SM (at most
- *                  256), each taking an equal, chunk-aligned share of all
+ *                  160), each taking an equal, chunk-aligned share of all
  *                  rows' history laid end to end (computed on the device
  *                  from context_lens); rows cut between blocks are merged
  *                  by a second launch on `stream`, in block order (results
@@ -273,7 +273,9 @@ np_status np_paged_decode_reduce(void* out, np_dtype out_dtype,
  *   - Returns NP_ERR_WORKSPACE, before anything is enqueued, when the
  *     partials, np_paged_decode_workspace_bytes(rows * query_len, q_heads,
  *     head_dim, num_splits), exceed NP_NOALLOC_SCRATCH_BYTES; a smaller
- *     num_splits fits.  num_splits <= 1 uses no scratch at all.
+ *     num_splits fits.  num_splits == 1 uses no scratch at all;
+ *     num_splits == 0 (the balanced read) keeps its cut-row partials there
+ *     (it fits for head_dim <= 128).
  *   - The first call on a device looks up the array's device address for
  *     that device (cudaGetSymbolAddress); make that first call before any
  *     stream capture.

@@ -32,7 +32,8 @@
 namespace npk {
 
 constexpr int kStreamMaxVRows = 4096;  // virtual rows (row, 8-head group) per launch
-constexpr int kStreamMaxCtas = 256;    // grid cap (the workspace is sized for it)
+constexpr int kStreamMaxCtas = 160;    // grid cap, >= the GB300's 152 SMs (the
+                                       // workspace is sized for it)
 
 // The merge launch is a programmatic dependent of the read: it may be
 // scheduled once every CTA of the read has started, and waits in

@@ -42,12 +42,23 @@ extern "C" np_status np_paged_decode_noalloc(
     const int32_t* block_tables, int32_t max_blocks_per_row, const int32_t* context_lens,
     int32_t rows, int32_t query_len, int32_t q_heads, float scale, int32_t num_splits,
     int32_t* err_word, np_stream_t stream) {
-  if (num_splits <= 1)  // nothing to merge: no scratch involved
+  if (num_splits == 1)  // nothing to merge: no scratch involved
     return np_paged_decode(out, q, k_pool, v_pool, dtype, num_blocks, block_size, kv_heads,
                            head_dim, block_tables, max_blocks_per_row, context_lens, rows,
                            query_len, q_heads, scale, num_splits, nullptr, 0, err_word, stream);
   if (rows < 0 || query_len <= 0 || q_heads <= 0 || head_dim <= 0) return NP_ERR_INVALID_ARG;
   if (rows == 0) return NP_OK;
+  if (num_splits == 0) {  // the balanced read: its cut-row partials go to the scratch
+    const size_t need = np_paged_decode_workspace_bytes(rows, q_heads, head_dim, 0);
+    if (need == 0 || need > (size_t)NP_NOALLOC_SCRATCH_BYTES) return NP_ERR_WORKSPACE;
+    void* ws = nullptr;
+    np_status st = scratch_address(&ws);
+    if (st != NP_OK) return st;
+    return np_paged_decode(out, q, k_pool, v_pool, dtype, num_blocks, block_size, kv_heads,
+                           head_dim, block_tables, max_blocks_per_row, context_lens, rows,
+                           query_len, q_heads, scale, 0, ws, NP_NOALLOC_SCRATCH_BYTES, err_word,
+                           stream);
+  }
   if (out == nullptr || reinterpret_cast<uintptr_t>(out) % 16 != 0) return NP_ERR_INVALID_ARG;
   const int32_t units_rows = rows * query_len;
   const size_t need = np_paged_decode_workspace_bytes(units_rows, q_heads, head_dim, num_splits);

@@ -24,11 +24,11 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _case(contexts, q_heads, kv_heads, block_size, dtype, seed):
+def _case(contexts, q_heads, kv_heads, block_size, dtype, seed, poison=True):
     w = wl.Workload(f"noalloc-{seed}", rows=len(contexts), q_heads=q_heads, kv_heads=kv_heads,
                     head_dim=128, block_size=block_size, dtype=dtype,
                     ctx=("fixed", tuple(contexts)), pool=("spare", 2), seed=seed)
-    inp = wl.make_inputs(w, device=DEV)
+    inp = wl.make_inputs(w, device=DEV, poison=poison)
     bt, cl = inp.block_tables.to(DEV), inp.context_lens.to(DEV)
     return w, inp, bt, cl
 
@@ -68,4 +68,32 @@ def test_noalloc_rejects_partials_larger_than_its_scratch(nplib):
     with pytest.raises(nplib.NPError) as e:
         nplib.np_paged_decode_noalloc(out, inp.q, inp.k_pool, inp.v_pool, bt, cl,
                                       w.softmax_scale, too_many)
+    assert e.value.status == nplib.NP_ERR_WORKSPACE
+
+
+def test_noalloc_balanced_read(nplib):
+    """num_splits = 0: the balanced read keeps its cut-row partials in the
+    library's array (head_dim 128 fits, 256 does not)."""
+    for (w, inp, bt, cl) in (_case([33, 2000, 700, 5, 1500], 40, 8, 32, "bf16", seed=84,
+                                   poison=False),
+                             _case([900, 1, 64, 3100], 32, 8, 16, "f32", seed=85,
+                                   poison=False)):
+        ws = nplib.workspace(w.rows, w.q_heads, w.head_dim, 0, device=DEV)
+        ref = torch.empty_like(inp.q)
+        nplib.np_paged_decode(ref, inp.q, inp.k_pool, inp.v_pool, bt, cl, w.softmax_scale, 0, ws)
+        out = torch.full_like(inp.q, float("nan"))
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        nplib.np_paged_decode_noalloc(out, inp.q, inp.k_pool, inp.v_pool, bt, cl,
+                                      w.softmax_scale, 0, err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert torch.isfinite(out.float()).all()
+        assert torch.equal(out, ref)  # the same launches, bit for bit
+    w = wl.Workload("noalloc-d256", rows=2, q_heads=16, kv_heads=8, head_dim=256, block_size=16,
+                    dtype="bf16", ctx=("fixed", (40, 70)), pool=("spare", 2), seed=86)
+    inp = wl.make_inputs(w, device=DEV)
+    with pytest.raises(nplib.NPError) as e:
+        nplib.np_paged_decode_noalloc(torch.empty_like(inp.q), inp.q, inp.k_pool, inp.v_pool,
+                                      inp.block_tables.to(DEV), inp.context_lens.to(DEV),
+                                      w.softmax_scale, 0)
     assert e.value.status == nplib.NP_ERR_WORKSPACE
