@@ -109,7 +109,7 @@ np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
   kern<<<L.splits, 32 * (8 + 1), smem, L.stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return NP_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(L.splits, (G * p.query_len + kMergeRpb - 1) / kMergeRpb);
+  cfg.gridDim = dim3(L.splits, (L.group * p.query_len + kMergeRpb - 1) / kMergeRpb);
   cfg.blockDim = dim3(256 * kMergeRpb);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = L.stream;
@@ -125,14 +125,16 @@ np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
 }
 #endif
 
-// bf16: TWO when the (query token, head) rows spill past the first 8 mma
-// rows (G * query_len > 8).  fp32: several query tokens only on the balanced
-// read, at most 8 rows (host-checked).
+// bf16 (G = 0: the group is read at run time, any g with g * query_len <=
+// 16): TWO when the (query token, head) rows spill past the first 8 mma rows.
+// fp32: several query tokens only on the balanced read, at most 8 rows
+// (host-checked).
 template <int G>
 np_status launch_one(DecodeLaunch& L, DecodeParams& p) {
 #if defined(NPK_HAS_STREAM) && NPK_BF16
   if (L.streamed)
-    return G * p.query_len > 8 ? launch_stream<G, true>(L, p) : launch_stream<G, false>(L, p);
+    return L.group * p.query_len > 8 ? launch_stream<G, true>(L, p)
+                                     : launch_stream<G, false>(L, p);
 #elif defined(NPK_HAS_STREAM)
   if (L.streamed) {  // fp32: several query tokens as (query token, head) rows, up to 8
     if constexpr (G <= 4)
@@ -142,7 +144,7 @@ np_status launch_one(DecodeLaunch& L, DecodeParams& p) {
 #endif
   if (L.streamed) return NP_ERR_UNSUPPORTED;
 #if NPK_BF16
-  const bool two = G * p.query_len > 8;
+  const bool two = L.group * p.query_len > 8;
 #if NPK_D % 64 == 0
   if (p.use_tmap)
     return two ? launch_variant<G, true, true>(L, p) : launch_variant<G, true, false>(L, p);
@@ -158,6 +160,9 @@ np_status launch_one(DecodeLaunch& L, DecodeParams& p) {
 }  // namespace
 
 np_status NPK_LAUNCHER(DecodeLaunch& L, DecodeParams& p) {
+#if NPK_BF16
+  return launch_one<0>(L, p);  // the tensor-core warps take the group at run time
+#else
   switch (L.group) {
     case 1: return launch_one<1>(L, p);
     case 2: return launch_one<2>(L, p);
@@ -166,6 +171,7 @@ np_status NPK_LAUNCHER(DecodeLaunch& L, DecodeParams& p) {
     case 8: return launch_one<8>(L, p);
     default: return NP_ERR_UNSUPPORTED;
   }
+#endif
 }
 
 }  // namespace npk

@@ -87,7 +87,7 @@ struct MmaCfg {
   static constexpr int CT = mma_chunk_tokens(D);  // tokens per stage
   // CT < ST is allowed: the tile's rows past the chunk are masked and their
   // shared-memory reads are redirected to the tile's first row.
-  static_assert(D % 16 == 0 && G >= 1 && G <= 8, "shape");
+  static_assert(D % 16 == 0 && G >= 0 && G <= 16, "shape");  // G = 0: set at run time
   static_assert((CT % ST == 0 || ST % CT == 0) && CT <= 32, "tiling");
   static_assert(!TMAP || D % 64 == 0, "TMA boxes are 64 dims wide");
 };
@@ -242,21 +242,23 @@ struct MmaWarp {
   float oA[KS][4];
   float oB[TWO ? KS : 1][4];
   int64_t limA, limB;  // last position each row may see (-1: a padding row)
+  int gr;              // query heads per kv head (G, or q_heads/kv_heads when G = 0)
 
   // q of row r, kv head kvh: mma row qi*G + h is query token qi, head
   // kvh*G + h; rows >= G*Q are zero.  Resets the softmax state.
   __device__ __forceinline__ void begin(const DecodeParams& p, int64_t r, int kvh, int64_t c,
                                         int lane) {
-    const int Q = p.query_len, MR = G * Q;
+    gr = G > 0 ? G : p.q_heads / p.kv_heads;
+    const int Q = p.query_len, MR = gr * Q;
     const int g4 = lane >> 2, c4 = lane & 3;
     auto qrow = [&](int row) -> const __nv_bfloat16* {
-      const int qi = row / G, h = row - (row / G) * G;
+      const int qi = row / gr, h = row - (row / gr) * gr;
       return static_cast<const __nv_bfloat16*>(p.q) +
-             ((r * Q + qi) * p.q_heads + kvh * G + h) * D;
+             ((r * Q + qi) * p.q_heads + kvh * gr + h) * D;
     };
     const bool liveA = g4 < MR, liveB = g4 + 8 < MR;
-    limA = liveA ? c - Q + g4 / G : -1;
-    limB = liveB ? c - Q + (g4 + 8) / G : -1;
+    limA = liveA ? c - Q + g4 / gr : -1;
+    limB = liveB ? c - Q + (g4 + 8) / gr : -1;
     const __nv_bfloat16* qa = liveA ? qrow(g4) : nullptr;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
@@ -381,33 +383,53 @@ struct MmaWarp {
   }
 
   // The whole row's normalised output: mma row qi*G + h to out[r, qi,
-  // kvh*G + h] (bf16), rows >= G*Q skipped.  After finish().
+  // kvh*G + h] (bf16), rows >= G*Q skipped.  After finish().  Each lane
+  // writes four rows at most (2*c4, 2*c4 + 1 and, with TWO, 8 more): their
+  // addresses and reciprocal sums are formed once.
   __device__ __forceinline__ void store_out(const DecodeParams& p, int64_t r, int kvh,
                                             int lane) const {
     constexpr unsigned FULL = 0xffffffffu;
-    const int Q = p.query_len, MR = G * Q;
+    const int Q = p.query_len, MR = gr * Q;
     const int g4 = lane >> 2, c4 = lane & 3;
     const float l_lo = __shfl_sync(FULL, lA, 8 * c4), l_hi = __shfl_sync(FULL, lA, 8 * c4 + 4);
     const float lb_lo = __shfl_sync(FULL, lB, 8 * c4), lb_hi = __shfl_sync(FULL, lB, 8 * c4 + 4);
-    auto put = [&](int row, int d, float x, float l) {
-      if (row >= MR) return;
-      const int qi = row / G, h = row - qi * G;
-      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) +
-                         ((r * Q + qi) * p.q_heads + (int64_t)kvh * G + h) * D;
-      o[d] = __float2bfloat16_rn(l > 0.f ? x / l : 0.f);
+    auto row_ptr = [&](int row) -> __nv_bfloat16* {
+      if (row >= MR) return nullptr;
+      const int qi = row / gr, h = row - qi * gr;
+      return static_cast<__nv_bfloat16*>(p.out) +
+             ((r * Q + qi) * p.q_heads + (int64_t)kvh * gr + h) * D;
     };
+    auto inv = [](float l) { return l > 0.f ? 1.f / l : 0.f; };
+    __nv_bfloat16* o0 = row_ptr(2 * c4);
+    __nv_bfloat16* o1 = row_ptr(2 * c4 + 1);
+    const float i0 = inv(l_lo), i1 = inv(l_hi);
 #pragma unroll
     for (int mi = 0; mi < KS; ++mi) {
       const int d = 16 * mi + g4;
-      put(2 * c4, d, oA[mi][0], l_lo);
-      put(2 * c4 + 1, d, oA[mi][1], l_hi);
-      put(2 * c4, d + 8, oA[mi][2], l_lo);
-      put(2 * c4 + 1, d + 8, oA[mi][3], l_hi);
-      if constexpr (TWO) {
-        put(8 + 2 * c4, d, oB[mi][0], lb_lo);
-        put(9 + 2 * c4, d, oB[mi][1], lb_hi);
-        put(8 + 2 * c4, d + 8, oB[mi][2], lb_lo);
-        put(9 + 2 * c4, d + 8, oB[mi][3], lb_hi);
+      if (o0) {
+        o0[d] = __float2bfloat16_rn(oA[mi][0] * i0);
+        o0[d + 8] = __float2bfloat16_rn(oA[mi][2] * i0);
+      }
+      if (o1) {
+        o1[d] = __float2bfloat16_rn(oA[mi][1] * i1);
+        o1[d + 8] = __float2bfloat16_rn(oA[mi][3] * i1);
+      }
+    }
+    if constexpr (TWO) {
+      __nv_bfloat16* o8 = row_ptr(8 + 2 * c4);
+      __nv_bfloat16* o9 = row_ptr(9 + 2 * c4);
+      const float i8 = inv(lb_lo), i9 = inv(lb_hi);
+#pragma unroll
+      for (int mi = 0; mi < KS; ++mi) {
+        const int d = 16 * mi + g4;
+        if (o8) {
+          o8[d] = __float2bfloat16_rn(oB[mi][0] * i8);
+          o8[d + 8] = __float2bfloat16_rn(oB[mi][2] * i8);
+        }
+        if (o9) {
+          o9[d] = __float2bfloat16_rn(oB[mi][1] * i9);
+          o9[d + 8] = __float2bfloat16_rn(oB[mi][3] * i9);
+        }
       }
     }
   }
@@ -468,9 +490,10 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
   const int NC = HG * TW;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int hq0 = hgi * HG * G;
+  const int Gr = G > 0 ? G : p.q_heads / p.kv_heads;  // query heads per kv head
+  const int hq0 = hgi * HG * Gr;
   const int Q = p.query_len;
-  const int MR = G * Q;  // real mma rows (<= 16)
+  const int MR = Gr * Q;  // real mma rows (<= 16)
 
   const int64_t cap = (int64_t)p.max_blocks_per_row * p.block_size;
   int64_t c = p.context_lens[r];
@@ -487,11 +510,11 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
     for (int qi = 0; qi < Q; ++qi) {
       const int64_t rq = (int64_t)r * Q + qi;
       if (p.num_splits > 1) {
-        for (int i = threadIdx.x; i < HG * G; i += blockDim.x)
+        for (int i = threadIdx.x; i < HG * Gr; i += blockDim.x)
           p.ws_lse[(rq * p.q_heads + hq0 + i) * p.num_splits + split] = -INFINITY;
       } else {
         __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + (rq * p.q_heads + hq0) * D;
-        for (int i = threadIdx.x; i < HG * G * D; i += blockDim.x) o[i] = __float2bfloat16_rn(0.f);
+        for (int i = threadIdx.x; i < HG * Gr * D; i += blockDim.x) o[i] = __float2bfloat16_rn(0.f);
       }
     }
     return;
@@ -616,9 +639,9 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
         for (int e = 0; e < DL; ++e) acc[e] = fmaf(mg[2 * RW + row * D + d0 + e], a, acc[e]);
       }
     }
-    const int qi = row / G, h = row - qi * G;
+    const int qi = row / Gr, h = row - qi * Gr;
     const int64_t rq = (int64_t)r * Q + qi;
-    const int hq = kvh * G + h;
+    const int hq = kvh * Gr + h;
     const float inv = ll > 0.f ? 1.f / ll : 0.f;
     float ov[DL];
 #pragma unroll

@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const int NHG = p.kv_heads / HG;
   const int V = R * NHG;
   const int Q = p.query_len;
-  const int MR = G * Q;
+  const int Gr = G > 0 ? G : p.q_heads / p.kv_heads;  // G = 0: the group set at run time
+  const int MR = Gr * Q;
   const int64_t cap = (int64_t)p.max_blocks_per_row * p.block_size;
 #if NPK_STREAM_PDL
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -277,8 +278,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       if (row_len(v) != 0) continue;
       const int r = v % R, hgi = v / R;
       for (int qi = 0; qi < Q; ++qi) {
-        T* o = static_cast<T*>(p.out) + (((int64_t)r * Q + qi) * p.q_heads + hgi * HG * G) * D;
-        for (int i = tid; i < HG * G * D; i += nthr) o[i] = T(0.f);
+        T* o = static_cast<T*>(p.out) + (((int64_t)r * Q + qi) * p.q_heads + hgi * HG * Gr) * D;
+        for (int i = tid; i < HG * Gr * D; i += nthr) o[i] = T(0.f);
       }
     }
     for (int v = vb; v <= ve && v < V; ++v) {  // the new tokens of this CTA's segments
@@ -539,7 +540,8 @@ __global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_ker
 #endif
   const int4 d = reinterpret_cast<const int4*>(p.st_desc)[b];
   const int Q = p.query_len;
-  if (d.x < 0 || row >= G * Q || hl >= HG) return;
+  const int Gr = G > 0 ? G : p.q_heads / p.kv_heads;  // G = 0: the group set at run time
+  if (d.x < 0 || row >= Gr * Q || hl >= HG) return;
   const int v = d.x, bl = d.z, slot_b = d.w;
   const int R = p.rows;
   const int r = v % R, hgi = v / R;
@@ -596,8 +598,8 @@ __global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_ker
   float ov[DL];
 #pragma unroll
   for (int e2 = 0; e2 < DL; ++e2) ov[e2] = acc[e2] * inv;
-  const int qi = row / G, h = row - qi * G;
-  T* o = static_cast<T*>(p.out) + (((int64_t)r * Q + qi) * p.q_heads + kvh * G + h) * D;
+  const int qi = row / Gr, h = row - qi * Gr;
+  T* o = static_cast<T*>(p.out) + (((int64_t)r * Q + qi) * p.q_heads + kvh * Gr + h) * D;
   Storage<T>::template store<DL>(o + d0, ov);
 }
 

@@ -70,7 +70,11 @@ def test_decode_validation(lib):
     ok_ptrs = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE)
     assert _decode(lib, hq=3, **ok_ptrs) == 1          # q_heads % kv_heads
     assert _decode(lib, d=48, **ok_ptrs) == 2          # head_dim not compiled
-    assert _decode(lib, hk=1, hq=3, **ok_ptrs) == 2    # group 3 not compiled
+    assert _decode(lib, hk=1, hq=3, **ok_ptrs) == 2    # fp32: group 3 not compiled
+    assert _decode(lib, hk=1, hq=17, dtype=1, **ok_ptrs) == 2  # bf16: group > 16
+    # bf16: any group <= 16 passes validation (on a machine without a GPU the
+    # launch itself then fails with NP_ERR_CUDA)
+    assert _decode(lib, hk=1, hq=3, dtype=1, **ok_ptrs) in (0, 5)
     assert _decode(lib, dtype=7, **ok_ptrs) == 2       # dtype
     assert _decode(lib, scale=float("nan"), **ok_ptrs) == 1
     assert _decode(lib, splits=-1, **ok_ptrs) == 1

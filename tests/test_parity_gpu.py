@@ -248,6 +248,22 @@ def test_every_head_dim_and_group(nplib, dtype, head_dim, group):
     _full_parity(nplib, w, num_splits=3)
 
 
+@pytest.mark.parametrize("group,kv_heads,query_len", [
+    (3, 8, 1), (6, 8, 2), (7, 8, 1), (7, 4, 2), (16, 8, 1), (3, 2, 5), (9, 1, 1), (12, 12, 1)])
+def test_any_group_on_bf16(nplib, group, kv_heads, query_len):
+    """bf16 pools take any GQA group up to 16 ((query token, head) rows <= 16):
+    the tensor-core warps read the group at run time.  Balanced read where
+    the kv heads allow it, and the split grid."""
+    ctx = [1, query_len, 300, 2049, 64, 0, 900]
+    ctx = [max(c, query_len) if c else 0 for c in ctx]
+    w = _custom(ctx, kv_heads * group, kv_heads, 128, 16, "bf16",
+                seed=300 + group * 7 + kv_heads + query_len, query_len=query_len)
+    if kv_heads % 4 == 0:
+        _full_parity(nplib, w, num_splits=0)
+    _full_parity(nplib, w, num_splits=1)
+    _full_parity(nplib, w, num_splits=3, fused=False)
+
+
 @pytest.mark.parametrize("kv_heads", [1, 3, 5, 12, 16])
 def test_kv_head_grouping(nplib, kv_heads):
     """kv_heads not a multiple of 8 and > 8 (several head groups per row)."""
