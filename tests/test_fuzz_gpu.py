@@ -23,7 +23,7 @@ def _draw(i: int):
     rnd = random.Random(1000 + i)
     dtype = rnd.choice(["bf16", "f32"])
     head_dim = rnd.choice([16, 32, 64, 128, 256])
-    group = rnd.choice([1, 2, 4, 5, 8])
+    group = rnd.choice([1, 2, 3, 4, 5, 6, 7, 8, 16] if dtype == "bf16" else [1, 2, 4, 5, 8])
     kv_heads = rnd.choice([1, 2, 3, 4, 8, 8, 12, 16])
     block_size = rnd.choice([1, 3, 8, 16, 24, 32, 64])
     rows = rnd.randint(1, 12)
