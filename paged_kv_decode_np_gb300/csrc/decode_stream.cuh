@@ -9,10 +9,13 @@
 // Partition (computed on the device from context_lens; no host sync, so the
 // step stays graph-capturable).  Virtual rows v = hgi*rows + r (row r, kv
 // head group hgi) are laid end to end, v's length being the row's context.
-// With W their total and P = gridDim.x (one CTA per SM), CTA b owns the
-// tokens from point(b*W/P) up to point((b+1)*W/P), where point(u) is the
-// (virtual row, token) holding stream position u, the token rounded down to a
-// whole chunk so that TMA boxes stay block-aligned.  A CTA walks its rows
+// With W their total and P = gridDim.x (one CTA per SM), the first Pe =
+// min(P, ceil(W / kMinCtaTokens)) CTAs share the stream -- a small step
+// gives each working CTA a few chunks instead of spreading a short row over
+// every SM -- and CTA b < Pe owns the tokens from point(b*W/Pe) up to
+// point((b+1)*W/Pe), where point(u) is the (virtual row, token) holding
+// stream position u, the token rounded down to a whole chunk so that TMA
+// boxes stay block-aligned; CTAs b >= Pe own nothing.  A CTA walks its rows
 // back to back with one producer/consumer pipeline: no drain between rows.
 //
 // Results.  A row that lies wholly inside one CTA is written straight to
@@ -208,8 +211,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   // ---- the partition: point(b) = (virtual row, chunk-aligned token) where
   // CTA b starts; CTA b owns [point(b), point(b+1))
   const int64_t total = pre[V];
+  constexpr int64_t kMinCtaTokens = 4 * C::CT;  // at least 4 chunks per working CTA
+  const int Pe = (int)min((int64_t)P, max((int64_t)1, (total + kMinCtaTokens - 1) / kMinCtaTokens));
   auto point = [&](int bb, int& pv, int64_t& pt) {
-    const int64_t u = (int64_t)bb * total / P;  // total < 2^43, bb <= 256: no overflow
+    const int64_t u = bb >= Pe ? total : (int64_t)bb * total / Pe;  // total < 2^43: no overflow
     int lo = 0, hi = V;  // the last v with pre[v] <= u
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -232,7 +237,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     range[3] = pt;
     // Merge descriptor.  CTA b owns the row its range ends inside, v, if v
     // began here ((vb, tb) <= (v, 0)).  The covering CTAs are b .. bl, bl
-    // the last whose stream position floor(bb*total/P) lies before the
+    // the last whose stream position floor(bb*total/Pe) lies before the
     // row's end pre[v+1]; CTAs after b hold v as their first row (slot 0),
     // b holds it in slot 0 if it is b's first row, else in slot 1.
     int4 d = make_int4(-1, 0, 0, 0);
@@ -240,7 +245,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       const int64_t x = pre[pv + 1];
       d.x = pv;
       d.y = (int)(x - pre[pv]);
-      d.z = (int)min((int64_t)P - 1, (x * P - 1) / total);
+      d.z = (int)min((int64_t)Pe - 1, (x * Pe - 1) / total);
       d.w = vb0 == pv ? 0 : 1;
     }
     reinterpret_cast<int4*>(p.st_desc)[b] = d;
