@@ -45,8 +45,9 @@
  *   - Pools: k_pool and v_pool are separate arrays, each
  *     [num_blocks, block_size, kv_heads, head_dim] of `dtype`.
  *   - Supported: dtype NP_F32 or NP_BF16; head_dim in {16, 32, 64, 128, 256};
- *     group g = q_heads/kv_heads in {1, 2, 4, 5, 8} on fp32 pools, any g from
- *     1 to 16 on bf16 pools; any block_size >= 1;
+ *     group g = q_heads/kv_heads in {1, 2, 4, 5, 8} on fp32 pools (any g up
+ *     to 8 through the balanced read, num_splits == 0), any g from 1 to 16
+ *     on bf16 pools; any block_size >= 1;
  *     any kv_heads >= 1; query_len 1, or any query_len with g * query_len
  *     <= 16 on bf16 pools, or <= 8 on fp32 pools through the balanced read
  *     (num_splits == 0).  Arithmetic is fp32 in every case (bf16 is widened

@@ -38,7 +38,8 @@ bool head_dim_supported(int32_t d) {
 
 // GQA group g = q_heads / kv_heads: any g up to 16 on bf16 pools (the
 // tensor-core warps take it at run time; g * query_len <= 16 is checked with
-// the query tokens), the compiled set on fp32 pools.
+// the query tokens), the compiled set on fp32 pools (other groups up to 8 run
+// on the balanced read only).
 bool group_supported(np_dtype dtype, int32_t g) {
   if (dtype == NP_BF16) return g >= 1 && g <= 16;
   return g == 1 || g == 2 || g == 4 || g == 5 || g == 8;
@@ -327,7 +328,10 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
       num_blocks <= 0 || block_size <= 0 || max_blocks_per_row <= 0 || num_splits < 0 ||
       num_splits > 65535 || !isfinite(scale))
     return NP_ERR_INVALID_ARG;
-  if (!head_dim_supported(head_dim) || !group_supported(dtype, q_heads / kv_heads))
+  if (!head_dim_supported(head_dim)) return NP_ERR_UNSUPPORTED;
+  // fp32 groups outside the compiled set (up to 8) run on the balanced read
+  if (!group_supported(dtype, q_heads / kv_heads) &&
+      !(dtype == NP_F32 && q_heads / kv_heads <= 8 && num_splits == 0))
     return NP_ERR_UNSUPPORTED;
   // several query tokens: (query token, head) rows of a group <= 16 on bf16
   // pools; <= 8 on fp32 pools, through the balanced read only

@@ -23,7 +23,8 @@
 // Rows: with one query token per row, the G heads (padded to a power of two);
 // with several (MQ), rows qi*G + h for query token qi and head h, up to 8,
 // each masked to the positions at or before its own (c - Q + qi), as in the
-// tensor-core warp.
+// tensor-core warp.  G = 0 (with MQ): the group is read at run time, for
+// groups outside the compiled set.
 // Stage layout (written by the producer's bulk copies): K rows [token][hg kv
 // heads][D] fp32, then V rows the same.
 #pragma once
@@ -48,6 +49,7 @@ struct FmaCfg {
   static_assert(D % 32 == 0 && D <= 256, "fp32 balanced read: head_dim 32..256");
   static_assert(DPL % 4 == 0 && 32 % LD == 0 && CT % LT == 0 && NT >= 1, "fp32 layout");
   static_assert(G <= 8, "fp32 balanced read: at most 8 query heads per kv head");
+  static_assert(G > 0 || MQ, "a group read at run time takes the 8-row layout");
 };
 
 template <int D, int G, bool MQ = false>
@@ -59,17 +61,19 @@ struct FmaWarp {
   float m, l;             // running max and sum of row (lane % GP)
   int32_t lim;            // last position row (lane % GP) may see (-1: a padding row);
                           // positions fit int32 on the balanced read
+  int gr;                 // query heads per kv head (G, or q_heads/kv_heads when G = 0)
 
   __device__ __forceinline__ void begin(const DecodeParams& p, int64_t r, int kvh, int64_t c,
                                         int lane) {
-    const int Q = p.query_len, MR = G * Q;
+    gr = G > 0 ? G : p.q_heads / p.kv_heads;
+    const int Q = p.query_len, MR = gr * Q;
     const int dl = lane % C::LD;
 #pragma unroll
     for (int row = 0; row < NR; ++row) {
-      const int qi = row / G, h = row - (row / G) * G;
+      const int qi = row / gr, h = row - (row / gr) * gr;
       if (row < MR) {
         const float* qr = static_cast<const float*>(p.q) +
-                          ((r * Q + qi) * p.q_heads + (int64_t)kvh * G + h) * D;
+                          ((r * Q + qi) * p.q_heads + (int64_t)kvh * gr + h) * D;
         Storage<float>::template load<C::DPL>(qr + dl * C::DPL, q[row]);
       }
 #pragma unroll
@@ -79,7 +83,7 @@ struct FmaWarp {
       }
     }
     const int rme = lane % C::GP;
-    lim = rme < MR ? (int32_t)(c - Q + rme / G) : -1;
+    lim = rme < MR ? (int32_t)(c - Q + rme / gr) : -1;
     m = -INFINITY;
     l = 0.f;
   }
@@ -217,7 +221,7 @@ struct FmaWarp {
   __device__ __forceinline__ void store_out(const DecodeParams& p, int64_t r, int kvh,
                                             int lane) const {
     constexpr unsigned FULL = 0xffffffffu;
-    const int Q = p.query_len, MR = G * Q;
+    const int Q = p.query_len, MR = gr * Q;
     const int dl = lane % C::LD;
 #pragma unroll
     for (int row = 0; row < NR; ++row) {
@@ -226,8 +230,8 @@ struct FmaWarp {
       float v[C::DPL];
 #pragma unroll
       for (int e = 0; e < C::DPL; ++e) v[e] = acc[row][e] * inv;
-      const int qi = row / G, h = row - (row / G) * G;
-      float* o = static_cast<float*>(p.out) + ((r * Q + qi) * p.q_heads + (int64_t)kvh * G + h) * D;
+      const int qi = row / gr, h = row - (row / gr) * gr;
+      float* o = static_cast<float*>(p.out) + ((r * Q + qi) * p.q_heads + (int64_t)kvh * gr + h) * D;
       if (lane < C::LD && row < MR) Storage<float>::template store<C::DPL>(o + dl * C::DPL, v);
     }
   }

@@ -169,7 +169,13 @@ np_status NPK_LAUNCHER(DecodeLaunch& L, DecodeParams& p) {
     case 4: return launch_one<4>(L, p);
     case 5: return launch_one<5>(L, p);
     case 8: return launch_one<8>(L, p);
-    default: return NP_ERR_UNSUPPORTED;
+    default:
+#ifdef NPK_HAS_STREAM
+      // other groups up to 8: the balanced read's 8-row FMA layout with the
+      // group read at run time (host-checked: balanced, g * query_len <= 8)
+      if (L.streamed && L.group <= 8) return launch_stream<0, true>(L, p);
+#endif
+      return NP_ERR_UNSUPPORTED;
   }
 #endif
 }

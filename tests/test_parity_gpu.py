@@ -264,6 +264,27 @@ def test_any_group_on_bf16(nplib, group, kv_heads, query_len):
     _full_parity(nplib, w, num_splits=3, fused=False)
 
 
+@pytest.mark.parametrize("group,kv_heads,query_len,head_dim", [
+    (3, 8, 1, 128), (6, 8, 1, 64), (7, 4, 1, 128), (3, 8, 2, 256), (6, 12, 1, 32)])
+def test_other_groups_on_fp32(nplib, group, kv_heads, query_len, head_dim):
+    """fp32 groups outside the compiled set (up to 8 rows) run on the
+    balanced read with the group read at run time; the split grid refuses
+    them."""
+    ctx = [1, 300, 2049, 64, 0, 900]
+    ctx = [max(c, query_len) if c else 0 for c in ctx]
+    w = _custom(ctx, kv_heads * group, kv_heads, head_dim, 16, "f32",
+                seed=400 + group * 7 + kv_heads + query_len, query_len=query_len)
+    _full_parity(nplib, w, num_splits=0)
+    _full_parity(nplib, w, num_splits=0, fused=False)
+    inp = wl.make_inputs(w)
+    d = [t.to(DEV) for t in (inp.q, inp.k_pool, inp.v_pool)]
+    bt, cl = inp.block_tables.to(DEV), inp.context_lens.to(DEV)
+    with pytest.raises(nplib.NPError) as e:
+        nplib.np_paged_decode(torch.empty_like(d[0]), d[0], d[1], d[2], bt, cl, 0.1,
+                              num_splits=1)
+    assert e.value.status == nplib.NP_ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("kv_heads", [1, 3, 5, 12, 16])
 def test_kv_head_grouping(nplib, kv_heads):
     """kv_heads not a multiple of 8 and > 8 (several head groups per row)."""
