@@ -529,15 +529,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 // (a fixed order: results are deterministic).  Every partial the merge
 // reads is finite (an empty one is m = -inf, l = 0, o = 0), so the weighted
 // sum runs without branches and its loads all issue before the first use.
-template <typename T, int D, int G>
+// RPW: mma rows per warp (2 when a row group has 16 rows, so that the merge
+// is one wave of warps): the loads of both rows go out in the same round.
+template <typename T, int D, int G, int RPW>
 __global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_kernel(
     const __grid_constant__ DecodeParams p) {
   constexpr unsigned FULL = 0xffffffffu;
   const int HG = p.head_group;  // kv heads per row group: 8 or 4
   constexpr int DL = D / 32;
-  constexpr int U = kMergeRpb >= 4 ? (DL >= 8 ? 4 : 8) : (DL >= 8 ? 8 : 16);
+  constexpr int U = RPW >= 2 ? (DL >= 8 ? 4 : 8) : (DL >= 8 ? 8 : 16);
   const int b = blockIdx.x;
-  const int row = blockIdx.y * kMergeRpb + (threadIdx.x >> 8);
+  const int row0 = (blockIdx.y * kMergeRpb + (threadIdx.x >> 8)) * RPW;
   const int hl = (threadIdx.x >> 5) & 7;
   const int lane = threadIdx.x & 31;
 #if NPK_STREAM_PDL
@@ -546,7 +548,8 @@ __global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_ker
   const int4 d = reinterpret_cast<const int4*>(p.st_desc)[b];
   const int Q = p.query_len;
   const int Gr = G > 0 ? G : p.q_heads / p.kv_heads;  // G = 0: the group set at run time
-  if (d.x < 0 || row >= Gr * Q || hl >= HG) return;
+  const int MR = Gr * Q;
+  if (d.x < 0 || row0 >= MR || hl >= HG) return;
   const int v = d.x, bl = d.z, slot_b = d.w;
   const int R = p.rows;
   const int r = v % R, hgi = v / R;
@@ -556,56 +559,84 @@ __global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_ker
     return p.ws_o + (((int64_t)j * 2 + (j == b ? slot_b : 0)) * HG + hl) * ent_floats;
   };
   const int d0 = lane * DL;
-
-  float mm = -INFINITY, lsum = 0.f, acc[DL];
+  int rows[RPW];  // this warp's mma rows (a row past MR repeats row0; not stored)
 #pragma unroll
-  for (int e2 = 0; e2 < DL; ++e2) acc[e2] = 0.f;
+  for (int k = 0; k < RPW; ++k) rows[k] = row0 + k < MR ? row0 + k : row0;
+
+  float mm[RPW], lsum[RPW], acc[RPW][DL];
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) {
+    mm[k] = -INFINITY;
+    lsum[k] = 0.f;
+#pragma unroll
+    for (int e2 = 0; e2 < DL; ++e2) acc[k][e2] = 0.f;
+  }
   for (int base = b; base <= bl; base += U) {
     const int nb = min(U, bl - base + 1);
-    float mj = -INFINITY, lj = 0.f;
+    float mj[RPW], lj[RPW];
+#pragma unroll
+    for (int k = 0; k < RPW; ++k) {
+      mj[k] = -INFINITY;
+      lj[k] = 0.f;
+    }
     if (lane < nb) {
       const float* e = entry(base + lane);
-      mj = e[row];
-      lj = e[kMmaRows + row];
-    }
-    float ok[U][DL];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {  // the batch's partials only (nb is known before any load)
-      if (u < nb) {
-        Storage<float>::template load<DL>(entry(base + u) + 2 * kMmaRows + row * D + d0, ok[u]);
-      } else {
-#pragma unroll
-        for (int e2 = 0; e2 < DL; ++e2) ok[u][e2] = 0.f;
+      for (int k = 0; k < RPW; ++k) {
+        mj[k] = e[rows[k]];
+        lj[k] = e[kMmaRows + rows[k]];
       }
     }
-    float bm = mj;
+    float ok[RPW][U][DL];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(FULL, bm, o));
-    const float mn = fmaxf(mm, bm);
-    const float msub = mn == -INFINITY ? 0.f : mn;
-    const float sc = ex2(mm - msub);  // mm = -inf: 0 (nothing merged yet)
-    const float aj = ex2(mj - msub);  // an empty partial (m = -inf): 0
-    float ls = aj * lj;
+    for (int u = 0; u < U; ++u) {  // the batch's partials only (nb is known before any load)
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(FULL, ls, o);
-    lsum = fmaf(lsum, sc, ls);
+      for (int k = 0; k < RPW; ++k) {
+        if (u < nb) {
+          Storage<float>::template load<DL>(
+              entry(base + u) + 2 * kMmaRows + rows[k] * D + d0, ok[k][u]);
+        } else {
 #pragma unroll
-    for (int e2 = 0; e2 < DL; ++e2) acc[e2] *= sc;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {  // in CTA order; lanes >= nb hold aj = 0
-      const float au = __shfl_sync(FULL, aj, u);
-#pragma unroll
-      for (int e2 = 0; e2 < DL; ++e2) acc[e2] = fmaf(ok[u][e2], au, acc[e2]);
+          for (int e2 = 0; e2 < DL; ++e2) ok[k][u][e2] = 0.f;
+        }
+      }
     }
-    mm = mn;
-  }
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-  float ov[DL];
 #pragma unroll
-  for (int e2 = 0; e2 < DL; ++e2) ov[e2] = acc[e2] * inv;
-  const int qi = row / Gr, h = row - qi * Gr;
-  T* o = static_cast<T*>(p.out) + (((int64_t)r * Q + qi) * p.q_heads + kvh * Gr + h) * D;
-  Storage<T>::template store<DL>(o + d0, ov);
+    for (int k = 0; k < RPW; ++k) {
+      float bm = mj[k];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(FULL, bm, o));
+      const float mn = fmaxf(mm[k], bm);
+      const float msub = mn == -INFINITY ? 0.f : mn;
+      const float sc = ex2(mm[k] - msub);  // mm = -inf: 0 (nothing merged yet)
+      const float aj = ex2(mj[k] - msub);  // an empty partial (m = -inf): 0
+      float ls = aj * lj[k];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(FULL, ls, o);
+      lsum[k] = fmaf(lsum[k], sc, ls);
+#pragma unroll
+      for (int e2 = 0; e2 < DL; ++e2) acc[k][e2] *= sc;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {  // in CTA order; lanes >= nb hold aj = 0
+        const float au = __shfl_sync(FULL, aj, u);
+#pragma unroll
+        for (int e2 = 0; e2 < DL; ++e2) acc[k][e2] = fmaf(ok[k][u][e2], au, acc[k][e2]);
+      }
+      mm[k] = mn;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) {
+    const int row = row0 + k;
+    if (row >= MR) break;
+    const float inv = lsum[k] > 0.f ? 1.f / lsum[k] : 0.f;
+    float ov[DL];
+#pragma unroll
+    for (int e2 = 0; e2 < DL; ++e2) ov[e2] = acc[k][e2] * inv;
+    const int qi = row / Gr, h = row - qi * Gr;
+    T* o = static_cast<T*>(p.out) + (((int64_t)r * Q + qi) * p.q_heads + kvh * Gr + h) * D;
+    Storage<T>::template store<DL>(o + d0, ov);
+  }
 }
 
 }  // namespace npk
