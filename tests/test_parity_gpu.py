@@ -662,6 +662,61 @@ def test_cuda_graph_capture_and_replay(nplib):
     assert_parity(out, ref, "bf16", "graph replay")
 
 
+def test_concurrent_streams_from_two_host_threads(nplib):
+    """Two decode steps in flight at once -- each on its own stream with its
+    own workspace, issued from its own host thread, 20 times over (the fused
+    append rewrites the same new token, so repeats are idempotent) -- both
+    match the oracle and leave the pools as the oracle's append does."""
+    import threading
+
+    cases = [_custom([700, 4096, 33, 0, 1200], 40, 8, 128, 32, "bf16", seed=600),
+             _custom([17, 900, 2500, 64], 32, 8, 128, 16, "f32", seed=601)]
+    runs = []
+    for w in cases:
+        inp = wl.make_inputs(w)
+        host = wl.full_host(inp)
+        dinp = wl.Inputs(w, inp.md, *(t.to(DEV) for t in
+                                      (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new)))
+        runs.append((w, inp, host, dinp))
+    outs, errs, failures = [None, None], [None, None], []
+
+    def worker(i):
+        try:  # no synchronisation inside: the two threads' steps overlap on the GPU
+            w, inp, host, dinp = runs[i]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                bt, cl, sm = (t.to(DEV) for t in (dinp.block_tables, dinp.context_lens,
+                                                  dinp.slot_mapping))
+                ws = nplib.workspace(w.rows, w.q_heads, w.head_dim, 0, device=DEV)
+                out = torch.full_like(dinp.q, float("nan"))
+                for _ in range(20):
+                    nplib.decode_step(out, dinp.q, dinp.k_pool, dinp.v_pool, bt, cl,
+                                      w.softmax_scale, k_new=dinp.k_new, v_new=dinp.v_new,
+                                      slot_mapping=sm, num_splits=0, workspace=ws,
+                                      err_word=errs[i], stream=s)
+                outs[i] = out
+        except Exception as e:  # reported on the main thread
+            failures.append(e)
+
+    for i in range(2):
+        errs[i] = torch.zeros(1, dtype=torch.int32, device=DEV)
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not failures, failures
+    for i, (w, inp, host, dinp) in enumerate(runs):
+        assert int(errs[i].item()) == 0
+        ref, _ = oracle_step(host, w.softmax_scale)
+        assert_parity(outs[i], ref, w.dtype, f"concurrent {w.name}")
+        rk, rv = host["k_pool"].copy(), host["v_pool"].copy()
+        oracle_append(rk, rv, host)
+        assert wl.host_array(dinp.k_pool).tobytes() == rk.tobytes()
+        assert wl.host_array(dinp.v_pool).tobytes() == rv.tobytes()
+
+
 def test_non_default_stream_and_determinism(nplib):
     w = _custom([900, 50, 2048], 32, 8, 128, 16, "bf16", seed=61)
     inp = wl.make_inputs(w)
