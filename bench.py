@@ -23,6 +23,8 @@ import argparse
 import hashlib
 import json
 import math
+
+import numpy as np
 import os
 import re
 import statistics
@@ -39,6 +41,7 @@ import torch  # noqa: E402
 import workloads as wl  # noqa: E402
 
 DEFAULT_WORKLOAD = "bf16-long"
+REF_TOTAL_S = 150.0  # oracle work of the whole --impl reference run, about
 METRIC = "paged decode read: KV GB/s and % of GB300 HBM peak; µs per decode step"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
@@ -211,12 +214,14 @@ def sum_over_ranks(dist, x: float) -> float:
 
 
 # ------------------------------------------------------------ CPU oracle ---
-def oracle_sample(inp: wl.Inputs, budget_s: float, seed: int = 0, threads: int = 1) -> dict:
+def oracle_sample(inp: wl.Inputs, budget_s: float, seed: int = 0, threads: int = 1,
+                  token_cap: int | None = None) -> dict:
     """Time the oracle (the C oracle as it stands) on randomly chosen rows of
     the step until ``budget_s`` seconds of wall time are done.  ``threads``
     rows run at once, each in its own host thread (the C calls release the
     interpreter lock); each batch's host copies are made before its clock
-    starts."""
+    starts.  ``token_cap`` reads at most that many history tokens of a row
+    (a prefix: the same work per token, for short samples)."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
 
@@ -239,6 +244,9 @@ def oracle_sample(inp: wl.Inputs, budget_s: float, seed: int = 0, threads: int =
             for r in batch:
                 h = wl.row_subproblem(inp, [r])
                 h["k_pool"], h["v_pool"] = h["k_pool"].copy(), h["v_pool"].copy()
+                if token_cap is not None:
+                    h["context_lens"] = np.minimum(h["context_lens"], token_cap).astype(
+                        h["context_lens"].dtype)
                 hosts.append(h)
             t0 = time.perf_counter()
             list(ex.map(one, hosts))
@@ -263,13 +271,21 @@ def run_reference(args, w: wl.Workload, dist, rank):
         return None
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = wl.make_inputs(w, device=dev, poison=False)
-    step_budget = args.ref_step_seconds
     nt = host_threads()
+    # the whole arm within a few minutes: about REF_TOTAL_S of oracle work in
+    # all; rows are cut to a prefix when one batch of whole rows would exceed
+    # a step's share (the per-token rate comes from a one-row calibration)
+    step_budget = min(args.ref_step_seconds, REF_TOTAL_S / max(1, args.steps + args.warmup))
+    cal = oracle_sample(inp, 0.0, seed=999, threads=1, token_cap=2048)
+    tok_s = (cal["kv_bytes"] / (2 * w.kv_heads * w.head_dim * w.elem_size)) / max(
+        cal["seconds"], 1e-6)
+    token_cap = max(w.block_size, int(tok_s * step_budget))
+    cap = token_cap if token_cap < int(inp.md.context_lens.max()) else None
     for i in range(args.warmup):
-        oracle_sample(inp, step_budget, seed=1000 + i, threads=nt)
+        oracle_sample(inp, step_budget, seed=1000 + i, threads=nt, token_cap=cap)
     times, kvb, rows = [], 0, []
     for i in range(args.steps):
-        s = oracle_sample(inp, step_budget, seed=i, threads=nt)
+        s = oracle_sample(inp, step_budget, seed=i, threads=nt, token_cap=cap)
         times.append(s["seconds"])
         kvb += s["kv_bytes"]
         rows.append(len(s["rows"]))
@@ -284,8 +300,10 @@ def run_reference(args, w: wl.Workload, dist, rank):
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": nt, "kind": "oracle",
                          "sample": f"each step: the C oracle (fp64) on randomly chosen rows "
                                    f"of the {w.name} step, {nt} rows at a time in {nt} host "
-                                   f"threads, until {step_budget:g} s of wall time "
-                                   f"({statistics.mean(rows):.1f} rows per step on average)"},
+                                   f"threads, until {step_budget:.3g} s of wall time "
+                                   f"({statistics.mean(rows):.1f} rows per step on average"
+                                   + (f", each row's first {cap} history tokens)" if cap
+                                      else ")")},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     return line
