@@ -306,30 +306,36 @@ def host_array(t: torch.Tensor) -> np.ndarray:
     return t.numpy().copy()
 
 
-def row_subproblem(inp: Inputs, rows: list[int]) -> dict:
+def row_subproblem(inp: Inputs, rows: list[int], max_tokens: int | None = None) -> dict:
     """Host copies of the blocks a few rows need, with tables renumbered.
 
     For a full-size pool the oracle cannot take the whole pool; it takes the
     listed rows' blocks (gathered by torch indexing, block order kept) and a
     table that points at them in order.  Paging only moves where K/V live, so
     this is the same read.  Call it BEFORE any kernel touches the pool.
+    ``max_tokens`` keeps each row's first max_tokens history tokens only (a
+    prefix of the read, for timing samples); a new token past the prefix is
+    then not appended (its slot is -1).
     """
     w, md = inp.w, inp.md
     bs = w.block_size
     ids, tables, offs = [], [], 0
     cl = md.context_lens[rows]
+    if max_tokens is not None:
+        cl = torch.clamp(cl, max=max_tokens)
     mb = max(1, max((-(-int(c) // bs)) for c in cl.tolist()))
     bt = torch.full((len(rows), mb), -1, dtype=torch.int32)
     qn = w.query_len
     slots = torch.full((len(rows), qn), -1, dtype=torch.int64)
     for i, r in enumerate(rows):
-        c = int(md.context_lens[r])
+        c = int(cl[i])
         n = -(-c // bs)
         ids.append(md.block_tables[r, :n].to(torch.int64))
         bt[i, :n] = torch.arange(offs, offs + n, dtype=torch.int32)
+        full = int(md.context_lens[r])
         for j in range(qn):
-            t = c - qn + j
-            if t >= 0:
+            t = full - qn + j
+            if 0 <= t < c:
                 slots[i, j] = (offs + t // bs) * bs + t % bs
         offs += n
     if qn == 1:
