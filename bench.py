@@ -68,6 +68,22 @@ def algorithmic_bytes(w: wl.Workload, md: wl.Metadata) -> dict:
     return {"kv": kv, "decode": kv + qo + tab + app, "append": app}
 
 
+def l2_plan(kv_bytes_per_step: int, pool_bytes: int) -> int:
+    """How the timed steps keep K/V out of L2: the number of pool copies the
+    steps rotate among, or 0 for an L2 flush between steps.
+
+    K/V of at least 4x L2 per step needs nothing (1 copy).  A smaller pool of
+    at least L2/16 is rotated: copies of it, more than 3x L2 in all, are read
+    in turn, so no step finds its K/V in L2 and steps still run back to back.
+    A tinier pool gets a 2x L2 buffer written between timed steps (outside
+    the timed region).
+    """
+    if kv_bytes_per_step >= 4 * L2_BYTES:
+        return 1
+    n = math.ceil(3 * L2_BYTES / pool_bytes) + 1
+    return n if n <= 48 else 0
+
+
 def measured_peak() -> tuple[float, str]:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -102,28 +118,86 @@ def profiled_traffic(workload: str) -> float | None:
 
 
 # ---------------------------------------------------------------- clocks ---
+class _Nvml:
+    """Read-only NVML queries through ctypes (the library ships with the
+    driver): SM clock, its maximum and the active clock-event reasons."""
+    SM = 1  # NVML_CLOCK_SM
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, pci_bus_id: str):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(),
+                                                     ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle for " + pci_bus_id)
+        try:
+            self.reasons_fn = self.lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self.reasons_fn = self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        c = self.c
+        sm, mx, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        if (self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, c.byref(sm)) != 0 or
+                self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM, c.byref(mx)) != 0):
+            return None
+        if self.reasons_fn(self.h, c.byref(rs)) != 0:
+            return None
+        return (float(sm.value), float(mx.value),
+                [n for b, n in self.REASONS.items() if rs.value & b])
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
+    """SM clocks and clock-event reasons sampled while the timed steps run:
+    NVML polled every 2 ms where it loads (a timed region of a few ms still
+    gets samples), else ``nvidia-smi -lms 200``."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, device: torch.device):
         self.gpu = None
-        try:  # nvidia-smi wants the PCI bus id of the device torch is using
+        try:  # NVML and nvidia-smi want the PCI bus id of the device torch is using
             pr = torch.cuda.get_device_properties(device)
             self.gpu = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
         except Exception:
             pass
         self.proc = None
-        self.lines: list[tuple[float, str]] = []
+        self.nvml = None
+        self.stop = threading.Event()
+        self.t = None
+        self.samples: list[tuple[float, float, float, list]] = []  # (time, sm, max, reasons)
         self.window = None
+        self.source = None
 
     def __enter__(self):
+        if self.gpu is not None:
+            try:
+                self.nvml = _Nvml(self.gpu)
+                if self.nvml.sample() is None:
+                    raise OSError("NVML query failed")
+                self.source = "nvml, 2 ms"
+                self.t = threading.Thread(target=self._poll, daemon=True)
+                self.t.start()
+                time.sleep(0.05)
+                return self
+            except (OSError, AttributeError):
+                self.nvml = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", *([f"--id={self.gpu}"] if self.gpu else []),
                  f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi, 200 ms"
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
             time.sleep(0.3)
@@ -131,16 +205,36 @@ class ClockSampler:
             self.proc = None
         return self
 
+    def _poll(self):
+        while not self.stop.is_set():
+            x = self.nvml.sample()
+            if x is not None:
+                self.samples.append((time.time(), *x))
+            self.stop.wait(0.002)
+
     def _read(self):
         for ln in self.proc.stdout:
-            self.lines.append((time.time(), ln.strip()))
+            parts = [p.strip() for p in ln.strip().split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            rs = [n for n, v in zip(self.NAMES, parts[5:9]) if v.lower().startswith("active")]
+            self.samples.append((time.time(), sm, mx, rs))
 
     def mark(self, start: float, end: float) -> None:
         """The host wall-clock window of the timed region."""
         self.window = (start, end)
 
     def __exit__(self, *exc):
-        if self.proc is not None:
+        if self.nvml is not None:
+            time.sleep(0.01)
+            self.stop.set()
+            self.t.join(timeout=5)
+            self.nvml.close()
+        elif self.proc is not None:
             time.sleep(0.25)
             self.proc.terminate()
             try:
@@ -150,29 +244,18 @@ class ClockSampler:
             self.t.join(timeout=5)
 
     def summary(self) -> dict:
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        lines = self.lines
+        samples = self.samples
+        inside = []
         if self.window is not None:  # samples taken while the timed steps ran
-            inside = [x for x in lines if self.window[0] <= x[0] <= self.window[1] + 0.05]
-            lines = inside or lines
-        for _, ln in lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+            inside = [x for x in samples
+                      if self.window[0] <= x[0] <= self.window[1] + 0.005]
+        use = inside or samples
+        if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm),
-                "in_timed_region": self.window is not None and lines is not self.lines}
+        reasons = sorted({r for x in use for r in x[3]})
+        return {"sm_mhz": statistics.median(x[1] for x in use),
+                "sm_max_mhz": max(x[2] for x in use), "reasons": reasons,
+                "samples": len(use), "in_timed_region": bool(inside), "source": self.source}
 
 
 # ------------------------------------------------------------ distributed --
@@ -329,27 +412,24 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     nbytes = algorithmic_bytes(w, md)
-    # inputs larger than L2 need no flush; otherwise write a 2xL2 buffer
-    # between timed steps, outside the timed kernels
+    pools = [(inp.k_pool, inp.v_pool)]
     flush = None
-    if nbytes["kv"] < 4 * L2_BYTES:
+    pool_bytes = 2 * inp.k_pool.numel() * inp.k_pool.element_size()
+    n_pools = l2_plan(nbytes["kv"], pool_bytes)
+    if n_pools == 0:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    else:
+        pools += [(inp.k_pool.clone(), inp.v_pool.clone()) for _ in range(n_pools - 1)]
 
-    def step(rec=None):
-        # append fused into the read's launch, then the split merge
-        launches = 0
-        if rec is not None:
-            rec[0].record(stream)
+    def step(i=0, s=stream):
+        # append fused into the read's launch, then the merge (balanced read)
+        # or the split reduce; returns the kernels launched
+        kp, vp = pools[i % len(pools)]
         npg.np_paged_append_decode(out if S <= 1 else None, inp.q, inp.k_new, inp.v_new, sm,
-                                   inp.k_pool, inp.v_pool, bt, cl, w.softmax_scale, S, ws, err,
-                                   stream)
-        if rec is not None:
-            rec[1].record(stream)
-        launches += 2 if S == 0 else 1  # the balanced read adds its merge launch
+                                   kp, vp, bt, cl, w.softmax_scale, S, ws, err, s)
         if S > 1:
-            npg.np_paged_decode_reduce(out, ws, S, stream)
-            launches += 1
-        return launches
+            npg.np_paged_decode_reduce(out, ws, S, s)
+        return 2 if S == 0 or S > 1 else 1
 
     # CPU baseline first (host copies of the sampled rows before any kernel)
     cpu = cpu1 = None
@@ -357,16 +437,35 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
         cpu = oracle_sample(inp, args.cpu_seconds, threads=host_threads())
         cpu1 = oracle_sample(inp, args.cpu_seconds / 4, seed=1)
 
-    for _ in range(args.warmup):
-        step()
+    for i in range(max(args.warmup, len(pools))):  # every pool copy touched once
+        step(i)
         if flush is not None:
             flush.zero_()
     torch.cuda.synchronize()
+    direct_out = out.clone()  # pool copy 0's step, launched directly
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    # The K timed steps are captured once, back to back, as one CUDA graph
+    # (step i on pool copy i mod the copies) and replayed: the same append,
+    # read and merge launches with the same arguments as direct calls, without
+    # the host's per-call cost between them (a 30 us step is shorter than one
+    # Python call plus its event records), as a decode graph over a model's
+    # layers would run them.  With an L2 flush between steps, one step is
+    # captured and replayed per step.
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    n_cap = args.steps if flush is None else 1
+    with torch.cuda.graph(graph, stream=cap):
+        for i in range(n_cap):
+            step_launches = step(i, cap)
+    torch.cuda.synchronize()
+    graph.replay()  # warm-up: the first launch uploads the graph
+    torch.cuda.synchronize()
+    if not torch.equal(out, direct_out):
+        raise RuntimeError("graph replay of the steps differs from the direct call")
+
     st_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(args.steps)]
+             for _ in range(args.steps if flush is not None else 0)]
     launches = 0
     with ClockSampler(dev) as clk:
         barrier(dist)
@@ -375,12 +474,16 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
-        for i in range(args.steps):
-            if flush is not None:
+        if flush is None:
+            graph.replay()
+            launches = step_launches * args.steps
+        else:
+            for i in range(args.steps):
                 flush.zero_()
-            st_ev[i][0].record(stream)
-            launches += step(ev[i])
-            st_ev[i][1].record(stream)
+                st_ev[i][0].record(stream)
+                graph.replay()
+                st_ev[i][1].record(stream)
+                launches += step_launches
         t_end.record(stream)
         torch.cuda.synchronize()
         clk.mark(wall0, time.time())
@@ -389,8 +492,9 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
         elapsed_ms = t_start.elapsed_time(t_end)
     else:  # exclude the L2 flushes between steps
         elapsed_ms = sum(a.elapsed_time(b) for a, b in st_ev)
-    decode_ms = [a.elapsed_time(b) for a, b in ev]
-    step_us = sorted(1e3 * a.elapsed_time(b) for a, b in st_ev)
+    # a step is the library's launches and nothing else
+    decode_ms = ([a.elapsed_time(b) for a, b in st_ev] if flush is not None
+                 else [elapsed_ms / args.steps])
     if int(err.item()) != 0:
         raise RuntimeError(f"device error flags {int(err.item()):#x}")
 
@@ -417,17 +521,18 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
     h2d = sum(t.numel() * t.element_size() for t in srcs.values())
     d2h = out_host.numel() * out_host.element_size()
 
-    def e2e_step():
+    def e2e_step(i=0):
+        kp, vp = pools[i % len(pools)]
         stage_d.copy_(stage_h, non_blocking=True)
         npg.np_paged_append_decode(out if S <= 1 else None, dbuf["q"], dbuf["k_new"],
-                                   dbuf["v_new"], dbuf["sm"], inp.k_pool, inp.v_pool,
+                                   dbuf["v_new"], dbuf["sm"], kp, vp,
                                    dbuf["bt"], dbuf["cl"], w.softmax_scale, S, ws, err, stream)
         if S > 1:
             npg.np_paged_decode_reduce(out, ws, S, stream)
         out_host.copy_(out, non_blocking=True)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    for i in range(max(args.warmup, len(pools))):
+        e2e_step(i)
     torch.cuda.synchronize()
     e_st = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(args.steps)]
@@ -437,7 +542,7 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
         if flush is not None:
             flush.zero_()
         e_st[i][0].record(stream)
-        e2e_step()
+        e2e_step(i)
         e_st[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(dist)
@@ -460,8 +565,6 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
         "ms_per_step": elapsed_ms / args.steps, "us_per_step": 1e3 * elapsed_ms / args.steps,
         "frac_of_hbm_peak": value / world / peak,
         "frac_of_nominal_8tbs": value / world / 8000.0,
-        "step_us": {"median": statistics.median(step_us),
-                    "p10": step_us[len(step_us) // 10], "p90": step_us[(9 * len(step_us)) // 10]},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1) q/K/V, shuffled free-list block tables)",
         "config": {
@@ -476,16 +579,25 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
             else None,
             "mean_context": float(md.context_lens.double().mean()),
             "kv_bytes_per_step": nbytes["kv"],
-            "l2": ("inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2"
-                   % (nbytes["kv"] / 1e9)) if flush is None else
-                  "L2 flushed (2x L2 buffer written) between timed steps, flush excluded",
+            "l2": ("L2 flushed (2x L2 buffer written) between timed steps, flush excluded"
+                   if flush is not None else
+                   "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2"
+                   % (nbytes["kv"] / 1e9) if len(pools) == 1 else
+                   "steps rotate among %d copies of the %.1f MB K/V pool (%.2f GB in all, "
+                   "over 3x the 129 MB L2), back to back, no flush"
+                   % (len(pools), pool_bytes / 1e6, len(pools) * pool_bytes / 1e9)),
             "parallelism": f"replicas x{world} (rows independent, no collective)",
+            "launch": ("the K steps captured back to back as one CUDA graph and replayed"
+                       if flush is None else "one step captured as a CUDA graph, replayed "
+                       "once per step between L2 flushes")
+                      + "; output checked equal to a direct call's",
         },
         "roofline": {
             "bound": "hbm",
             "kernel": ("paged_decode_stream_kernel + its merge launch (timed together)"
-                       if S == 0 else "paged_decode_mma_kernel" if w.dtype == "bf16"
-                       else "paged_decode_kernel"),
+                       if S == 0 else ("paged_decode_mma_kernel" if w.dtype == "bf16"
+                                       else "paged_decode_kernel")
+                       + (" + lse_reduce_kernel (timed together)" if S > 1 else "")),
             "achieved": achieved,
             "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
             if peak_kind == "measured" else "fallback 6.8 TB/s",

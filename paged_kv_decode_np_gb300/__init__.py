@@ -137,7 +137,7 @@ def _dtype_code(dt) -> int:
 def _dev(t: torch.Tensor, name: str) -> int:
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.device.type != "cuda":
+    if not t.is_cuda:
         raise ValueError(f"{name} must be on a CUDA device (no CPU path exists)")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")

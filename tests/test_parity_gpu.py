@@ -727,3 +727,50 @@ def test_non_default_stream_and_determinism(nplib):
         a, _, _ = gpu_step(nplib, d, stream=s)
     b, _, _ = gpu_step(nplib, d)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("dtype,splits", [("bf16", 0), ("f32", 0), ("bf16", 4), ("f32", 1)])
+def test_cuda_graph_capture_and_replay(nplib, dtype, splits):
+    """A decode step captured in a CUDA graph and replayed: the replay equals
+    the direct call bit for bit and matches the oracle; after q is rewritten
+    in place, a replay reads the new q (the graph re-runs the kernels on the
+    captured buffers rather than repeating a result)."""
+    w = _custom([700, 4096, 33, 0, 1200, 5000], 32, 8, 128, 16, dtype, seed=610 + splits)
+    inp = wl.make_inputs(w)
+    host = wl.full_host(inp)
+    d = wl.Inputs(w, inp.md, *(t.to(DEV) for t in
+                               (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new)))
+    bt, cl, sm = (t.to(DEV) for t in (d.block_tables, d.context_lens, d.slot_mapping))
+    ws = nplib.workspace(w.rows, w.q_heads, w.head_dim, splits, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = torch.full_like(d.q, float("nan"))
+
+    def step(s):
+        nplib.decode_step(out, d.q, d.k_pool, d.v_pool, bt, cl, w.softmax_scale,
+                          k_new=d.k_new, v_new=d.v_new, slot_mapping=sm, num_splits=splits,
+                          workspace=ws, err_word=err, stream=s)
+
+    step(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    direct = out.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step(s)
+    out.fill_(float("nan"))
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(out, direct)
+    ref, _ = oracle_step(host, w.softmax_scale)
+    assert_parity(out, ref, w.dtype, f"graph replay {w.name}")
+
+    q2 = torch.randn(d.q.shape, generator=torch.Generator().manual_seed(77)).to(d.q.dtype)
+    d.q.copy_(q2.to(DEV))
+    g.replay()
+    torch.cuda.synchronize()
+    host2 = dict(host, q=wl.host_array(d.q))
+    ref2, _ = oracle_step(host2, w.softmax_scale)
+    assert_parity(out, ref2, w.dtype, f"graph replay with a new q {w.name}")
