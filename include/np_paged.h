@@ -185,8 +185,10 @@ size_t np_paged_decode_workspace_bytes(int32_t rows, int32_t q_heads,
  *                  160), each taking an equal, chunk-aligned share of all
  *                  rows' history laid end to end (computed on the device
  *                  from context_lens); rows cut between blocks are merged
- *                  by a second launch on `stream`, in block order (results
- *                  are deterministic).  out is written; no reduce call.
+ *                  by a second launch on `stream`, each cut row's merge
+ *                  spread over the blocks that read it, in block order
+ *                  (results are deterministic).  out is written; no reduce
+ *                  call.
  *                  Needs head_dim a multiple of 64 (bf16) or 32 (fp32, up
  *                  to 256), kv_heads a multiple of 4 (taken 8 at a time when
  *                  a multiple of 8, else 4; bf16 with groups of 4 also needs

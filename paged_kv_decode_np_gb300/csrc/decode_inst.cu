@@ -78,9 +78,6 @@ np_status launch_variant(DecodeLaunch& L, DecodeParams& p) {
   return cudaGetLastError() == cudaSuccess ? NP_OK : NP_ERR_CUDA;
 }
 
-#ifndef NPK_MERGE_RPW2
-#define NPK_MERGE_RPW2 1  // two mma rows per merge warp for 16-row groups
-#endif
 #if (NPK_BF16 && NPK_D % 64 == 0) || (!NPK_BF16 && NPK_D % 32 == 0)
 #define NPK_HAS_STREAM 1
 // The balanced streamed read: grid = L.splits CTAs (one per SM), 8 kv heads
@@ -112,9 +109,7 @@ np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
   kern<<<L.splits, 32 * (8 + 1), smem, L.stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return NP_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  const int mr = L.group * p.query_len;
-  const int rpw = mr >= 16 && NPK_MERGE_RPW2 ? 2 : 1;  // rows per merge warp
-  cfg.gridDim = dim3(L.splits, (mr + kMergeRpb * rpw - 1) / (kMergeRpb * rpw));
+  cfg.gridDim = dim3(L.splits, 1);  // one block per CTA of the read
   cfg.blockDim = dim3(256 * kMergeRpb);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = L.stream;
@@ -123,7 +118,8 @@ np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
   attr[0].val.programmaticStreamSerializationAllowed = NPK_STREAM_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if ((rpw == 2 ? cudaLaunchKernelEx(&cfg, paged_decode_stream_merge_kernel<StorageT, NPK_D, G, 2>, p)
+  const int mr = L.group * p.query_len;
+  if ((mr >= 16 ? cudaLaunchKernelEx(&cfg, paged_decode_stream_merge_kernel<StorageT, NPK_D, G, 2>, p)
                 : cudaLaunchKernelEx(&cfg, paged_decode_stream_merge_kernel<StorageT, NPK_D, G, 1>,
                                      p)) != cudaSuccess)
     return NP_ERR_CUDA;

@@ -46,8 +46,8 @@ constexpr int kStreamMaxCtas = 160;    // grid cap, >= the GB300's 152 SMs (the
 #define NPK_STREAM_PDL 1
 #endif
 
-// mma rows per merge block (8 warps, one per kv head, for each): fewer,
-// larger blocks launch faster when a row group has many rows.
+// Merge blocks have 256 * NPK_MERGE_RPB threads (16 warps by default),
+// which share the block's merge tasks.
 #ifndef NPK_MERGE_RPB
 #define NPK_MERGE_RPB 2
 #endif
@@ -66,8 +66,8 @@ struct StreamWs {
   __host__ __device__ static constexpr size_t parts_bytes(int d) {
     return (size_t)kStreamMaxCtas * 2 * 8 * entry_floats(d) * sizeof(float);
   }
-  __host__ __device__ static constexpr size_t bytes(int d) {
-    return parts_bytes(d) + (size_t)kStreamMaxCtas * 4 * sizeof(int32_t);
+  __host__ __device__ static constexpr size_t bytes(int d) {  // + two int4 descriptors per CTA
+    return parts_bytes(d) + (size_t)kStreamMaxCtas * 8 * sizeof(int32_t);
   }
 };
 
@@ -235,20 +235,36 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     point(b + 1, pv, pt);
     range[2] = pv;
     range[3] = pt;
-    // Merge descriptor.  CTA b owns the row its range ends inside, v, if v
-    // began here ((vb, tb) <= (v, 0)).  The covering CTAs are b .. bl, bl
-    // the last whose stream position floor(bb*total/Pe) lies before the
-    // row's end pre[v+1]; CTAs after b hold v as their first row (slot 0),
-    // b holds it in slot 0 if it is b's first row, else in slot 1.
-    int4 d = make_int4(-1, 0, 0, 0);
+    // Merge descriptors {v, b0, bl, slot}: a cut row v, its covering CTAs
+    // b0 .. bl, and the slot of b0's partial.  The covering CTAs of v are
+    // b0, the CTA whose range holds (v, 0), through bl, the last whose
+    // stream position floor(bb*total/Pe) lies before the row's end
+    // pre[v+1]; CTAs after b0 hold v as their first row (slot 0), b0 holds
+    // it in slot 0 if it is b0's first row, else in slot 1.  Descriptor 0:
+    // the row this CTA's range ends inside, if it began here ((vb, tb) <=
+    // (v, 0)).  Descriptor 1: the row this range starts inside (tb > 0),
+    // begun by an earlier CTA b0 = ceil(X*Pe/total) - 1 with X =
+    // min(pre[v+1], pre[v] + CT) -- the first CTA whose end point lies past
+    // (v, 0) -- and b0's slot 0 exactly when floor(b0*total/Pe) >= pre[v].
+    int4 d = make_int4(-1, 0, 0, 0), e = make_int4(-1, 0, 0, 0);
     if (pt > 0 && pv < V && (vb0 < pv || tb0 == 0)) {
       const int64_t x = pre[pv + 1];
       d.x = pv;
-      d.y = (int)(x - pre[pv]);
+      d.y = b;
       d.z = (int)min((int64_t)Pe - 1, (x * Pe - 1) / total);
       d.w = vb0 == pv ? 0 : 1;
     }
-    reinterpret_cast<int4*>(p.st_desc)[b] = d;
+    if (tb0 > 0 && vb0 < V) {
+      const int64_t x0 = pre[vb0], x1 = pre[vb0 + 1];
+      const int64_t X = min(x1, x0 + (int64_t)C::CT);
+      const int b0 = (int)((X * Pe + total - 1) / total) - 1;
+      e.x = vb0;
+      e.y = b0;
+      e.z = (int)min((int64_t)Pe - 1, (x1 * Pe - 1) / total);
+      e.w = (int64_t)b0 * total / Pe >= x0 ? 0 : 1;
+    }
+    reinterpret_cast<int4*>(p.st_desc)[2 * b] = d;
+    reinterpret_cast<int4*>(p.st_desc)[2 * b + 1] = e;
   }
   __syncthreads();
   const int vb = (int)range[0], ve = (int)range[2];
@@ -519,44 +535,31 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   }
 }
 
-// Merge of the cut rows.  Grid (the read's CTAs, G*Q mma rows); CTA b of
-// the read is blockIdx.x here, and 8 warps = 8 kv heads.  The read left
-// CTA b's descriptor {v, c, bl, slot}: the row v it owns, cut between CTAs
-// b .. bl.  Warp hl merges mma row blockIdx.y of its kv head over batches
-// of U covering CTAs in ascending order; each batch is one round of loads
-// (lane j: partial j's m and l; every lane: its head_dim slice of all U
-// partial rows), then a rescale of the running state to the batch's max
-// (a fixed order: results are deterministic).  Every partial the merge
-// reads is finite (an empty one is m = -inf, l = 0, o = 0), so the weighted
-// sum runs without branches and its loads all issue before the first use.
-// RPW: mma rows per warp (2 when a row group has 16 rows, so that the merge
-// is one wave of warps): the loads of both rows go out in the same round.
+// One merge task: mma rows row0 .. row0+RPW-1 of kv head hl of the cut
+// row v, over the partials of its covering CTAs b0 .. bl in ascending order,
+// in batches of U; each batch is one round of loads (lane j: partial j's m
+// and l; every lane: its head_dim slice of all U partial rows of its RPW
+// mma rows), then a rescale of the running state to the batch's max (a
+// fixed order: results are deterministic).  Every partial the merge reads
+// is finite (an empty one is m = -inf, l = 0, o = 0), so the weighted sum
+// runs without branches and its loads all issue before the first use.
+// RPW = 2 when a row group has 16 mma rows (fewer tasks per row).
 template <typename T, int D, int G, int RPW>
-__global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_kernel(
-    const __grid_constant__ DecodeParams p) {
+__device__ __forceinline__ void merge_task(const DecodeParams& p, int v, int b0, int bl,
+                                           int slot_b0, int row0, int hl, int lane) {
   constexpr unsigned FULL = 0xffffffffu;
-  const int HG = p.head_group;  // kv heads per row group: 8 or 4
+  const int HG = p.head_group;
   constexpr int DL = D / 32;
   constexpr int U = RPW >= 2 ? (DL >= 8 ? 4 : 8) : (DL >= 8 ? 8 : 16);
-  const int b = blockIdx.x;
-  const int row0 = (blockIdx.y * kMergeRpb + (threadIdx.x >> 8)) * RPW;
-  const int hl = (threadIdx.x >> 5) & 7;
-  const int lane = threadIdx.x & 31;
-#if NPK_STREAM_PDL
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // the read is complete
-#endif
-  const int4 d = reinterpret_cast<const int4*>(p.st_desc)[b];
   const int Q = p.query_len;
   const int Gr = G > 0 ? G : p.q_heads / p.kv_heads;  // G = 0: the group set at run time
   const int MR = Gr * Q;
-  if (d.x < 0 || row0 >= MR || hl >= HG) return;
-  const int v = d.x, bl = d.z, slot_b = d.w;
   const int R = p.rows;
   const int r = v % R, hgi = v / R;
   const int kvh = hgi * HG + hl;
   const int64_t ent_floats = (int64_t)StreamWs::entry_floats(D);
   auto entry = [&](int j) -> const float* {  // CTA j's partial of row v, kv head hl
-    return p.ws_o + (((int64_t)j * 2 + (j == b ? slot_b : 0)) * HG + hl) * ent_floats;
+    return p.ws_o + (((int64_t)j * 2 + (j == b0 ? slot_b0 : 0)) * HG + hl) * ent_floats;
   };
   const int d0 = lane * DL;
   int rows[RPW];  // this warp's mma rows (a row past MR repeats row0; not stored)
@@ -571,7 +574,7 @@ __global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_ker
 #pragma unroll
     for (int e2 = 0; e2 < DL; ++e2) acc[k][e2] = 0.f;
   }
-  for (int base = b; base <= bl; base += U) {
+  for (int base = b0; base <= bl; base += U) {
     const int nb = min(U, bl - base + 1);
     float mj[RPW], lj[RPW];
 #pragma unroll
@@ -636,6 +639,46 @@ __global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_ker
     const int qi = row / Gr, h = row - qi * Gr;
     T* o = static_cast<T*>(p.out) + (((int64_t)r * Q + qi) * p.q_heads + kvh * Gr + h) * D;
     Storage<T>::template store<DL>(o + d0, ov);
+  }
+}
+
+// Merge of the cut rows.  One block per CTA of the read (one wave: every
+// block's work runs at once).  A cut row cut n ways (covering CTAs b0 ..
+// bl, n = bl - b0 + 1) is merged in tasks of RPW mma rows of one kv head,
+// numbered t = group * head_group + head and dealt out over the covering
+// CTAs: the block of CTA b0 + (t mod n) runs task t, so the row is merged
+// on n SMs rather than on its first CTA's.  The read left CTA c's two
+// descriptors: the row it began and cut (c = b0) and the row it continued
+// (c > b0); the block's warps take its tasks of both in turn.
+template <typename T, int D, int G, int RPW>
+__global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_kernel(
+    const __grid_constant__ DecodeParams p) {
+  const int HG = p.head_group;  // kv heads per row group: 8 or 4
+  const int c = blockIdx.x;
+  const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
+#if NPK_STREAM_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the read is complete
+#endif
+  const int4* desc = reinterpret_cast<const int4*>(p.st_desc) + 2 * c;
+  const int4 d = desc[0], e = desc[1];
+  const int Gr = G > 0 ? G : p.q_heads / p.kv_heads;
+  const int NT = (Gr * p.query_len + RPW - 1) / RPW * HG;  // tasks per cut row
+  int kd = 0, nd = 1, ke = 0, ne = 1, oe = 0;
+  if (d.x >= 0) {  // tasks 0, n, 2n, ... of the row begun here
+    nd = max(1, d.z - d.y + 1);
+    kd = (NT + nd - 1) / nd;
+  }
+  if (e.x >= 0) {  // tasks o, o + n, ... of the row continued here (o = c - b0)
+    ne = max(1, e.z - e.y + 1);
+    oe = c - e.y;
+    ke = oe >= 0 && oe < NT ? (NT - oe + ne - 1) / ne : 0;
+  }
+  for (int k = w; k < kd + ke; k += nw) {
+    const bool own = k < kd;
+    const int t = own ? k * nd : oe + (k - kd) * ne;
+    const int4 x = own ? d : e;
+    merge_task<T, D, G, RPW>(p, x.x, x.y, x.z, x.w, (t / HG) * RPW, t % HG, lane);
   }
 }
 
