@@ -102,22 +102,35 @@ __device__ __forceinline__ void fused_append(const DecodeParams& p, int r, int h
     const int64_t pos = c - Q + j;
     if (pos < 0 || pos < t0 || pos >= t1) continue;
     const int64_t rq = (int64_t)r * Q + j;
-    const int64_t s = p.slot_mapping[rq];
-    if (s < 0) continue;
+    const int64_t nvec = (int64_t)HG * D * ES / 16;  // 16-byte vectors of the slice
+    const int64_t src0 = (rq * p.kv_heads + (int64_t)hgi * HG) * D * ES / 16;
+    const uint4* kn = static_cast<const uint4*>(p.k_new);
+    const uint4* vn = static_cast<const uint4*>(p.v_new);
+    // the slot, its table entry and this thread's first vectors are loaded
+    // together (one round trip, not three in a chain): at the kernel's start
+    // the read's own copies load the memory system
+    const bool first = tid < nvec;
+    uint4 k0 = make_uint4(0, 0, 0, 0), v0 = k0;
+    if (first) {
+      k0 = kn[src0 + tid];
+      v0 = vn[src0 + tid];
+    }
     const int64_t bs = p.block_size;
+    const int64_t s = p.slot_mapping[rq];
     const int64_t b = p.block_tables[(int64_t)r * p.max_blocks_per_row + pos / bs];
+    if (s < 0) continue;
     if (b < 0 || b >= p.num_blocks || s != b * bs + pos % bs) {
       if (tid == 0) set_flag(p.err, NP_FLAG_SLOT);
       continue;
     }
-    const int64_t nvec = (int64_t)HG * D * ES / 16;  // 16-byte vectors of the slice
-    const int64_t src0 = (rq * p.kv_heads + (int64_t)hgi * HG) * D * ES / 16;
     const int64_t dst0 = (s * p.kv_heads + (int64_t)hgi * HG) * D * ES / 16;
-    const uint4* kn = static_cast<const uint4*>(p.k_new);
-    const uint4* vn = static_cast<const uint4*>(p.v_new);
     uint4* kd = static_cast<uint4*>(const_cast<void*>(p.k_pool));
     uint4* vd = static_cast<uint4*>(const_cast<void*>(p.v_pool));
-    for (int64_t i = tid; i < nvec; i += nthreads) {
+    if (first) {
+      kd[dst0 + tid] = k0;
+      vd[dst0 + tid] = v0;
+    }
+    for (int64_t i = tid + nthreads; i < nvec; i += nthreads) {
       kd[dst0 + i] = kn[src0 + i];
       vd[dst0 + i] = vn[src0 + i];
     }

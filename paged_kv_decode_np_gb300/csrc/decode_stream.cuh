@@ -269,11 +269,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   __syncthreads();
   const int vb = (int)range[0], ve = (int)range[2];
   const int64_t tb = range[1], te = range[3];
+  // from here on a row's (clamped) length comes from the prefix in shared
+  // memory, not from another global load
+  auto len_of = [&](int v) -> int64_t { return pre[v + 1] - pre[v]; };
 
   // segment k of this CTA (rows vb..ve): token range [ts, tend) of row v
   auto seg_bounds = [&](int v, int64_t& ts, int64_t& tend) {
     ts = (v == vb) ? tb : 0;
-    tend = (v == ve) ? te : row_len(v);
+    tend = (v == ve) ? te : len_of(v);
   };
 
   StageLayout<D, true> L;
@@ -296,7 +299,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   if (warp < kProducer) {
     const int tid = threadIdx.x, nthr = 32 * kProducer;
     for (int v = b; v < V; v += P) {  // rows with no history: zeros
-      if (row_len(v) != 0) continue;
+      if (len_of(v) != 0) continue;
       const int r = v % R, hgi = v / R;
       for (int qi = 0; qi < Q; ++qi) {
         T* o = static_cast<T*>(p.out) + (((int64_t)r * Q + qi) * p.q_heads + hgi * HG * Gr) * D;
@@ -307,7 +310,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       int64_t ts, tend;
       seg_bounds(v, ts, tend);
       if (ts < tend)
-        fused_append<D, (int)sizeof(T)>(p, v % R, v / R, HG, row_len(v), ts, tend, tid, nthr);
+        fused_append<D, (int)sizeof(T)>(p, v % R, v / R, HG, len_of(v), ts, tend, tid, nthr);
     }
     asm volatile("bar.arrive %0, %1;" ::"r"(kAppendBar), "r"(blockDim.x) : "memory");
     if (warp >= HG) return;
@@ -335,7 +338,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     auto load_window = [&](int v, int32_t w) -> int32_t {
       if (v < 0) return 0;
       const int32_t j = w + lane;
-      return j < (int32_t)((row_len(v) + bs - 1) / bs)
+      return j < (int32_t)((len_of(v) + bs - 1) / bs)
                  ? p.block_tables[(int64_t)(v % R) * p.max_blocks_per_row + j]
                  : 0;
     };
@@ -355,7 +358,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     while (v >= 0 && !stop) {
       const int hgi = v / R;
       const int32_t lastw = (tend - 1) / bs / 32 * 32;
-      const int32_t first_new = (int32_t)row_len(v) - Q;  // the row's first new position
+      const int32_t first_new = (int32_t)len_of(v) - Q;  // the row's first new position
       int64_t nts, nte;
       const int vn = next_seg(v + 1, nts, nte);
       auto set_next = [&]() {  // the window after (v, ww), loaded now
@@ -493,7 +496,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     if (ts >= tend) continue;
     const int r = v % R, hgi = v / R;
     const int kvh = hgi * HG + hl;
-    const int64_t c = row_len(v);
+    const int64_t c = len_of(v);
     W.begin(p, r, kvh, c, lane);
     bool ok = true;
     for (int64_t cb = ts; cb < tend; cb += C::CT, ++gch) {
