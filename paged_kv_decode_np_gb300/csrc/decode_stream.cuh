@@ -102,14 +102,17 @@ struct StreamKind<float, D, G, MQ> {  // FMA pipes, 1-D bulk copies of token row
 };
 
 // Shared memory: ring (1024-aligned) | full, empty barriers | abort |
-// virtual-row prefix (int64, V + 1) | consumer tiles (16-aligned).  hg = kv
+// virtual rows' chunk prefix (int64, V + 1) | their lengths (int32, V) |
+// consumer tiles (16-aligned).  hg = kv
 // heads per CTA (8 or 4).
 template <typename T, int D, int G, bool TWO>
 struct StreamSmem {
   using K = StreamKind<T, D, G, TWO>;
+  __host__ __device__ static constexpr size_t lens_offset(int hg, int stages, int vrows) {
+    return K::stage_bytes(hg) * stages + 16ull * stages + 16 + (size_t)(vrows + 1) * 8;
+  }
   __host__ __device__ static constexpr size_t tiles_offset(int hg, int stages, int vrows) {
-    return (K::stage_bytes(hg) * stages + 16ull * stages + 16 +
-            (size_t)(vrows + 1) * sizeof(int64_t) + 15) / 16 * 16;
+    return (lens_offset(hg, stages, vrows) + (size_t)vrows * 4 + 15) / 16 * 16;
   }
   __host__ __device__ static constexpr size_t total(int hg, int stages, int vrows) {
     return 1024 + tiles_offset(hg, stages, vrows) + 8 * K::tile_floats() * sizeof(float);
@@ -149,6 +152,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   uint64_t* empty_bar = full_bar + stages;
   volatile int* abort = reinterpret_cast<volatile int*>(empty_bar + stages);
   int64_t* pre = reinterpret_cast<int64_t*>(smem + ring + 16ull * stages + 16);
+  int32_t* lens =
+      reinterpret_cast<int32_t*>(smem + StreamSmem<T, D, G, TWO>::lens_offset(HG, stages, V));
   float* tiles =
       reinterpret_cast<float*>(smem + StreamSmem<T, D, G, TWO>::tiles_offset(HG, stages, V));
   __shared__ int64_t wsum[32];
@@ -168,15 +173,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     fence_mbar_init();
   }
 
-  // ---- prefix of the virtual rows' lengths: each thread sums a run of
-  // rows, warps scan the run sums with shuffles, warp 0 scans the warp sums
+  // ---- prefix of the virtual rows' chunk counts (ceil(length / CT)):
+  // each thread sums a run of rows, warps scan the run sums with shuffles,
+  // warp 0 scans the warp sums; the lengths stay in shared memory
   {
     const int nt = blockDim.x;
     const int per = (V + nt - 1) / nt;
     const int v0 = threadIdx.x * per, v1 = min(V, v0 + per);
     int64_t sum = 0;
     for (int v = v0; v < v1; ++v) {
-      sum += row_len(v);
+      const int64_t len = row_len(v);
+      lens[v] = (int32_t)len;
+      sum += (len + C::CT - 1) / C::CT;
       if (b == 0 && v < R && (p.context_lens[v] < 0 || p.context_lens[v] > cap))
         set_flag(p.err, NP_FLAG_CONTEXT);  // clamped above
     }
@@ -203,18 +211,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     int64_t run = x - sum + (warp > 0 ? wsum[warp - 1] : 0);
     for (int v = v0; v < v1; ++v) {
       pre[v] = run;
-      run += row_len(v);
+      run += ((int64_t)lens[v] + C::CT - 1) / C::CT;
     }
   }
   __syncthreads();
 
-  // ---- the partition: point(b) = (virtual row, chunk-aligned token) where
-  // CTA b starts; CTA b owns [point(b), point(b+1))
-  const int64_t total = pre[V];
-  constexpr int64_t kMinCtaTokens = 4 * C::CT;  // at least 4 chunks per working CTA
-  const int Pe = (int)min((int64_t)P, max((int64_t)1, (total + kMinCtaTokens - 1) / kMinCtaTokens));
+  // ---- the partition, in chunks (CT tokens; a row's last chunk may be
+  // short): the rows' chunks laid end to end, CTA b takes chunks
+  // [floor(b*W/Pe), floor((b+1)*W/Pe)) of the W in all -- equal chunk
+  // counts to within one.  point(b) = (virtual row, first token) where CTA b
+  // starts; CTA b owns [point(b), point(b+1))
+  const int64_t total = pre[V];  // W
+  constexpr int64_t kMinCtaChunks = 4;  // at least 4 chunks per working CTA
+  const int Pe = (int)min((int64_t)P, max((int64_t)1, (total + kMinCtaChunks - 1) / kMinCtaChunks));
   auto point = [&](int bb, int& pv, int64_t& pt) {
-    const int64_t u = bb >= Pe ? total : (int64_t)bb * total / Pe;  // total < 2^43: no overflow
+    const int64_t u = bb >= Pe ? total : (int64_t)bb * total / Pe;  // total < 2^41: no overflow
     int lo = 0, hi = V;  // the last v with pre[v] <= u
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -222,7 +233,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       else hi = mid - 1;
     }
     pv = lo;
-    pt = lo < V ? (u - pre[lo]) / C::CT * C::CT : 0;
+    pt = lo < V ? (u - pre[lo]) * C::CT : 0;
   };
   if (threadIdx.x == 0) {
     int pv;
@@ -238,14 +249,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     // Merge descriptors {v, b0, bl, slot}: a cut row v, its covering CTAs
     // b0 .. bl, and the slot of b0's partial.  The covering CTAs of v are
     // b0, the CTA whose range holds (v, 0), through bl, the last whose
-    // stream position floor(bb*total/Pe) lies before the row's end
-    // pre[v+1]; CTAs after b0 hold v as their first row (slot 0), b0 holds
-    // it in slot 0 if it is b0's first row, else in slot 1.  Descriptor 0:
-    // the row this CTA's range ends inside, if it began here ((vb, tb) <=
-    // (v, 0)).  Descriptor 1: the row this range starts inside (tb > 0),
-    // begun by an earlier CTA b0 = ceil(X*Pe/total) - 1 with X =
-    // min(pre[v+1], pre[v] + CT) -- the first CTA whose end point lies past
-    // (v, 0) -- and b0's slot 0 exactly when floor(b0*total/Pe) >= pre[v].
+    // stream position floor(bb*W/Pe) lies before the row's end pre[v+1];
+    // CTAs after b0 hold v as their first row (slot 0), b0 holds it in slot
+    // 0 if it is b0's first row, else in slot 1.  Descriptor 0: the row this
+    // CTA's range ends inside, if it began here ((vb, tb) <= (v, 0)).
+    // Descriptor 1: the row this range starts inside (tb > 0), begun by an
+    // earlier CTA b0 = ceil((pre[v] + 1)*Pe/W) - 1 -- the first CTA whose
+    // end point lies past (v, 0) -- and b0's slot 0 exactly when
+    // floor(b0*W/Pe) >= pre[v].
     int4 d = make_int4(-1, 0, 0, 0), e = make_int4(-1, 0, 0, 0);
     if (pt > 0 && pv < V && (vb0 < pv || tb0 == 0)) {
       const int64_t x = pre[pv + 1];
@@ -256,7 +267,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
     if (tb0 > 0 && vb0 < V) {
       const int64_t x0 = pre[vb0], x1 = pre[vb0 + 1];
-      const int64_t X = min(x1, x0 + (int64_t)C::CT);
+      const int64_t X = min(x1, x0 + 1);
       const int b0 = (int)((X * Pe + total - 1) / total) - 1;
       e.x = vb0;
       e.y = b0;
@@ -269,9 +280,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   __syncthreads();
   const int vb = (int)range[0], ve = (int)range[2];
   const int64_t tb = range[1], te = range[3];
-  // from here on a row's (clamped) length comes from the prefix in shared
-  // memory, not from another global load
-  auto len_of = [&](int v) -> int64_t { return pre[v + 1] - pre[v]; };
+  // from here on a row's (clamped) length comes from shared memory, not
+  // from another global load
+  auto len_of = [&](int v) -> int64_t { return lens[v]; };
 
   // segment k of this CTA (rows vb..ve): token range [ts, tend) of row v
   auto seg_bounds = [&](int v, int64_t& ts, int64_t& tend) {
