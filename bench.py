@@ -631,7 +631,7 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
             "query_len": w.query_len,
             "block_size": w.block_size, "max_blocks_per_row": bt.shape[1],
             "num_blocks": md.num_blocks, "num_splits": S,
-            "schedule": "balanced stream (one CTA per SM, equal token shares)" if S == 0
+            "schedule": "balanced stream (one CTA per SM, equal chunk shares)" if S == 0
             else f"split-K x{S}",
             "split_len": npg.np_paged_decode_split_len(w.block_size, bt.shape[1], S) if S > 0
             else None,

@@ -182,7 +182,7 @@ size_t np_paged_decode_workspace_bytes(int32_t rows, int32_t q_heads,
  *                  output and lse into `workspace`; call
  *                  np_paged_decode_reduce next to produce out.
  *                  0: the balanced read -- one thread block per SM (at most
- *                  160), each taking an equal, chunk-aligned share of all
+ *                  160), each taking an equal share (in chunks) of all
  *                  rows' history laid end to end (computed on the device
  *                  from context_lens); rows cut between blocks are merged
  *                  by a second launch on `stream`, each cut row's merge
