@@ -235,47 +235,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     pv = lo;
     pt = lo < V ? (u - pre[lo]) * C::CT : 0;
   };
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 || threadIdx.x == 32) {  // the two ends, found in parallel
+    const int k = threadIdx.x >> 5;
     int pv;
     int64_t pt;
-    point(b, pv, pt);
-    range[0] = pv;
-    range[1] = pt;
-    const int vb0 = pv;
-    const int64_t tb0 = pt;
-    point(b + 1, pv, pt);
-    range[2] = pv;
-    range[3] = pt;
-    // Merge descriptors {v, b0, bl, slot}: a cut row v, its covering CTAs
-    // b0 .. bl, and the slot of b0's partial.  The covering CTAs of v are
-    // b0, the CTA whose range holds (v, 0), through bl, the last whose
-    // stream position floor(bb*W/Pe) lies before the row's end pre[v+1];
-    // CTAs after b0 hold v as their first row (slot 0), b0 holds it in slot
-    // 0 if it is b0's first row, else in slot 1.  Descriptor 0: the row this
-    // CTA's range ends inside, if it began here ((vb, tb) <= (v, 0)).
-    // Descriptor 1: the row this range starts inside (tb > 0), begun by an
-    // earlier CTA b0 = ceil((pre[v] + 1)*Pe/W) - 1 -- the first CTA whose
-    // end point lies past (v, 0) -- and b0's slot 0 exactly when
-    // floor(b0*W/Pe) >= pre[v].
-    int4 d = make_int4(-1, 0, 0, 0), e = make_int4(-1, 0, 0, 0);
-    if (pt > 0 && pv < V && (vb0 < pv || tb0 == 0)) {
-      const int64_t x = pre[pv + 1];
-      d.x = pv;
-      d.y = b;
-      d.z = (int)min((int64_t)Pe - 1, (x * Pe - 1) / total);
-      d.w = vb0 == pv ? 0 : 1;
-    }
-    if (tb0 > 0 && vb0 < V) {
-      const int64_t x0 = pre[vb0], x1 = pre[vb0 + 1];
-      const int64_t X = min(x1, x0 + 1);
-      const int b0 = (int)((X * Pe + total - 1) / total) - 1;
-      e.x = vb0;
-      e.y = b0;
-      e.z = (int)min((int64_t)Pe - 1, (x1 * Pe - 1) / total);
-      e.w = (int64_t)b0 * total / Pe >= x0 ? 0 : 1;
-    }
-    reinterpret_cast<int4*>(p.st_desc)[2 * b] = d;
-    reinterpret_cast<int4*>(p.st_desc)[2 * b + 1] = e;
+    point(b + k, pv, pt);
+    range[2 * k] = pv;
+    range[2 * k + 1] = pt;
   }
   __syncthreads();
   const int vb = (int)range[0], ve = (int)range[2];
@@ -297,7 +263,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   L.RS = 0;
   L.hl = warp % HG;
   if (K::kTmap && (L.BT < 1 || L.BT > C::CT || C::CT % L.BT != 0)) {
-    if (threadIdx.x == 0) set_flag(p.err, NP_FLAG_CONFIG);
+    if (threadIdx.x == 0) {  // no partials: the merge finds no cut rows
+      set_flag(p.err, NP_FLAG_CONFIG);
+      reinterpret_cast<int4*>(p.st_desc)[2 * b] = make_int4(-1, 0, 0, 0);
+      reinterpret_cast<int4*>(p.st_desc)[2 * b + 1] = make_int4(-1, 0, 0, 0);
+    }
     return;
   }
 
@@ -324,6 +294,40 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         fused_append<D, (int)sizeof(T)>(p, v % R, v / R, HG, len_of(v), ts, tend, tid, nthr);
     }
     asm volatile("bar.arrive %0, %1;" ::"r"(kAppendBar), "r"(blockDim.x) : "memory");
+    if (threadIdx.x == 0) {
+      // Merge descriptors {v, b0, bl, slot}: a cut row v, its covering CTAs
+      // b0 .. bl, and the slot of b0's partial.  The covering CTAs of v are
+      // b0, the CTA whose range holds (v, 0), through bl, the last whose
+      // stream position floor(bb*W/Pe) lies before the row's end pre[v+1];
+      // CTAs after b0 hold v as their first row (slot 0), b0 holds it in
+      // slot 0 if it is b0's first row, else in slot 1.  Descriptor 0: the
+      // row this CTA's range ends inside, if it began here ((vb, tb) <= (v,
+      // 0)).  Descriptor 1: the row this range starts inside (tb > 0), begun
+      // by an earlier CTA b0 = ceil((pre[v] + 1)*Pe/W) - 1 -- the first CTA
+      // whose end point lies past (v, 0) -- and b0's slot 0 exactly when
+      // floor(b0*W/Pe) >= pre[v].  Written here, after the partition, so the
+      // 64-bit divisions stay off the producer's start; the merge reads
+      // them only once the read has finished.
+      int4 d = make_int4(-1, 0, 0, 0), e = make_int4(-1, 0, 0, 0);
+      if (te > 0 && ve < V && (vb < ve || tb == 0)) {
+        const int64_t x = pre[ve + 1];
+        d.x = ve;
+        d.y = b;
+        d.z = (int)min((int64_t)Pe - 1, (x * Pe - 1) / total);
+        d.w = vb == ve ? 0 : 1;
+      }
+      if (tb > 0 && vb < V) {
+        const int64_t x0 = pre[vb], x1 = pre[vb + 1];
+        const int64_t X = min(x1, x0 + 1);
+        const int b0 = (int)((X * Pe + total - 1) / total) - 1;
+        e.x = vb;
+        e.y = b0;
+        e.z = (int)min((int64_t)Pe - 1, (x1 * Pe - 1) / total);
+        e.w = (int64_t)b0 * total / Pe >= x0 ? 0 : 1;
+      }
+      reinterpret_cast<int4*>(p.st_desc)[2 * b] = d;
+      reinterpret_cast<int4*>(p.st_desc)[2 * b + 1] = e;
+    }
     if (warp >= HG) return;
   }
 
@@ -675,7 +679,15 @@ __global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_ker
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the read is complete
 #endif
   const int4* desc = reinterpret_cast<const int4*>(p.st_desc) + 2 * c;
-  const int4 d = desc[0], e = desc[1];
+  int4 d = desc[0], e = desc[1];
+  // a descriptor names a row and CTAs of this launch, or nothing
+  const int nv = p.rows * (p.kv_heads / HG);
+  auto valid = [&](const int4& x) {
+    return x.x >= 0 && x.x < nv && x.y >= 0 && x.y <= c && x.z >= c && x.z < (int)gridDim.x &&
+           (x.w == 0 || x.w == 1);
+  };
+  if (!valid(d)) d.x = -1;
+  if (!valid(e)) e.x = -1;
   const int Gr = G > 0 ? G : p.q_heads / p.kv_heads;
   const int NT = (Gr * p.query_len + RPW - 1) / RPW * HG;  // tasks per cut row
   int kd = 0, nd = 1, ke = 0, ne = 1, oe = 0;
