@@ -458,6 +458,25 @@ def test_balanced_read_fp32(nplib, kv_heads, group, head_dim, block_size):
     _full_parity(nplib, w, num_splits=0, fused=False)
 
 
+@pytest.mark.parametrize("dtype,ctx,block_size", [
+    ("bf16", [20000], 16),                    # one row cut across every CTA
+    ("f32", [9000], 16),
+    ("bf16", [16] * 40 + [15] * 40, 16),      # many one-chunk rows: few cuts
+    ("f32", [8] * 100 + [1] * 20, 8),
+    ("bf16", [16 * 37, 16 * 5, 16 * 300, 16], 16),  # lengths whole chunks
+    ("f32", [8 * 41, 8 * 3, 8 * 500, 8], 8),
+    ("bf16", [0, 0, 0, 70000, 0], 32),        # empty rows around a long one
+    ("bf16", [3, 3, 3], 4),                   # fewer chunks than 4 per SM: few CTAs
+])
+def test_balanced_read_partition_edges(nplib, dtype, ctx, block_size):
+    """Partition edge cases of the balanced read: a row cut into as many
+    pieces as there are CTAs (its merge tasks dealt over all of them), many
+    rows of one chunk each, rows of whole chunks (boundaries on row ends),
+    empty rows beside a long one, and a step too small for every SM."""
+    w = _custom(ctx, 32, 8, 128, block_size, dtype, seed=700 + len(ctx) + block_size)
+    _full_parity(nplib, w, num_splits=0)
+
+
 def test_balanced_read_two_calls_one_workspace(nplib):
     """The workspace needs no zeroing: a NaN-filled one, reused by a second
     call with other lengths, must not leak stale partials."""
