@@ -8,17 +8,17 @@
  *      pool of fixed-size blocks at the flat slot given by a slot mapping,
  *      slot = physical_block * block_size + offset ("Day 25: the fused read
  *      dispatches to the kernel backend", What I added today: the read gets
- *      the layer's K/V pools and the slot mapping for the whole history;
+ *      the layer's K/V pools and a slot mapping covering every history token;
  *      What I learned 1: scatter and gather are exact copies).
  *
  *   2. np_paged_decode: each row's single query token attends over that
  *      row's whole history, which is scattered over the pool and addressed
  *      through the row's block table ("Day 17: paging under the sampling
- *      path", Post angle and Diagram: a pool of fixed KV blocks and a block
- *      table mapping tokens to blocks).  The result equals scaled-dot-product
+ *      path", Post angle and Diagram: the cache is a pool of fixed-size
+ *      blocks, and each row's block table maps its positions to blocks).  The result equals scaled-dot-product
  *      attention over the gathered history ("Day 25", What I added today),
  *      computed as a streamed (online) softmax that never materialises the
- *      [rows, heads, 1, ctx] score rectangle ("Day 60: the read becomes a
+ *      [rows, heads, 1, ctx] array of scores ("Day 60: the read becomes a
  *      choice", What I added today and Post angle).  Query heads share kv
  *      heads in groups (GQA): q head h reads kv head h / (q_heads/kv_heads).
  *

@@ -10,13 +10,13 @@
  *      vectors at pool slot block_tables[r][t / bs] * bs + t % bs, kv head
  *      kh ("Day 17: paging under the sampling path", Diagram: a block table
  *      maps tokens to blocks; "Day 25: the fused read dispatches to the
- *      kernel backend", What I added today: SDPA over the assembled slots);
+ *      kernel backend", What I added today: attention over the gathered slots);
  *   2. scores: s_t = scale * sum_d q[r, i, h, d] * K_t[d], over the split's
  *      tokens t in [s * split_len, min((s + 1) * split_len, e)), where
  *      e = c - query_len + i + 1: query token i is the row's position
  *      c - query_len + i and the causal softmax lets it see history
- *      positions up to its own ("Day 25", What I learned 1: the causal fp32
- *      softmax by exact index).  With query_len = 1, e = c: the whole
+ *      positions up to its own ("Day 25", What I learned 1: the reference
+ *      softmax is causal, in fp32, position by position).  With query_len = 1, e = c: the whole
  *      history.  Several query tokens per row are the query_len axis of the
  *      read's score shape rows * heads * query_len * width ("Day 60: the
  *      read becomes a choice", What I learned 5);

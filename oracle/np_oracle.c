@@ -18,7 +18,7 @@
  *    t % block_size.
  *
  *  - The read is the same scaled-dot-product attention over the assembled
- *    slots that the byte-exact torch reference computes: gather the row's
+ *    slots that the torch reference (exact to the byte) computes: gather the row's
  *    whole history by block table, then an exact (two-pass) softmax by index
  *    ("Day 25: the fused read dispatches to the kernel backend", What I added
  *    today and What I learned 1).  One query token per row; it is the newest
@@ -31,8 +31,8 @@
  *
  *  - A decode step first writes the new token's K/V into its slot,
  *    slot = block * block_size + offset, through a slot mapping ("Day 25",
- *    What I added today: the read is handed "the slot mapping for the whole
- *    history"); scatter and gather are exact copies (What I learned 1).
+ *    What I added today: the read receives a slot mapping that covers every
+ *    history token); scatter and gather are exact copies (What I learned 1).
  *    A negative slot means "no token" and is skipped.
  *
  *  - For long contexts the history of a (row, head) can be cut into

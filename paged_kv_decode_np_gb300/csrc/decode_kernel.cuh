@@ -8,10 +8,10 @@
 // "Day 25: the fused read dispatches to the kernel backend", What I added
 // today).  The softmax is streamed: a running max m and sum l per head, the
 // accumulator rescaled by 2^(m_old - m_new) whenever the max grows, so no
-// score rectangle is ever built ("Day 60: the read becomes a choice", What
-// I added today and Post angle; "Day 25", Why it matters: the online softmax
-// reassociates the exponent sums, so results are close to, not bit-equal
-// with, the exact softmax).
+// full array of scores is ever built ("Day 60: the read becomes a choice", What
+// I added today and Post angle; "Day 25", Why it matters: the streamed
+// softmax sums the exponentials in another order, so results are close to,
+// not bit-equal with, the exact softmax).
 //
 // Work decomposition (GB300 design, not from the pages):
 //   grid  = (num_splits, rows, kv_heads / HG)

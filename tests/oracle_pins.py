@@ -13,8 +13,8 @@ What pins what:
     not by the oracle's div/mod form;  lse equals ``torch.logsumexp`` of the
     scores;
   * invariants: permuting physical blocks (and the tables with them) changes
-    nothing, bit for bit ("paging moves where the K/V live, not what attention
-    computes");  NaN in every slot outside the history never reaches the
+    nothing, bit for bit (paging changes where K/V are stored, never the attention result:
+    "Day 17: paging under the sampling path", Diagram);  NaN in every slot outside the history never reaches the
     output;
   * closed forms: one token gives exactly V_0; zero scale or zero query gives
     the mean of V and lse = log(c); identical keys give the mean of V; one
