@@ -531,14 +531,18 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
     ev_h2d, ev_kern, ev_d2h = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
     used = [False, False]
 
+    # each (pool copy, staging slot) step prepared once: the loop then pays
+    # the binding's checks and argument conversion once, not per step
+    prepared = {}
+    for pi, (kp, vp) in enumerate(pools):
+        for k in range(2):
+            db = dbufs[k]
+            prepared[pi, k] = npg.PreparedStep(outs[k], db["q"], db["k_new"], db["v_new"],
+                                               db["sm"], kp, vp, db["bt"], db["cl"],
+                                               w.softmax_scale, S, ws, err, stream)
+
     def launch(i, k):
-        kp, vp = pools[i % len(pools)]
-        db = dbufs[k]
-        npg.np_paged_append_decode(outs[k] if S <= 1 else None, db["q"], db["k_new"],
-                                   db["v_new"], db["sm"], kp, vp, db["bt"], db["cl"],
-                                   w.softmax_scale, S, ws, err, stream)
-        if S > 1:
-            npg.np_paged_decode_reduce(outs[k], ws, S, stream)
+        prepared[i % len(pools), k].launch()
 
     def e2e_serial(i):
         stage_d[0].copy_(stage_h, non_blocking=True)

@@ -36,7 +36,8 @@ __all__ = [
     "np_paged_decode_workspace_bytes", "np_paged_decode", "np_paged_decode_reduce",
     "np_paged_decode_noalloc", "NP_NOALLOC_SCRATCH_BYTES", "np_paged_append_decode",
     "np_selftest_bounded_wait",
-    "workspace", "decode_step", "NP_OK", "NP_ERR_INVALID_ARG", "NP_ERR_UNSUPPORTED",
+    "workspace", "decode_step", "PreparedStep", "NP_OK", "NP_ERR_INVALID_ARG",
+    "NP_ERR_UNSUPPORTED",
     "NP_ERR_WORKSPACE", "NP_ERR_OUT_OF_RANGE", "NP_ERR_CUDA", "NP_F32", "NP_BF16",
     "NP_FLAG_BLOCK_ID", "NP_FLAG_CONTEXT", "NP_FLAG_SLOT", "NP_FLAG_TIMEOUT", "NP_FLAG_CONFIG",
 ]
@@ -269,6 +270,15 @@ def np_paged_append_decode(out, q, k_new, v_new, slot_mapping, k_pool, v_pool, b
     k_new/v_new: [rows, kv_heads, head_dim] (or [rows, query_len, kv_heads,
     head_dim]); slot_mapping: int64 [rows] (or [rows, query_len]).
     """
+    st = load().np_paged_append_decode(*_append_decode_args(
+        out, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables, context_lens, scale,
+        num_splits, workspace, err_word, stream))
+    _check(st, "np_paged_append_decode")
+
+
+def _append_decode_args(out, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables,
+                        context_lens, scale, num_splits, workspace, err_word, stream) -> list:
+    """np_paged_append_decode's C arguments, after the checks."""
     rows, qn, q_heads, d, nb, bs, hk = _check_read_args(
         "np_paged_append_decode", out, q, k_pool, v_pool, block_tables, context_lens)
     want = (rows, hk, d) if q.dim() == 3 else (rows, qn, hk, d)
@@ -280,25 +290,69 @@ def np_paged_append_decode(out, q, k_new, v_new, slot_mapping, k_pool, v_pool, b
         raise ValueError(f"np_paged_append_decode: slot_mapping must be int64 {list(want_sm)}")
     ws_ptr = _opt(workspace, "workspace")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = load().np_paged_append_decode(
-        _opt(out, "out"), _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
-        _dev(slot_mapping, "slot_mapping"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
-        _dtype_code(q.dtype), nb, bs, hk, d, _dev(block_tables, "block_tables"),
-        block_tables.shape[1], _dev(context_lens, "context_lens"), rows, qn, q_heads,
-        float(scale), num_splits, ws_ptr, ws_bytes, _opt(err_word, "err_word"),
-        _stream(stream))
-    _check(st, "np_paged_append_decode")
+    return [_opt(out, "out"), _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+            _dev(slot_mapping, "slot_mapping"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+            _dtype_code(q.dtype), nb, bs, hk, d, _dev(block_tables, "block_tables"),
+            block_tables.shape[1], _dev(context_lens, "context_lens"), rows, qn, q_heads,
+            float(scale), num_splits, ws_ptr, ws_bytes, _opt(err_word, "err_word"),
+            _stream(stream)]
 
 
 def np_paged_decode_reduce(out, workspace, num_splits: int, stream=None):
     """Merge split partials in ``workspace`` into ``out`` ([rows, q_heads, head_dim]
     or [rows, query_len, q_heads, head_dim])."""
+    st = load().np_paged_decode_reduce(*_reduce_args(out, workspace, num_splits, stream))
+    _check(st, "np_paged_decode_reduce")
+
+
+def _reduce_args(out, workspace, num_splits, stream) -> list:
     rows, qn, q_heads, d = _q_shape(out, "out")
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = load().np_paged_decode_reduce(
-        _dev(out, "out"), _dtype_code(out.dtype), _dev(workspace, "workspace"), ws_bytes,
-        rows * qn, q_heads, d, num_splits, _stream(stream))
-    _check(st, "np_paged_decode_reduce")
+    return [_dev(out, "out"), _dtype_code(out.dtype), _dev(workspace, "workspace"), ws_bytes,
+            rows * qn, q_heads, d, num_splits, _stream(stream)]
+
+
+class PreparedStep:
+    """One decode step -- the fused append and read (np_paged_append_decode)
+    and, for a split read, np_paged_decode_reduce -- with its arguments
+    checked and converted to C types once.  ``launch()`` re-issues the same
+    calls at a fraction of the binding's per-call host cost, for loops that
+    run a step again and again on the same buffers (their contents may
+    change between launches; their addresses, shapes, the schedule and the
+    stream may not).  Arguments as for np_paged_append_decode; ``out`` is
+    always the step's output.
+    """
+
+    def __init__(self, out, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables,
+                 context_lens, scale, num_splits: int = 1, workspace=None, err_word=None,
+                 stream=None):
+        lib = load()
+        calls = [("np_paged_append_decode", _append_decode_args(
+            out if num_splits <= 1 else None, q, k_new, v_new, slot_mapping, k_pool, v_pool,
+            block_tables, context_lens, scale, num_splits, workspace, err_word, stream))]
+        if num_splits > 1:
+            calls.append(("np_paged_decode_reduce",
+                          _reduce_args(out, workspace, num_splits, stream)))
+        self._calls = []
+        for name, args in calls:
+            typed = getattr(lib, name)
+            # a second handle to the same symbol, without argtypes: it passes
+            # the already-typed arguments through unconverted
+            raw = lib._FuncPtr((name, lib))
+            raw.restype = ctypes.c_int
+            cargs = tuple(t(a) for t, a in zip(typed.argtypes, args))
+            self._calls.append((name, raw, cargs))
+        self.launches = (2 if num_splits == 0 else 1) + (1 if num_splits > 1 else 0)
+        self._refs = (out, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables,
+                      context_lens, workspace, err_word)  # keep the buffers alive
+
+    def launch(self) -> int:
+        """Issue the step; returns the number of library kernels launched."""
+        for name, fn, cargs in self._calls:
+            st = fn(*cargs)
+            if st != NP_OK:
+                raise NPError(st, name)
+        return self.launches
 
 
 def np_paged_decode_noalloc(out, q, k_pool, v_pool, block_tables, context_lens, scale,

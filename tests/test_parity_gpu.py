@@ -793,3 +793,37 @@ def test_cuda_graph_capture_and_replay(nplib, dtype, splits):
     host2 = dict(host, q=wl.host_array(d.q))
     ref2, _ = oracle_step(host2, w.softmax_scale)
     assert_parity(out, ref2, w.dtype, f"graph replay with a new q {w.name}")
+
+
+@pytest.mark.parametrize("dtype,splits", [("bf16", 0), ("f32", 0), ("bf16", 4), ("f32", 1)])
+def test_prepared_step(nplib, dtype, splits):
+    """PreparedStep issues the same calls as decode_step: equal output bit
+    for bit, the oracle's result, and a relaunch after q is rewritten in
+    place reads the new q."""
+    w = _custom([700, 4096, 33, 0, 1200, 5000], 32, 8, 128, 16, dtype, seed=630 + splits)
+    inp = wl.make_inputs(w)
+    host = wl.full_host(inp)
+    d = wl.Inputs(w, inp.md, *(t.to(DEV) for t in
+                               (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new)))
+    bt, cl, sm = (t.to(DEV) for t in (d.block_tables, d.context_lens, d.slot_mapping))
+    ws = nplib.workspace(w.rows, w.q_heads, w.head_dim, splits, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out_ref = torch.full_like(d.q, float("nan"))
+    nplib.decode_step(out_ref, d.q, d.k_pool, d.v_pool, bt, cl, w.softmax_scale,
+                      k_new=d.k_new, v_new=d.v_new, slot_mapping=sm, num_splits=splits,
+                      workspace=ws, err_word=err)
+    out = torch.full_like(d.q, float("nan"))
+    ps = nplib.PreparedStep(out, d.q, d.k_new, d.v_new, sm, d.k_pool, d.v_pool, bt, cl,
+                            w.softmax_scale, splits, ws, err)
+    assert ps.launch() == (2 if splits == 0 else 1) + (1 if splits > 1 else 0)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(out, out_ref)
+    ref, _ = oracle_step(host, w.softmax_scale)
+    assert_parity(out, ref, w.dtype, f"prepared {w.name}")
+    q2 = torch.randn(d.q.shape, generator=torch.Generator().manual_seed(78)).to(d.q.dtype)
+    d.q.copy_(q2.to(DEV))
+    ps.launch()
+    torch.cuda.synchronize()
+    ref2, _ = oracle_step(dict(host, q=wl.host_array(d.q)), w.softmax_scale)
+    assert_parity(out, ref2, w.dtype, f"prepared relaunch {w.name}")
