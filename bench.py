@@ -350,6 +350,19 @@ def host_threads() -> int:
                else (os.cpu_count() or 1))
 
 
+def cpu_model() -> str:
+    """The host CPU's model name as lscpu reports it (else the machine type)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.split(":")[0].strip() in ("Model name", "Model Name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine() or "unknown"
+
+
 # ---------------------------------------------------------------- arms ----
 def run_reference(args, w: wl.Workload, dist, rank):
     """The oracle arm: each step is the oracle on a bounded sample of rows."""
@@ -385,6 +398,7 @@ def run_reference(args, w: wl.Workload, dist, rank):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "description": w.description},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": nt, "kind": "oracle",
+                         "cpu_model": cpu_model(), "hardware_threads": os.cpu_count(),
                          "sample": f"each step: the C oracle (fp64) on randomly chosen rows "
                                    f"of the {w.name} step, {nt} rows at a time in {nt} host "
                                    f"threads, until {step_budget:.3g} s of wall time "
@@ -492,6 +506,30 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
         elapsed_ms = t_start.elapsed_time(t_end)
     else:  # exclude the L2 flushes between steps
         elapsed_ms = sum(a.elapsed_time(b) for a, b in st_ev)
+
+    # the per-step distribution (median, p10, p90), from a separate pass:
+    # one-step graphs (one per pool copy) replayed with an event pair around
+    # each, so each sample is one step's device time; with the L2 flush, the
+    # timed pass's own per-step pairs
+    if flush is None:
+        one = []
+        for i in range(len(pools)):
+            g1 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g1, stream=cap):
+                step(i, cap)
+            one.append(g1)
+        torch.cuda.synchronize()
+        n_dist = min(args.steps, 200)
+        d_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(n_dist)]
+        for i in range(n_dist):
+            d_ev[i][0].record(stream)
+            one[i % len(one)].replay()
+            d_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        step_us = sorted(1e3 * a.elapsed_time(b) for a, b in d_ev)
+    else:
+        step_us = sorted(1e3 * a.elapsed_time(b) for a, b in st_ev)
     # a step is the library's launches and nothing else
     decode_ms = ([a.elapsed_time(b) for a, b in st_ev] if flush is not None
                  else [elapsed_ms / args.steps])
@@ -627,6 +665,11 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
         "ms_per_step": elapsed_ms / args.steps, "us_per_step": 1e3 * elapsed_ms / args.steps,
         "frac_of_hbm_peak": value / world / peak,
         "frac_of_nominal_8tbs": value / world / 8000.0,
+        "step_us": {"median": statistics.median(step_us), "p10": step_us[len(step_us) // 10],
+                    "p90": step_us[(9 * len(step_us)) // 10], "samples": len(step_us),
+                    "how": "one-step graph replays, an event pair around each (each sample "
+                           "includes the graph's launch latency, which back-to-back steps "
+                           "hide)" if flush is None else "the timed steps' event pairs"},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1) q/K/V, shuffled free-list block tables)",
         "config": {
@@ -683,6 +726,7 @@ def run_ours(args, w: wl.Workload, dist, rank, world, local):
     if cpu is not None:
         line["cpu_baseline"] = {
             "value": cpu["gbs"], "unit": UNIT, "cores": cpu["threads"], "kind": "oracle",
+            "cpu_model": cpu_model(), "hardware_threads": os.cpu_count(),
             "sample": f"rows {cpu['rows']} of this step ({cpu['kv_bytes'] / 1e9:.3f} GB of K/V,"
                       f" {cpu['seconds']:.1f} s wall), the C oracle in fp64, append + read, "
                       f"{cpu['threads']} rows at a time in {cpu['threads']} host threads",
