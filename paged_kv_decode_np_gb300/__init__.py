@@ -20,7 +20,12 @@ Typical decode step::
         npg.np_paged_decode_reduce(out, ws, num_splits=S)
 
 S == 0 (the balanced read) writes ``out`` itself; S > 1 leaves split
-partials for np_paged_decode_reduce.
+partials for np_paged_decode_reduce.  A loop that runs the same step on the
+same buffers again and again can check and convert the arguments once::
+
+    step = npg.PreparedStep(out, q, k_new, v_new, slot_mapping, k_pool, v_pool,
+                            block_tables, context_lens, scale, S, ws)
+    step.launch()   # the same library calls, ~4 us of host time
 """
 from __future__ import annotations
 

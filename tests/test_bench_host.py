@@ -65,3 +65,18 @@ def test_l2_plan():
     assert bench.l2_plan(20_000, 40_000) == 0           # tiny pool: flush instead
     assert bench.l2_plan(L2 // 16, L2 // 16) == 0       # 49 copies: too many, flush
     assert bench.l2_plan(L2 // 8, L2 // 8) == 25
+
+
+def test_algorithmic_bytes_by_hand():
+    """The roofline numerator on the tiny fp32 case, counted by hand: rows 2,
+    q heads 4, kv heads 2, head_dim 16, block 8, contexts 16 and 64, fp32.
+    K/V history (16 + 64) tokens x 2 (K, V) x 2 heads x 16 dims x 4 B = 20480;
+    q and out 2 x 2 rows x 4 heads x 16 x 4 = 1024; table entries
+    (2 + 8) x 4 + context lengths 2 x 4 = 48; the append: new K and V read
+    and written, 2 x 2 x 2 rows x 2 heads x 16 x 4 = 1024, plus 2 slots x 8."""
+    import workloads as wl
+    w = wl.WORKLOADS["tiny-fp32"]
+    inp = wl.make_inputs(w, device="cpu")
+    assert inp.md.context_lens.tolist() == [16, 64]
+    got = bench.algorithmic_bytes(w, inp.md)
+    assert got == {"kv": 20480, "decode": 20480 + 1024 + 48 + 1040, "append": 1040}
