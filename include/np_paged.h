@@ -39,6 +39,11 @@
  *     runs asynchronously; the return value covers argument validation and
  *     the launch only.  Validation failures return before anything is
  *     enqueued.
+ *   - Host threads may call the library concurrently (its only shared state
+ *     is per-device launch configuration, set once, and per-thread caches
+ *     of tensor maps).  On the device, a workspace belongs to one call in
+ *     flight: calls that may overlap (other streams, or a graph replayed
+ *     alongside) each need their own workspace, output and err_word.
  *   - Device-side problems never trap or fault: the affected token/block is
  *     skipped or clamped and a bit is OR-ed into *err_word (a device int32
  *     the caller zeroes and reads when convenient; NULL = not reported).
