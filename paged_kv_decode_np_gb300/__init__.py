@@ -140,24 +140,44 @@ def _dtype_code(dt) -> int:
     raise TypeError(f"unsupported dtype {dt}; the library stores float32 or bfloat16")
 
 
-def _dev(t: torch.Tensor, name: str) -> int:
+def _current_device() -> int:
+    """The CUDA device the library's kernels launch on: torch's current one
+    (the stream, the tensor maps and the no-allocation scratch all belong
+    to it); -1 where CUDA cannot initialise, so that the tensors' own check
+    reports the problem."""
+    try:
+        return torch.cuda.current_device()
+    except (RuntimeError, AssertionError):
+        return -1
+
+
+def _dev(t: torch.Tensor, name: str, cur: int) -> int:
+    """The device address of ``t``, after checking that it is a contiguous
+    tensor on device ``cur`` (a tensor on another GPU would be dereferenced
+    by kernels running on this one)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be on a CUDA device (no CPU path exists)")
+    if t.device.index != cur:
+        raise ValueError(f"{name} is on {t.device} but the current device is cuda:{cur}; "
+                         "call inside torch.cuda.device(...) of the tensors' GPU")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t.data_ptr()
 
 
-def _opt(t: torch.Tensor | None, name: str) -> int | None:
-    return None if t is None else _dev(t, name)
+def _opt(t: torch.Tensor | None, name: str, cur: int) -> int | None:
+    return None if t is None else _dev(t, name, cur)
 
 
 def _stream(stream) -> int | None:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
+        if stream.device.index != _current_device():
+            raise ValueError(f"stream is on {stream.device} but the current device is "
+                             f"cuda:{_current_device()}")
         return stream.cuda_stream
     return int(stream)
 
@@ -196,10 +216,12 @@ def np_kv_append(k_pool, v_pool, k_new, v_new, slot_mapping, err_word=None, stre
         raise ValueError("np_kv_append: shape/dtype mismatch")
     if slot_mapping.dtype != torch.int64 or slot_mapping.shape != (k_new.shape[0],):
         raise ValueError("np_kv_append: slot_mapping must be int64 [num_tokens]")
+    cur = _current_device()
     st = load().np_kv_append(
-        _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), _dtype_code(k_pool.dtype), nb, bs, hk,
-        d, _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(slot_mapping, "slot_mapping"),
-        k_new.shape[0], _opt(err_word, "err_word"), _stream(stream))
+        _dev(k_pool, "k_pool", cur), _dev(v_pool, "v_pool", cur), _dtype_code(k_pool.dtype), nb,
+        bs, hk, d, _dev(k_new, "k_new", cur), _dev(v_new, "v_new", cur),
+        _dev(slot_mapping, "slot_mapping", cur), k_new.shape[0], _opt(err_word, "err_word", cur),
+        _stream(stream))
     _check(st, "np_kv_append")
 
 
@@ -256,14 +278,15 @@ def np_paged_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale,
     """
     rows, qn, q_heads, d, nb, bs, hk = _check_read_args(
         "np_paged_decode", out, q, k_pool, v_pool, block_tables, context_lens)
-    ws_ptr = _opt(workspace, "workspace")
+    cur = _current_device()
+    ws_ptr = _opt(workspace, "workspace", cur)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load().np_paged_decode(
-        _opt(out, "out"), _dev(q, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
-        _dtype_code(q.dtype), nb, bs, hk, d, _dev(block_tables, "block_tables"),
-        block_tables.shape[1], _dev(context_lens, "context_lens"), rows, qn, q_heads,
-        float(scale), num_splits, ws_ptr, ws_bytes, _opt(err_word, "err_word"),
-        _stream(stream))
+        _opt(out, "out", cur), _dev(q, "q", cur), _dev(k_pool, "k_pool", cur),
+        _dev(v_pool, "v_pool", cur), _dtype_code(q.dtype), nb, bs, hk, d,
+        _dev(block_tables, "block_tables", cur), block_tables.shape[1],
+        _dev(context_lens, "context_lens", cur), rows, qn, q_heads, float(scale), num_splits,
+        ws_ptr, ws_bytes, _opt(err_word, "err_word", cur), _stream(stream))
     _check(st, "np_paged_decode")
 
 
@@ -293,14 +316,15 @@ def _append_decode_args(out, q, k_new, v_new, slot_mapping, k_pool, v_pool, bloc
     want_sm = (rows,) if q.dim() == 3 else (rows, qn)
     if slot_mapping.dtype != torch.int64 or tuple(slot_mapping.shape) != want_sm:
         raise ValueError(f"np_paged_append_decode: slot_mapping must be int64 {list(want_sm)}")
-    ws_ptr = _opt(workspace, "workspace")
+    cur = _current_device()
+    ws_ptr = _opt(workspace, "workspace", cur)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    return [_opt(out, "out"), _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
-            _dev(slot_mapping, "slot_mapping"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
-            _dtype_code(q.dtype), nb, bs, hk, d, _dev(block_tables, "block_tables"),
-            block_tables.shape[1], _dev(context_lens, "context_lens"), rows, qn, q_heads,
-            float(scale), num_splits, ws_ptr, ws_bytes, _opt(err_word, "err_word"),
-            _stream(stream)]
+    return [_opt(out, "out", cur), _dev(q, "q", cur), _dev(k_new, "k_new", cur),
+            _dev(v_new, "v_new", cur), _dev(slot_mapping, "slot_mapping", cur),
+            _dev(k_pool, "k_pool", cur), _dev(v_pool, "v_pool", cur), _dtype_code(q.dtype), nb,
+            bs, hk, d, _dev(block_tables, "block_tables", cur), block_tables.shape[1],
+            _dev(context_lens, "context_lens", cur), rows, qn, q_heads, float(scale),
+            num_splits, ws_ptr, ws_bytes, _opt(err_word, "err_word", cur), _stream(stream)]
 
 
 def np_paged_decode_reduce(out, workspace, num_splits: int, stream=None):
@@ -313,8 +337,9 @@ def np_paged_decode_reduce(out, workspace, num_splits: int, stream=None):
 def _reduce_args(out, workspace, num_splits, stream) -> list:
     rows, qn, q_heads, d = _q_shape(out, "out")
     ws_bytes = workspace.numel() * workspace.element_size()
-    return [_dev(out, "out"), _dtype_code(out.dtype), _dev(workspace, "workspace"), ws_bytes,
-            rows * qn, q_heads, d, num_splits, _stream(stream)]
+    cur = _current_device()
+    return [_dev(out, "out", cur), _dtype_code(out.dtype), _dev(workspace, "workspace", cur),
+            ws_bytes, rows * qn, q_heads, d, num_splits, _stream(stream)]
 
 
 class PreparedStep:
@@ -369,11 +394,13 @@ def np_paged_decode_noalloc(out, q, k_pool, v_pool, block_tables, context_lens, 
         raise ValueError("np_paged_decode_noalloc: out is required")
     rows, qn, q_heads, d, nb, bs, hk = _check_read_args(
         "np_paged_decode_noalloc", out, q, k_pool, v_pool, block_tables, context_lens)
+    cur = _current_device()
     st = load().np_paged_decode_noalloc(
-        _dev(out, "out"), _dev(q, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
-        _dtype_code(q.dtype), nb, bs, hk, d, _dev(block_tables, "block_tables"),
-        block_tables.shape[1], _dev(context_lens, "context_lens"), rows, qn, q_heads,
-        float(scale), num_splits, _opt(err_word, "err_word"), _stream(stream))
+        _dev(out, "out", cur), _dev(q, "q", cur), _dev(k_pool, "k_pool", cur),
+        _dev(v_pool, "v_pool", cur), _dtype_code(q.dtype), nb, bs, hk, d,
+        _dev(block_tables, "block_tables", cur), block_tables.shape[1],
+        _dev(context_lens, "context_lens", cur), rows, qn, q_heads, float(scale), num_splits,
+        _opt(err_word, "err_word", cur), _stream(stream))
     _check(st, "np_paged_decode_noalloc")
 
 
@@ -381,8 +408,8 @@ def np_selftest_bounded_wait(err_word, limit_cycles: int, stream=None):
     """Device check of the read's wait-timeout path: a wait that nothing
     completes gives up after ``limit_cycles`` and ORs NP_FLAG_TIMEOUT into
     ``err_word`` (a device int32 tensor); see np_paged.h."""
-    st = load().np_selftest_bounded_wait(_dev(err_word, "err_word"), int(limit_cycles),
-                                         _stream(stream))
+    st = load().np_selftest_bounded_wait(_dev(err_word, "err_word", _current_device()),
+                                         int(limit_cycles), _stream(stream))
     _check(st, "np_selftest_bounded_wait")
 
 

@@ -69,7 +69,7 @@ def stub(tmp_path, monkeypatch):
     lib.stub_last.restype = ctypes.c_char_p
     monkeypatch.setattr(npg, "_LIB", lib)
     # CPU tensors stand in for device ones: only their addresses are passed
-    monkeypatch.setattr(npg, "_dev", lambda t, name: t.data_ptr())
+    monkeypatch.setattr(npg, "_dev", lambda t, name, cur: t.data_ptr())
     monkeypatch.setattr(npg, "_stream", lambda s: 0x5151)
     return lib
 
