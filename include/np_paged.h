@@ -286,8 +286,15 @@ np_status np_paged_decode_reduce(void* out, np_dtype out_dtype,
  *     num_splits == 0 (the balanced read) keeps its cut-row partials there
  *     (it fits for head_dim <= 128).
  *   - The first call on a device looks up the array's device address for
- *     that device (cudaGetSymbolAddress); make that first call before any
- *     stream capture.
+ *     that device (cudaGetSymbolAddress) and keeps it for the life of the
+ *     process; make that first call before any stream capture.  Tearing the
+ *     device's context down (cudaDeviceReset) can move the array, and the
+ *     kept address then points at nothing: do not call this entry point on
+ *     a device after resetting it.
+ *   - Sizes np_paged_decode refuses (negative rows; query_len, q_heads or
+ *     head_dim below 1; num_splits outside 0..65535: NP_ERR_INVALID_ARG; rows above
+ *     65535 or query_len above 16: NP_ERR_UNSUPPORTED) are refused with the
+ *     same codes before the scratch size is compared.
  *   - Every call on a device shares the one array, which keeps the last
  *     call's contents (nothing in it needs to start zeroed).  Calls whose
  *     execution overlaps on the GPU (different streams, or overlapping

@@ -46,7 +46,13 @@ extern "C" np_status np_paged_decode_noalloc(
     return np_paged_decode(out, q, k_pool, v_pool, dtype, num_blocks, block_size, kv_heads,
                            head_dim, block_tables, max_blocks_per_row, context_lens, rows,
                            query_len, q_heads, scale, num_splits, nullptr, 0, err_word, stream);
-  if (rows < 0 || query_len <= 0 || q_heads <= 0 || head_dim <= 0) return NP_ERR_INVALID_ARG;
+  // The shape checks np_paged_decode makes before it looks at a workspace,
+  // with its codes, so that a bad shape is never reported as a scratch
+  // size problem (and rows * query_len below cannot overflow).
+  if (rows < 0 || query_len <= 0 || q_heads <= 0 || head_dim <= 0 || num_splits < 0 ||
+      num_splits > 65535)
+    return NP_ERR_INVALID_ARG;
+  if (rows > 65535 || query_len > 16) return NP_ERR_UNSUPPORTED;
   if (rows == 0) return NP_OK;
   if (num_splits == 0) {  // the balanced read: its cut-row partials go to the scratch
     const size_t need = np_paged_decode_workspace_bytes(rows, q_heads, head_dim, 0);
@@ -60,9 +66,10 @@ extern "C" np_status np_paged_decode_noalloc(
                            stream);
   }
   if (out == nullptr || reinterpret_cast<uintptr_t>(out) % 16 != 0) return NP_ERR_INVALID_ARG;
-  const int32_t units_rows = rows * query_len;
-  const size_t need = np_paged_decode_workspace_bytes(units_rows, q_heads, head_dim, num_splits);
-  if (need > (size_t)NP_NOALLOC_SCRATCH_BYTES) return NP_ERR_WORKSPACE;
+  const int64_t units_rows = (int64_t)rows * query_len;  // <= 65535 * 16: fits int32
+  const size_t need =
+      np_paged_decode_workspace_bytes((int32_t)units_rows, q_heads, head_dim, num_splits);
+  if (need == 0 || need > (size_t)NP_NOALLOC_SCRATCH_BYTES) return NP_ERR_WORKSPACE;
   void* ws = nullptr;
   np_status st = scratch_address(&ws);
   if (st != NP_OK) return st;
@@ -71,6 +78,6 @@ extern "C" np_status np_paged_decode_noalloc(
                        query_len, q_heads, scale, num_splits, ws, NP_NOALLOC_SCRATCH_BYTES,
                        err_word, stream);
   if (st != NP_OK) return st;
-  return np_paged_decode_reduce(out, dtype, ws, NP_NOALLOC_SCRATCH_BYTES, units_rows, q_heads,
-                                head_dim, num_splits, stream);
+  return np_paged_decode_reduce(out, dtype, ws, NP_NOALLOC_SCRATCH_BYTES, (int32_t)units_rows,
+                                q_heads, head_dim, num_splits, stream);
 }

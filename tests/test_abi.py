@@ -101,6 +101,39 @@ def test_decode_validation(lib):
     assert _decode(lib, qlen=8, dtype=1, splits=4, **ok_ptrs) == 3   # workspace missing
 
 
+def _noalloc(lib, **kw):
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, dtype=1, nb=16, bs=16, hk=8, d=128, bt=FAKE,
+             mb=4, cl=FAKE, rows=2, qlen=1, hq=16, scale=0.1, splits=4, err=None)
+    a.update(kw)
+    return lib.np_paged_decode_noalloc(a["out"], a["q"], a["k"], a["v"], a["dtype"], a["nb"],
+                                       a["bs"], a["hk"], a["d"], a["bt"], a["mb"], a["cl"],
+                                       a["rows"], a["qlen"], a["hq"], a["scale"], a["splits"],
+                                       a["err"], None)
+
+
+def test_noalloc_validation_precedes_the_scratch_check(lib):
+    """Sizes np_paged_decode refuses get its codes from the no-allocation
+    entry point too -- never NP_ERR_WORKSPACE -- and rows * query_len is
+    never formed for them; only valid shapes reach the scratch-size check.
+    Every call here returns before touching the device."""
+    assert _noalloc(lib, rows=70000) == 2                   # rows past the grid limit
+    assert _noalloc(lib, rows=2**31 - 1, qlen=16) == 2      # the product would overflow int32
+    assert _noalloc(lib, qlen=17) == 2
+    assert _noalloc(lib, qlen=0) == 1
+    assert _noalloc(lib, rows=-1) == 1
+    assert _noalloc(lib, splits=-1) == 1
+    assert _noalloc(lib, splits=70000) == 1
+    assert _noalloc(lib, hq=0) == 1
+    assert _noalloc(lib, d=0) == 1
+    assert _noalloc(lib, rows=0) == 0                       # nothing to do
+    assert _noalloc(lib, out=None) == 1                     # out is always written
+    assert _noalloc(lib, out=FAKE + 4) == 1
+    # a valid shape whose partials exceed the array
+    per = 2 * 16 * 4 * 129
+    assert _noalloc(lib, splits=(32 << 20) // per + 1) == 3
+    assert _noalloc(lib, splits=1, hq=17) == 1              # one split: np_paged_decode's checks
+
+
 def test_append_validation(lib):
     f = lib.np_kv_append
     assert f(FAKE, FAKE, 0, 16, 16, 2, 128, FAKE, FAKE, FAKE, 0, None, None) == 0  # no tokens
