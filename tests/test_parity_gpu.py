@@ -637,7 +637,7 @@ def test_tensors_off_the_current_device_are_refused(nplib, monkeypatch):
     dereferenced there.  The binding refuses it before any launch (the
     current device is made to look like another one, so one GPU suffices)."""
     w = _custom([40, 70], 16, 8, 128, 16, "bf16", seed=59)
-    inp = wl.make_inputs(w)
+    inp = wl.make_inputs(w, poison=False)      # finite pools: compared with torch.equal
     q, kp, vp, kn, vn = (t.to(DEV) for t in (inp.q, inp.k_pool, inp.v_pool, inp.k_new, inp.v_new))
     bt, cl, sm = (t.to(DEV) for t in (inp.block_tables, inp.context_lens, inp.slot_mapping))
     ws = nplib.workspace(w.rows, w.q_heads, w.head_dim, 4)
