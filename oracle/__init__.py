@@ -20,6 +20,7 @@ Array conventions (numpy, C-contiguous):
 from __future__ import annotations
 
 import ctypes
+import threading
 
 import numpy as np
 
@@ -38,6 +39,7 @@ _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
 _LIB = None
+_LOAD_LOCK = threading.Lock()
 
 
 class OracleError(RuntimeError):
@@ -51,8 +53,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     global _LIB
     if path is not None:
         return _declare(ctypes.CDLL(path))
-    if _LIB is None:
-        _LIB = _declare(ctypes.CDLL(_build.build()))
+    with _LOAD_LOCK:  # host threads may call the oracle at once
+        if _LIB is None:
+            _LIB = _declare(ctypes.CDLL(_build.build()))
     return _LIB
 
 

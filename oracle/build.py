@@ -9,6 +9,7 @@ from __future__ import annotations
 import os
 import subprocess
 import sys
+import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 BUILD_DIR = os.path.join(HERE, "_build")
@@ -27,16 +28,20 @@ def _stale(target: str, deps: list[str]) -> bool:
 def compile_oracle(sources: list[str], out_path: str) -> None:
     """gcc -O2 (no fast-math: libm exp/log and IEEE arithmetic as written)."""
     os.makedirs(os.path.dirname(out_path), exist_ok=True)
-    tmp = out_path + f".tmp{os.getpid()}"
+    tmp = out_path + f".tmp{os.getpid()}.{threading.get_ident()}"
     cmd = ["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-Wall", "-Wextra",
            "-o", tmp, *sources, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out_path)
 
 
+_LOCK = threading.Lock()
+
+
 def build(force: bool = False) -> str:
-    if force or _stale(LIB_PATH, DEPS):
-        compile_oracle(SOURCES, LIB_PATH)
+    with _LOCK:  # threads of one process build it once
+        if force or _stale(LIB_PATH, DEPS):
+            compile_oracle(SOURCES, LIB_PATH)
     return LIB_PATH
 
 
