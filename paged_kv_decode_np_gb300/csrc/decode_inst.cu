@@ -118,11 +118,24 @@ np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
   attr[0].val.programmaticStreamSerializationAllowed = NPK_STREAM_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // Merge tasks: two mma rows each when a row group has 16; half the
+  // head_dim each when the rows are likely cut into more than 16 pieces
+  // (more CTAs than 16 per virtual row), so that one round of loads covers
+  // a row's partials.
   const int mr = L.group * p.query_len;
-  if ((mr >= 16 ? cudaLaunchKernelEx(&cfg, paged_decode_stream_merge_kernel<StorageT, NPK_D, G, 2>, p)
-                : cudaLaunchKernelEx(&cfg, paged_decode_stream_merge_kernel<StorageT, NPK_D, G, 1>,
-                                     p)) != cudaSuccess)
-    return NP_ERR_CUDA;
+  cudaError_t rc = cudaErrorInvalidValue;
+  bool done = false;
+  if constexpr (NPK_D >= 64 && NPK_MERGE_DH2) {
+    if (mr < 16 && 16 * vrows < L.splits) {
+      rc = cudaLaunchKernelEx(&cfg, paged_decode_stream_merge_kernel<StorageT, NPK_D, G, 1, 2>, p);
+      done = true;
+    }
+  }
+  if (!done)
+    rc = mr >= 16
+             ? cudaLaunchKernelEx(&cfg, paged_decode_stream_merge_kernel<StorageT, NPK_D, G, 2, 1>, p)
+             : cudaLaunchKernelEx(&cfg, paged_decode_stream_merge_kernel<StorageT, NPK_D, G, 1, 1>, p);
+  if (rc != cudaSuccess) return NP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? NP_OK : NP_ERR_CUDA;
 }
 #endif

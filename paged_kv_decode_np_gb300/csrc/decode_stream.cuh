@@ -46,6 +46,11 @@ constexpr int kStreamMaxCtas = 160;    // grid cap, >= the GB300's 152 SMs (the
 #define NPK_STREAM_PDL 1
 #endif
 
+// Merge tasks may cover half the head_dim (rows cut into many pieces).
+#ifndef NPK_MERGE_DH2
+#define NPK_MERGE_DH2 1
+#endif
+
 // Merge blocks have 256 * NPK_MERGE_RPB threads (16 warps by default),
 // which share the block's merge tasks.
 #ifndef NPK_MERGE_RPB
@@ -554,21 +559,31 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 }
 
 // One merge task: mma rows row0 .. row0+RPW-1 of kv head hl of the cut
-// row v, over the partials of its covering CTAs b0 .. bl in ascending order,
-// in batches of U; each batch is one round of loads (lane j: partial j's m
-// and l; every lane: its head_dim slice of all U partial rows of its RPW
-// mma rows), then a rescale of the running state to the batch's max (a
-// fixed order: results are deterministic).  Every partial the merge reads
-// is finite (an empty one is m = -inf, l = 0, o = 0), so the weighted sum
-// runs without branches and its loads all issue before the first use.
-// RPW = 2 when a row group has 16 mma rows (fewer tasks per row).
-template <typename T, int D, int G, int RPW>
+// row v -- head_dim part dh of DH -- over the partials of its covering CTAs
+// b0 .. bl in ascending order, in batches of U; each batch is one round of
+// loads (lane j: partial j's m and l; every lane: its slice of the part for
+// all U partial rows of its RPW mma rows), then a rescale of the running
+// state to the batch's max (a fixed order: results are deterministic).
+// Every partial the merge reads is finite (an empty one is m = -inf, l = 0,
+// o = 0), so the weighted sum runs without branches and its loads all issue
+// before the first use.  RPW = 2 when a row group has 16 mma rows (fewer
+// tasks per row); DH = 2 when rows are cut many ways: half the head_dim per
+// task lets one batch hold 32 partials (one round of loads where a whole
+// head_dim would take two).
+template <typename T, int D, int G, int RPW, int DH>
+struct MergeCfg {
+  static constexpr int DL = D / DH / 32;  // dims per lane
+  static constexpr int U = 64 / (RPW * DL) < 32 ? 64 / (RPW * DL) : 32;  // partials per batch
+  static_assert(DL >= 1 && D % (DH * 32) == 0, "merge slices");
+};
+
+template <typename T, int D, int G, int RPW, int DH>
 __device__ __forceinline__ void merge_task(const DecodeParams& p, int v, int b0, int bl,
-                                           int slot_b0, int row0, int hl, int lane) {
+                                           int slot_b0, int row0, int hl, int dh, int lane) {
   constexpr unsigned FULL = 0xffffffffu;
   const int HG = p.head_group;
-  constexpr int DL = D / 32;
-  constexpr int U = RPW >= 2 ? (DL >= 8 ? 4 : 8) : (DL >= 8 ? 8 : 16);
+  constexpr int DL = MergeCfg<T, D, G, RPW, DH>::DL;
+  constexpr int U = MergeCfg<T, D, G, RPW, DH>::U;
   const int Q = p.query_len;
   const int Gr = G > 0 ? G : p.q_heads / p.kv_heads;  // G = 0: the group set at run time
   const int MR = Gr * Q;
@@ -579,7 +594,7 @@ __device__ __forceinline__ void merge_task(const DecodeParams& p, int v, int b0,
   auto entry = [&](int j) -> const float* {  // CTA j's partial of row v, kv head hl
     return p.ws_o + (((int64_t)j * 2 + (j == b0 ? slot_b0 : 0)) * HG + hl) * ent_floats;
   };
-  const int d0 = lane * DL;
+  const int d0 = dh * (D / DH) + lane * DL;
   int rows[RPW];  // this warp's mma rows (a row past MR repeats row0; not stored)
 #pragma unroll
   for (int k = 0; k < RPW; ++k) rows[k] = row0 + k < MR ? row0 + k : row0;
@@ -662,13 +677,14 @@ __device__ __forceinline__ void merge_task(const DecodeParams& p, int v, int b0,
 
 // Merge of the cut rows.  One block per CTA of the read (one wave: every
 // block's work runs at once).  A cut row cut n ways (covering CTAs b0 ..
-// bl, n = bl - b0 + 1) is merged in tasks of RPW mma rows of one kv head,
-// numbered t = group * head_group + head and dealt out over the covering
-// CTAs: the block of CTA b0 + (t mod n) runs task t, so the row is merged
-// on n SMs rather than on its first CTA's.  The read left CTA c's two
-// descriptors: the row it began and cut (c = b0) and the row it continued
-// (c > b0); the block's warps take its tasks of both in turn.
-template <typename T, int D, int G, int RPW>
+// bl, n = bl - b0 + 1) is merged in tasks of RPW mma rows of one kv head
+// (and one of DH head_dim parts), numbered t = (group * head_group + head)
+// * DH + part and dealt out over the covering CTAs: the block of CTA b0 +
+// (t mod n) runs task t, so the row is merged on n SMs rather than on its
+// first CTA's.  The read left CTA c's two descriptors: the row it began and
+// cut (c = b0) and the row it continued (c > b0); the block's warps take
+// its tasks of both in turn.
+template <typename T, int D, int G, int RPW, int DH>
 __global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_kernel(
     const __grid_constant__ DecodeParams p) {
   const int HG = p.head_group;  // kv heads per row group: 8 or 4
@@ -689,7 +705,7 @@ __global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_ker
   if (!valid(d)) d.x = -1;
   if (!valid(e)) e.x = -1;
   const int Gr = G > 0 ? G : p.q_heads / p.kv_heads;
-  const int NT = (Gr * p.query_len + RPW - 1) / RPW * HG;  // tasks per cut row
+  const int NT = (Gr * p.query_len + RPW - 1) / RPW * HG * DH;  // tasks per cut row
   int kd = 0, nd = 1, ke = 0, ne = 1, oe = 0;
   if (d.x >= 0) {  // tasks 0, n, 2n, ... of the row begun here
     nd = max(1, d.z - d.y + 1);
@@ -704,7 +720,8 @@ __global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_ker
     const bool own = k < kd;
     const int t = own ? k * nd : oe + (k - kd) * ne;
     const int4 x = own ? d : e;
-    merge_task<T, D, G, RPW>(p, x.x, x.y, x.z, x.w, (t / HG) * RPW, t % HG, lane);
+    const int hd = t / DH;  // t = hd * DH + part, hd = group * head_group + head
+    merge_task<T, D, G, RPW, DH>(p, x.x, x.y, x.z, x.w, (hd / HG) * RPW, hd % HG, t % DH, lane);
   }
 }
 
