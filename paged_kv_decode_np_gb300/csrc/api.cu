@@ -38,11 +38,10 @@ bool head_dim_supported(int32_t d) {
 
 // GQA group g = q_heads / kv_heads: any g up to 16 on bf16 pools (the
 // tensor-core warps take it at run time; g * query_len <= 16 is checked with
-// the query tokens), the compiled set on fp32 pools (other groups up to 8 run
-// on the balanced read only).
+// the query tokens), up to 8 on fp32 pools (the FMA warp holds 8 rows;
+// groups outside {1, 2, 4, 5, 8} take its run-time-group layout).
 bool group_supported(np_dtype dtype, int32_t g) {
-  if (dtype == NP_BF16) return g >= 1 && g <= 16;
-  return g == 1 || g == 2 || g == 4 || g == 5 || g == 8;
+  return g >= 1 && g <= (dtype == NP_BF16 ? 16 : 8);
 }
 
 // a*b*... without int64 overflow; false on overflow or negative input
@@ -329,17 +328,16 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
       num_splits > 65535 || !isfinite(scale))
     return NP_ERR_INVALID_ARG;
   if (!head_dim_supported(head_dim)) return NP_ERR_UNSUPPORTED;
-  // fp32 groups outside the compiled set (up to 8) run on the balanced read
-  if (!group_supported(dtype, q_heads / kv_heads) &&
-      !(dtype == NP_F32 && q_heads / kv_heads <= 8 && num_splits == 0))
-    return NP_ERR_UNSUPPORTED;
+  if (!group_supported(dtype, q_heads / kv_heads)) return NP_ERR_UNSUPPORTED;
   // several query tokens: (query token, head) rows of a group <= 16 on bf16
-  // pools; <= 8 on fp32 pools, through the balanced read only
+  // pools, <= 8 on fp32 pools
   if (query_len > 1) {
     const int64_t mrows = (int64_t)(q_heads / kv_heads) * query_len;
-    if (dtype == NP_BF16 ? mrows > 16 : (mrows > 8 || num_splits != 0))
-      return NP_ERR_UNSUPPORTED;
+    if (mrows > (dtype == NP_BF16 ? 16 : 8)) return NP_ERR_UNSUPPORTED;
   }
+  // the fp32 warps keep token positions in int32
+  if (dtype == NP_F32 && (int64_t)max_blocks_per_row * block_size > INT32_MAX)
+    return NP_ERR_UNSUPPORTED;
   int64_t slots = 0, pool_elems = 0, pool_bytes = 0, tab = 0;
   if (!mul_ok(num_blocks, block_size, &slots) ||
       !mul_ok(slots, (int64_t)kv_heads * head_dim, &pool_elems) ||

@@ -30,6 +30,7 @@
 #pragma once
 
 #include "decode_kernel.cuh"
+#include "decode_mma.cuh"  // kMmaRows, split_write_rows
 
 namespace npk {
 
@@ -46,7 +47,7 @@ struct FmaCfg {
   static constexpr int LOG_LD = LD >= 32 ? 5 : LD >= 16 ? 4 : LD >= 8 ? 3 : LD >= 4 ? 2 : 1;
   static constexpr int NE = (CT * GP + 31) / 32;       // tile entries per lane in the softmax
   static constexpr int TILE = CT * GP + 8;             // floats per warp: p[CT][GP], alpha[GP]
-  static_assert(D % 32 == 0 && D <= 256, "fp32 balanced read: head_dim 32..256");
+  static_assert(D % 16 == 0 && D <= 256, "fp32 consumer: head_dim 16..256");
   static_assert(DPL % 4 == 0 && 32 % LD == 0 && CT % LT == 0 && NT >= 1, "fp32 layout");
   static_assert(G <= 8, "fp32 balanced read: at most 8 query heads per kv head");
   static_assert(G > 0 || MQ, "a group read at run time takes the 8-row layout");
@@ -237,20 +238,224 @@ struct FmaWarp {
   }
 
   // Unnormalised rows into a [16 rows][D] fp32 array plus m and l ([16]
-  // each), as the merge of cut rows reads them; rows >= MR are skipped.
+  // each) through the store st, as the merges read them; rows >= MR are
+  // skipped.
+  template <typename St = PlainStore>
   __device__ __forceinline__ void store_rows(float* m_out, float* l_out, float* o_out, int MR,
-                                             int lane) const {
+                                             int lane, St st = St()) const {
     const int dl = lane % C::LD;
     if (lane < MR && lane < NR) {
-      m_out[lane] = m;
-      l_out[lane] = l;
+      st(&m_out[lane], m);
+      st(&l_out[lane], l);
     }
     if (lane < C::LD) {
 #pragma unroll
       for (int row = 0; row < NR; ++row)
-        if (row < MR) Storage<float>::template store<C::DPL>(o_out + row * D + dl * C::DPL, acc[row]);
+        if (row < MR) {
+#pragma unroll
+          for (int e = 0; e < C::DPL; e += 4) st.v4(o_out + row * D + dl * C::DPL + e, &acc[row][e]);
+        }
     }
   }
 };
+
+
+// ------------------------------------------------------------------------
+// The split grid on fp32 pools: grid (num_splits, rows, kv_heads / HG),
+// HG*TW consumer warps (FmaWarp, one kv head each; the TW warps of a head
+// take alternate chunks) + 1 producer warp.  A CTA reads tokens
+// [split*split_len, +split_len) of its row for HG kv heads; the producer
+// walks the row's block table (32 entries per load, broadcast by shuffles)
+// and stages chunks of CT token rows [token][HG heads][D] fp32 with 1-D bulk
+// copies -- one per run of tokens inside a block when the pool holds just
+// the CTA's HG kv heads (a contiguous range), else one per token row.  The
+// TW warps of a head merge their states at the end (split_write_rows) and
+// write the rows' output, or this split's partials for the reduce.
+
+// Shared memory: ring (after the read: the warps' (m, l, O) rows for the
+// merge) | per-warp consumer tiles | full, empty barriers | abort flag.
+template <int D, int G, bool MQ>
+struct FmaSplitSmem {
+  using C = FmaCfg<D, G, MQ>;
+  __host__ __device__ static constexpr size_t stage_bytes(int hg) {
+    return 2ull * C::CT * hg * D * sizeof(float);
+  }
+  __host__ __device__ static constexpr size_t ring_bytes(int hg, int stages, int warps) {
+    const size_t ring = stage_bytes(hg) * stages;
+    const size_t m = (size_t)warps * kMmaRows * (D + 2) * sizeof(float);
+    return ((ring > m ? ring : m) + 127) / 128 * 128;
+  }
+  __host__ __device__ static constexpr size_t tiles_bytes(int warps) {
+    return (size_t)warps * C::TILE * sizeof(float);
+  }
+  __host__ __device__ static constexpr size_t total(int hg, int stages, int warps) {
+    return ring_bytes(hg, stages, warps) + tiles_bytes(warps) + 16ull * stages + 16;
+  }
+};
+
+template <int D, int G, bool MQ>
+__global__ void __launch_bounds__(kMaxThreads, 1)
+    paged_decode_fma_kernel(const __grid_constant__ DecodeParams p) {
+  using C = FmaCfg<D, G, MQ>;
+  using S = FmaSplitSmem<D, G, MQ>;
+  constexpr unsigned FULL = 0xffffffffu;
+
+  const int split = blockIdx.x;
+  const int r = blockIdx.y;
+  const int hgi = blockIdx.z;
+  const int HG = p.head_group;
+  const int TW = p.token_warps;
+  const int NC = HG * TW;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int Gr = G > 0 ? G : p.q_heads / p.kv_heads;  // query heads per kv head
+  const int hq0 = hgi * HG * Gr;
+  const int Q = p.query_len;
+  const int MR = Gr * Q;  // (query token, head) rows, <= 8
+
+  const int64_t cap = (int64_t)p.max_blocks_per_row * p.block_size;
+  int64_t c = p.context_lens[r];
+  if (c < 0 || c > cap) {
+    if (threadIdx.x == 0) set_flag(p.err, NP_FLAG_CONTEXT);
+    c = c < 0 ? 0 : cap;
+  }
+  const int64_t t0 = (int64_t)split * p.split_len;
+  const int64_t t1 = min(t0 + p.split_len, c);
+
+  fused_append<D, 4>(p, r, hgi, HG, c, t0, t1);
+
+  if (t0 >= t1) {  // nothing to read: an empty split / an empty row
+    for (int qi = 0; qi < Q; ++qi) {
+      const int64_t rq = (int64_t)r * Q + qi;
+      if (p.num_splits > 1) {
+        for (int i = threadIdx.x; i < HG * Gr; i += blockDim.x)
+          p.ws_lse[(rq * p.q_heads + hq0 + i) * p.num_splits + split] = -INFINITY;
+      } else {
+        float* o = static_cast<float*>(p.out) + (rq * p.q_heads + hq0) * D;
+        for (int i = threadIdx.x; i < HG * Gr * D; i += blockDim.x) o[i] = 0.f;
+      }
+    }
+    return;
+  }
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int stages = p.stages;
+  const size_t stage_bytes = S::stage_bytes(HG);
+  const size_t ring = S::ring_bytes(HG, stages, NC);
+  float* tiles = reinterpret_cast<float*>(smem + ring);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + ring + S::tiles_bytes(NC));
+  uint64_t* empty_bar = full_bar + stages;
+  volatile int* abort = reinterpret_cast<volatile int*>(empty_bar + stages);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(smem_u32(&full_bar[i]), 1);
+      mbar_init(smem_u32(&empty_bar[i]), HG);  // one arrive per consumer warp of a chunk
+    }
+    *abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int64_t nch = (t1 - t0 + C::CT - 1) / C::CT;  // chunks in this split
+  const uint32_t row_bytes = (uint32_t)HG * D * sizeof(float);  // a token's row in a stage
+  FmaWarp<D, G, MQ> W;
+
+  if (warp == NC) {
+    // ======================= producer warp: block-table walk + bulk copies
+    const uint64_t pol = policy_evict_first();
+    const int64_t bs = p.block_size;
+    const int64_t tab0 = (int64_t)r * p.max_blocks_per_row;
+    const int64_t nblk = (c + bs - 1) / bs;  // table entries this row uses
+    const bool whole = (HG == p.kv_heads);
+    const int64_t pool_row = (int64_t)p.kv_heads * D * sizeof(float);  // bytes per slot
+    const char* kpool = static_cast<const char*>(p.k_pool) + (int64_t)hgi * row_bytes;
+    const char* vpool = static_cast<const char*>(p.v_pool) + (int64_t)hgi * row_bytes;
+    int64_t win = -1;
+    int32_t my_id = 0;
+    int64_t issued = 0;
+    for (int64_t ch = 0; ch < nch; ++ch) {
+      const int st = (int)(ch % stages);
+      if (ch >= stages) {
+        bool ok = mbar_wait(smem_u32(&empty_bar[st]), (uint32_t)((ch / stages - 1) & 1), abort);
+        if (!__all_sync(FULL, ok)) break;
+      }
+      const int64_t cb = t0 + ch * C::CT;
+      const int64_t ce = min(cb + (int64_t)C::CT, t1);
+      const uint32_t fb = smem_u32(&full_bar[st]);
+      const uint32_t kdst = smem_u32(smem + st * stage_bytes);
+      const uint32_t vdst = kdst + (uint32_t)(stage_bytes / 2);
+      if (lane == 0) mbar_arrive_expect_tx(fb, 2u * (uint32_t)(ce - cb) * row_bytes);
+      for (int64_t t = cb; t < ce;) {
+        const int64_t j = t / bs;
+        const int64_t off = t - j * bs;
+        const int64_t n = min(bs - off, ce - t);
+        if (win < 0 || j >= win + 32) {
+          win = j;
+          const int64_t jj = j + lane;
+          my_id = jj < nblk ? p.block_tables[tab0 + jj] : 0;
+        }
+        int64_t b = __shfl_sync(FULL, my_id, (int)(j - win));
+        if (b < 0 || b >= p.num_blocks) {
+          if (lane == 0) set_flag(p.err, NP_FLAG_BLOCK_ID);
+          b = 0;
+        }
+        const int64_t slot = b * bs + off;
+        const uint32_t so = (uint32_t)(t - cb) * row_bytes;
+        if (whole) {
+          if (lane == 0) {
+            bulk_g2s(kdst + so, kpool + slot * pool_row, (uint32_t)n * row_bytes, fb, pol);
+            bulk_g2s(vdst + so, vpool + slot * pool_row, (uint32_t)n * row_bytes, fb, pol);
+          }
+        } else {
+          for (int64_t i = lane; i < n; i += 32) {
+            bulk_g2s(kdst + so + (uint32_t)i * row_bytes, kpool + (slot + i) * pool_row,
+                     row_bytes, fb, pol);
+            bulk_g2s(vdst + so + (uint32_t)i * row_bytes, vpool + (slot + i) * pool_row,
+                     row_bytes, fb, pol);
+          }
+        }
+        t += n;
+      }
+      issued = ch + 1;
+    }
+    if (*abort) {  // never leave copies in flight (bounded)
+      for (int64_t ch = max((int64_t)0, issued - stages); ch < issued; ++ch)
+        mbar_wait_drain(smem_u32(&full_bar[ch % stages]), (uint32_t)((ch / stages) & 1));
+    }
+  } else {
+    // ======================= consumer warp: kv head hl, chunks tw, tw+TW, ...
+    const int hl = warp % HG;
+    const int tw = warp / HG;
+    float* tile = tiles + (size_t)warp * C::TILE;
+    W.begin(p, r, hgi * HG + hl, c, lane);
+    for (int64_t ch = tw; ch < nch; ch += TW) {
+      const int st = (int)(ch % stages);
+      bool ok = mbar_wait(smem_u32(&full_bar[st]), (uint32_t)((ch / stages) & 1), abort);
+      if (!__all_sync(FULL, ok)) {
+        set_flag(p.err, NP_FLAG_TIMEOUT);
+        break;
+      }
+      const int64_t tch = t0 + ch * C::CT;  // position of the chunk's first token
+      const int nvalid = (int)min((int64_t)C::CT, t1 - tch);
+      const float* ks = reinterpret_cast<const float*>(smem + st * stage_bytes);
+      W.consume(ks, ks + stage_bytes / 8, hl, HG, nvalid, tch, tile, lane);
+      __syncwarp();  // every lane's reads of this stage are done
+      if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
+    }
+    W.finish();
+  }
+
+  // ======================= epilogue: stage (m, l, O) per warp, merge, store
+  __syncthreads();  // (A) ring no longer in use
+  float* merge = reinterpret_cast<float*>(smem);
+  if (warp < NC) {
+    float* mg = merge + warp * kMmaRows * (D + 2);
+    W.store_rows(mg, mg + kMmaRows, mg + 2 * kMmaRows, MR, lane);
+  }
+  __syncthreads();  // (B)
+  if (warp >= NC || warp / HG != 0) return;
+  split_write_rows<float, D>(p, merge, r, split, hgi * HG + warp, warp, HG, TW, Gr, lane);
+}
 
 }  // namespace npk

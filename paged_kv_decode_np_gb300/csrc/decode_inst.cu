@@ -1,7 +1,7 @@
 // decode_inst.cu -- instantiates the decode kernel for one storage type and
 // head_dim (chosen at compile time: -DNPK_BF16=0/1 -DNPK_D=<head_dim>) and
 // for every supported GQA group, behind one launcher function.
-#include "decode_kernel.cuh"
+#include "decode_fma.cuh"
 #include "decode_launch.h"
 #include "decode_mma.cuh"
 #include "decode_stream.cuh"
@@ -29,8 +29,10 @@ namespace npk {
 namespace {
 
 // bf16 pools run on the tensor cores (decode_mma.cuh): through tiled TMA
-// boxes when the host built pool maps, else through per-token copies.  fp32
-// pools keep full fp32 products on the FMA pipes (decode_kernel.cuh).
+// boxes when the host built pool maps, else through per-token copies
+// (TWO: mma rows past the first 8).  fp32 pools keep full fp32 products on
+// the FMA pipes (decode_fma.cuh; TWO: several query tokens, the 8-row
+// layout).
 template <int G, bool TMAP, bool TWO>
 struct Variant {
 #if NPK_BF16
@@ -38,9 +40,9 @@ struct Variant {
   static constexpr auto kernel = paged_decode_mma_kernel<NPK_D, G, TMAP, TWO>;
   static size_t fixed(int) { return 16 + 128 + 1024; }
 #else
-  using SM = DecodeSmem<StorageT, NPK_D, G>;
-  static constexpr auto kernel = paged_decode_kernel<StorageT, NPK_D, G>;
-  static size_t fixed(int warps) { return SM::ptile_bytes(warps) + 16 + 128; }
+  using SM = FmaSplitSmem<NPK_D, G, TWO>;
+  static constexpr auto kernel = paged_decode_fma_kernel<NPK_D, G, TWO>;
+  static size_t fixed(int warps) { return SM::tiles_bytes(warps) + 16 + 128; }
 #endif
 };
 
@@ -168,7 +170,9 @@ np_status launch_one(DecodeLaunch& L, DecodeParams& p) {
   return two ? launch_variant<G, false, true>(L, p) : launch_variant<G, false, false>(L, p);
 #else
   p.use_tmap = 0;
-  return launch_variant<G, false, false>(L, p);
+  // several query tokens: (query token, head) rows, up to 8, group at run time
+  return p.query_len > 1 ? launch_variant<0, false, true>(L, p)
+                         : launch_variant<G, false, false>(L, p);
 #endif
 }
 
@@ -185,12 +189,15 @@ np_status NPK_LAUNCHER(DecodeLaunch& L, DecodeParams& p) {
     case 5: return launch_one<5>(L, p);
     case 8: return launch_one<8>(L, p);
     default:
+      // other groups up to 8: the FMA warp's 8-row layout with the group read
+      // at run time (host-checked: g * query_len <= 8)
+      if (L.group > 8) return NP_ERR_UNSUPPORTED;
 #ifdef NPK_HAS_STREAM
-      // other groups up to 8: the balanced read's 8-row FMA layout with the
-      // group read at run time (host-checked: balanced, g * query_len <= 8)
-      if (L.streamed && L.group <= 8) return launch_stream<0, true>(L, p);
+      if (L.streamed) return launch_stream<0, true>(L, p);
 #endif
-      return NP_ERR_UNSUPPORTED;
+      if (L.streamed) return NP_ERR_UNSUPPORTED;
+      p.use_tmap = 0;
+      return launch_variant<0, false, true>(L, p);
   }
 #endif
 }

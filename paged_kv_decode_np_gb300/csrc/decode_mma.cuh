@@ -435,18 +435,19 @@ struct MmaWarp {
   }
 
   // Unnormalised result rows into a [16 rows][D] fp32 array plus m and l
-  // ([16] each); rows >= MR are skipped.
+  // ([16] each) through the store st; rows >= MR are skipped.
+  template <typename St = PlainStore>
   __device__ __forceinline__ void store_rows(float* m_out, float* l_out, float* o_out, int MR,
-                                             int lane) const {
+                                             int lane, St st = St()) const {
     const int g4 = lane >> 2;
     if ((lane & 3) == 0) {
       if (g4 < MR) {
-        m_out[g4] = mA;
-        l_out[g4] = lA;
+        st(&m_out[g4], mA);
+        st(&l_out[g4], lA);
       }
       if (TWO && g4 + 8 < MR) {
-        m_out[g4 + 8] = mB;
-        l_out[g4 + 8] = lB;
+        st(&m_out[g4 + 8], mB);
+        st(&l_out[g4 + 8], lB);
       }
     }
     const int c0 = 2 * (lane & 3);  // mma rows of this lane's O^T columns
@@ -454,26 +455,85 @@ struct MmaWarp {
     for (int mi = 0; mi < KS; ++mi) {
       const int d = 16 * mi + g4;
       if (c0 < MR) {
-        o_out[c0 * D + d] = oA[mi][0];
-        o_out[c0 * D + d + 8] = oA[mi][2];
+        st(&o_out[c0 * D + d], oA[mi][0]);
+        st(&o_out[c0 * D + d + 8], oA[mi][2]);
       }
       if (c0 + 1 < MR) {
-        o_out[(c0 + 1) * D + d] = oA[mi][1];
-        o_out[(c0 + 1) * D + d + 8] = oA[mi][3];
+        st(&o_out[(c0 + 1) * D + d], oA[mi][1]);
+        st(&o_out[(c0 + 1) * D + d + 8], oA[mi][3]);
       }
       if constexpr (TWO) {
         if (c0 + 8 < MR) {
-          o_out[(c0 + 8) * D + d] = oB[mi][0];
-          o_out[(c0 + 8) * D + d + 8] = oB[mi][2];
+          st(&o_out[(c0 + 8) * D + d], oB[mi][0]);
+          st(&o_out[(c0 + 8) * D + d + 8], oB[mi][2]);
         }
         if (c0 + 9 < MR) {
-          o_out[(c0 + 9) * D + d] = oB[mi][1];
-          o_out[(c0 + 9) * D + d + 8] = oB[mi][3];
+          st(&o_out[(c0 + 9) * D + d], oB[mi][1]);
+          st(&o_out[(c0 + 9) * D + d + 8], oB[mi][3]);
         }
       }
     }
   }
 };
+
+// The split grid's last step, for the consumer warp of kv head hl with
+// tw = 0: the TW warps of that head left their unnormalised rows (m in log2
+// units, l, O) in `merge` ([warp][m[16] l[16] O[16][D]] fp32); merge them
+// (max and weights) and write each of the G*Q rows -- normalised to `out`
+// (type T) for an unsplit read, else as this split's partial o and natural
+// log lse.
+template <typename T, int D>
+__device__ __forceinline__ void split_write_rows(const DecodeParams& p, const float* merge,
+                                                 int64_t r, int split, int kvh, int hl, int HG,
+                                                 int TW, int Gr, int lane) {
+  constexpr int RW = kMmaRows;
+  const int stride_w = RW * (D + 2);
+  const int Q = p.query_len, MR = Gr * Q;
+  constexpr int DL = D >= 32 ? D / 32 : 1;  // dims per lane
+  const int d0 = lane * DL;
+  for (int row = 0; row < MR; ++row) {
+    float mm = -INFINITY;
+    for (int w2 = 0; w2 < TW; ++w2) mm = fmaxf(mm, merge[(hl + w2 * HG) * stride_w + row]);
+    float ll = 0.f;
+    float acc[DL];
+#pragma unroll
+    for (int e = 0; e < DL; ++e) acc[e] = 0.f;
+    for (int w2 = 0; w2 < TW; ++w2) {
+      const float* mg = merge + (hl + w2 * HG) * stride_w;
+      const float a = (mg[row] == -INFINITY) ? 0.f : ex2(mg[row] - mm);
+      ll = fmaf(mg[RW + row], a, ll);
+      if (d0 < D) {
+#pragma unroll
+        for (int e = 0; e < DL; ++e) acc[e] = fmaf(mg[2 * RW + row * D + d0 + e], a, acc[e]);
+      }
+    }
+    const int qi = row / Gr, h = row - qi * Gr;
+    const int64_t rq = r * Q + qi;
+    const int hq = kvh * Gr + h;
+    const float inv = ll > 0.f ? 1.f / ll : 0.f;
+    float ov[DL];
+#pragma unroll
+    for (int e = 0; e < DL; ++e) ov[e] = acc[e] * inv;
+    if (d0 < D) {
+      if (p.num_splits == 1) {
+        T* orow = static_cast<T*>(p.out) + (rq * p.q_heads + hq) * D;
+        Storage<T>::template store<DL>(orow + d0, ov);
+      } else {
+        const int64_t rs = (rq * p.q_heads + hq) * p.num_splits + split;
+        float* orow = p.ws_o + rs * D + d0;
+        if constexpr (DL >= 4) {
+#pragma unroll
+          for (int e = 0; e < DL; e += 4) Storage<float>::template store<4>(orow + e, ov + e);
+        } else {
+#pragma unroll
+          for (int e = 0; e < DL; ++e) orow[e] = ov[e];
+        }
+        if (lane == 0)
+          p.ws_lse[rs] = ll > 0.f ? mm * 0.69314718055994531f + logf(ll) : -INFINITY;
+      }
+    }
+  }
+}
 
 template <int D, int G, bool TMAP, bool TWO>
 __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
@@ -611,60 +671,13 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
   // ======================= epilogue: stage (m, l, O) per warp, merge, store
   __syncthreads();  // (A) ring no longer in use
   float* merge = reinterpret_cast<float*>(smem);
-  constexpr int RW = kMmaRows;
-  const int stride_w = RW * (D + 2);
   if (warp < NC) {
-    float* mg = merge + warp * stride_w;
-    W.store_rows(mg, mg + RW, mg + 2 * RW, MR, lane);
+    float* mg = merge + warp * kMmaRows * (D + 2);
+    W.store_rows(mg, mg + kMmaRows, mg + 2 * kMmaRows, MR, lane);
   }
   __syncthreads();  // (B)
   if (warp >= NC || warp / HG != 0) return;
-  const int hl = warp;  // tw == 0
-  const int kvh = hgi * HG + hl;
-  constexpr int DL = D >= 32 ? D / 32 : 1;  // dims per lane
-  const int d0 = lane * DL;
-  for (int row = 0; row < MR; ++row) {
-    float mm = -INFINITY;
-    for (int w2 = 0; w2 < TW; ++w2) mm = fmaxf(mm, merge[(hl + w2 * HG) * stride_w + row]);
-    float ll = 0.f;
-    float acc[DL];
-#pragma unroll
-    for (int e = 0; e < DL; ++e) acc[e] = 0.f;
-    for (int w2 = 0; w2 < TW; ++w2) {
-      const float* mg = merge + (hl + w2 * HG) * stride_w;
-      const float a = (mg[row] == -INFINITY) ? 0.f : ex2(mg[row] - mm);
-      ll = fmaf(mg[RW + row], a, ll);
-      if (d0 < D) {
-#pragma unroll
-        for (int e = 0; e < DL; ++e) acc[e] = fmaf(mg[2 * RW + row * D + d0 + e], a, acc[e]);
-      }
-    }
-    const int qi = row / Gr, h = row - qi * Gr;
-    const int64_t rq = (int64_t)r * Q + qi;
-    const int hq = kvh * Gr + h;
-    const float inv = ll > 0.f ? 1.f / ll : 0.f;
-    float ov[DL];
-#pragma unroll
-    for (int e = 0; e < DL; ++e) ov[e] = acc[e] * inv;
-    if (d0 < D) {
-      if (p.num_splits == 1) {
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + (rq * p.q_heads + hq) * D;
-        Storage<__nv_bfloat16>::template store<DL>(orow + d0, ov);
-      } else {
-        const int64_t rs = (rq * p.q_heads + hq) * p.num_splits + split;
-        float* orow = p.ws_o + rs * D + d0;
-        if constexpr (DL >= 4) {
-#pragma unroll
-          for (int e = 0; e < DL; e += 4) Storage<float>::template store<4>(orow + e, ov + e);
-        } else {
-#pragma unroll
-          for (int e = 0; e < DL; ++e) orow[e] = ov[e];
-        }
-        if (lane == 0)
-          p.ws_lse[rs] = ll > 0.f ? mm * 0.69314718055994531f + logf(ll) : -INFINITY;
-      }
-    }
-  }
+  split_write_rows<__nv_bfloat16, D>(p, merge, r, split, hgi * HG + warp, warp, HG, TW, Gr, lane);
 }
 
 }  // namespace npk

@@ -51,6 +51,20 @@ constexpr int kStreamMaxCtas = 160;    // grid cap, >= the GB300's 152 SMs (the
 #define NPK_MERGE_DH2 1
 #endif
 
+// Cut-row partials and merge descriptors are stored with an L2 evict-last
+// hint (the merge reads them back after the read has streamed the pools).
+#ifndef NPK_PARTIAL_KEEP
+#define NPK_PARTIAL_KEEP 1
+#endif
+#if NPK_PARTIAL_KEEP
+using PartialStore = L2KeepStore;
+#else
+struct PartialStore : PlainStore {
+  __device__ __forceinline__ static PartialStore make() { return PartialStore(); }
+  __device__ __forceinline__ void i4(int4* p, int4 v) const { *p = v; }
+};
+#endif
+
 // Merge blocks have 256 * NPK_MERGE_RPB threads (16 warps by default),
 // which share the block's merge tasks.
 #ifndef NPK_MERGE_RPB
@@ -330,8 +344,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         e.z = (int)min((int64_t)Pe - 1, (x1 * Pe - 1) / total);
         e.w = (int64_t)b0 * total / Pe >= x0 ? 0 : 1;
       }
-      reinterpret_cast<int4*>(p.st_desc)[2 * b] = d;
-      reinterpret_cast<int4*>(p.st_desc)[2 * b + 1] = e;
+      const PartialStore keep = PartialStore::make();  // read back by the merge
+      keep.i4(reinterpret_cast<int4*>(p.st_desc) + 2 * b, d);
+      keep.i4(reinterpret_cast<int4*>(p.st_desc) + 2 * b + 1, e);
     }
     if (warp >= HG) return;
   }
@@ -496,15 +511,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
   // ======================= consumer warp hl: its kv head of every segment
   const int hl = warp;
+  const PartialStore keep = PartialStore::make();  // cut-row partials: read by the merge
   if (vb == ve && tb == te && vb < V) {
     // an empty range inside row vb: an empty partial (m = -inf, l = 0, o = 0)
     // in slot 0 for the merge of that row
     float* ent = p.ws_o + ((int64_t)b * 2 * HG + hl) * (int64_t)StreamWs::entry_floats(D);
     if (lane < kMmaRows) {
-      ent[lane] = -INFINITY;
-      ent[kMmaRows + lane] = 0.f;
+      keep(&ent[lane], -INFINITY);
+      keep(&ent[kMmaRows + lane], 0.f);
     }
-    for (int i = lane; i < kMmaRows * D; i += 32) ent[2 * kMmaRows + i] = 0.f;
+    for (int i = lane; i < kMmaRows * D; i += 32) keep(&ent[2 * kMmaRows + i], 0.f);
   }
   typename K::Warp W;
   float* tile = tiles + (size_t)hl * K::tile_floats();  // fp32 consumers' scratch
@@ -554,7 +570,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     first = false;
     const int64_t entry = ((int64_t)b * 2 + slot) * HG + hl;
     float* ent = p.ws_o + entry * (int64_t)StreamWs::entry_floats(D);
-    W.store_rows(ent, ent + kMmaRows, ent + 2 * kMmaRows, MR, lane);
+    W.store_rows(ent, ent + kMmaRows, ent + 2 * kMmaRows, MR, lane, keep);
   }
 }
 

@@ -120,6 +120,42 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// ------------------------------------------------------ row stores --------
+// Plain stores of result rows (shared or global memory).
+struct PlainStore {
+  __device__ __forceinline__ void operator()(float* p, float v) const { *p = v; }
+  __device__ __forceinline__ void v4(float* p, const float* v) const {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+};
+
+// Global stores of rows that a later kernel of the same step reads back
+// (the balanced read's cut-row partials and merge descriptors), with an L2
+// evict-last hint: the read streams GBs through L2 (evict-first) after
+// writing them, and without the hint the merge finds them in DRAM.
+struct L2KeepStore {
+  uint64_t pol;
+  __device__ __forceinline__ static L2KeepStore make() {
+    L2KeepStore s;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(s.pol));
+    return s;
+  }
+  __device__ __forceinline__ void operator()(float* p, float v) const {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol)
+                 : "memory");
+  }
+  __device__ __forceinline__ void v4(float* p, const float* v) const {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
+                 "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "l"(pol)
+                 : "memory");
+  }
+  __device__ __forceinline__ void i4(int4* p, int4 v) const {
+    asm volatile("st.global.L2::cache_hint.v4.s32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+  }
+};
+
 // ----------------------------------------------------------- arithmetic ---
 // 2^x (PTX ex2.approx, flush-to-zero); ex2(-inf) = +0.
 __device__ __forceinline__ float ex2(float x) {

@@ -70,7 +70,10 @@ def test_decode_validation(lib):
     ok_ptrs = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE)
     assert _decode(lib, hq=3, **ok_ptrs) == 1          # q_heads % kv_heads
     assert _decode(lib, d=48, **ok_ptrs) == 2          # head_dim not compiled
-    assert _decode(lib, hk=1, hq=3, **ok_ptrs) == 2    # fp32: group 3 not compiled
+    assert _decode(lib, hk=1, hq=9, **ok_ptrs) == 2    # fp32: group > 8
+    # fp32: any group <= 8 passes validation (without a GPU the launch then
+    # fails with NP_ERR_CUDA)
+    assert _decode(lib, hk=1, hq=3, **ok_ptrs) in (0, 5)
     assert _decode(lib, hk=1, hq=17, dtype=1, **ok_ptrs) == 2  # bf16: group > 16
     # bf16: any group <= 16 passes validation (on a machine without a GPU the
     # launch itself then fails with NP_ERR_CUDA)
@@ -94,7 +97,9 @@ def test_decode_validation(lib):
     assert _decode(lib, splits=4, ws=FAKE, wsb=100, **ok_ptrs) == 3
     assert _decode(lib, nb=2**62, **ok_ptrs) == 4            # pool bytes overflow
     assert _decode(lib, qlen=0, **ok_ptrs) == 1              # no query token
-    assert _decode(lib, qlen=2, **ok_ptrs) == 2              # fp32: several tokens, split grid
+    assert _decode(lib, qlen=2, **ok_ptrs) in (0, 5)         # fp32: 4 rows on the split grid
+    assert _decode(lib, qlen=5, **ok_ptrs) == 2              # fp32: g*query_len > 8
+    assert _decode(lib, mb=2**20, bs=2**12, **ok_ptrs) == 2  # fp32: positions past int32
     assert _decode(lib, qlen=2, splits=0, hk=8, hq=16, **ok_ptrs) == 3  # balanced: needs workspace
     assert _decode(lib, qlen=5, splits=0, hk=8, hq=16, **ok_ptrs) == 2  # fp32: g*query_len > 8
     assert _decode(lib, qlen=9, dtype=1, **ok_ptrs) == 2     # bf16: g*query_len > 16

@@ -23,14 +23,14 @@ def _draw(i: int):
     rnd = random.Random(1000 + i)
     dtype = rnd.choice(["bf16", "f32"])
     head_dim = rnd.choice([16, 32, 64, 128, 256])
-    group = rnd.choice([1, 2, 3, 4, 5, 6, 7, 8, 16] if dtype == "bf16" else [1, 2, 4, 5, 8])
+    group = rnd.choice([1, 2, 3, 4, 5, 6, 7, 8, 16] if dtype == "bf16" else [1, 2, 3, 4, 5, 6, 7, 8])
     kv_heads = rnd.choice([1, 2, 3, 4, 8, 8, 12, 16])
     block_size = rnd.choice([1, 3, 8, 16, 24, 32, 64])
     rows = rnd.randint(1, 12)
-    # several query tokens: bf16 g*Q <= 16 anywhere; fp32 g*Q <= 8 on the balanced read
+    # several query tokens: (query token, head) rows g*Q <= 16 on bf16, <= 8 on fp32
     balanced_ok = (kv_heads % 4 == 0 and head_dim % (64 if dtype == "bf16" else 32) == 0
                    and (dtype == "f32" or kv_heads % 8 == 0 or block_size % 2 == 0))
-    q_max = 16 // group if dtype == "bf16" else (8 // group if balanced_ok else 1)
+    q_max = (16 if dtype == "bf16" else 8) // group
     query_len = rnd.choice([1, 1, 1, max(1, min(q_max, rnd.randint(2, 5)))])
     budget = 60_000 // (kv_heads * max(head_dim, 32))  # keeps the oracle fast
     ctx = []
@@ -47,7 +47,7 @@ def _draw(i: int):
     if query_len > 1:  # rows hold their query run (shorter rows are covered elsewhere)
         ctx = [max(c, query_len) if c else 0 for c in ctx]
     sched = rnd.choice([1, rnd.randint(2, 9)])
-    if balanced_ok and (rnd.random() < 0.7 or (dtype == "f32" and query_len > 1)):
+    if balanced_ok and rnd.random() < 0.7:
         sched = 0  # the default schedule where it applies
     fused = rnd.random() < 0.6
     w = wl.Workload(f"fuzz-{i}", rows=rows, q_heads=kv_heads * group, kv_heads=kv_heads,

@@ -104,8 +104,8 @@ def test_workload_full_parity(nplib, name, fused):
 # the bench times (the plan's schedule, the append fused into the read), every
 # output of every row against the oracle, and both pools after the step
 # against the oracle's append, byte for byte.
-FULL_SIZE = ["tiny-fp32", "llama-fp32", "bf16-gqa4", "bf16-long", "bf16-ragged-bs8",
-             "bf16-ragged-bs32", "bf16-gqa4-q4"]
+FULL_SIZE = ["tiny-fp32", "llama-fp32", "llama-fp32-kv16", "bf16-gqa4", "bf16-long",
+             "bf16-ragged-bs8", "bf16-ragged-bs32", "bf16-gqa4-q4"]
 
 
 @pytest.mark.parametrize("name", FULL_SIZE)
@@ -267,24 +267,22 @@ def test_any_group_on_bf16(nplib, group, kv_heads, query_len):
 
 
 @pytest.mark.parametrize("group,kv_heads,query_len,head_dim", [
-    (3, 8, 1, 128), (6, 8, 1, 64), (7, 4, 1, 128), (3, 8, 2, 256), (6, 12, 1, 32)])
+    (3, 8, 1, 128), (6, 8, 1, 64), (7, 4, 1, 128), (3, 8, 2, 256), (6, 12, 1, 32),
+    (3, 2, 1, 128), (7, 1, 1, 64), (3, 3, 2, 16), (6, 5, 1, 256)])
 def test_other_groups_on_fp32(nplib, group, kv_heads, query_len, head_dim):
-    """fp32 groups outside the compiled set (up to 8 rows) run on the
-    balanced read with the group read at run time; the split grid refuses
-    them."""
+    """fp32 groups outside {1, 2, 4, 5, 8} (up to 8 (query token, head) rows)
+    run on the FMA warp's layout with the group read at run time: on the
+    balanced read where the kv heads allow it, and on the split grid, one
+    split or several."""
     ctx = [1, 300, 2049, 64, 0, 900]
     ctx = [max(c, query_len) if c else 0 for c in ctx]
     w = _custom(ctx, kv_heads * group, kv_heads, head_dim, 16, "f32",
                 seed=400 + group * 7 + kv_heads + query_len, query_len=query_len)
-    _full_parity(nplib, w, num_splits=0)
-    _full_parity(nplib, w, num_splits=0, fused=False)
-    inp = wl.make_inputs(w)
-    d = [t.to(DEV) for t in (inp.q, inp.k_pool, inp.v_pool)]
-    bt, cl = inp.block_tables.to(DEV), inp.context_lens.to(DEV)
-    with pytest.raises(nplib.NPError) as e:
-        nplib.np_paged_decode(torch.empty_like(d[0]), d[0], d[1], d[2], bt, cl, 0.1,
-                              num_splits=1)
-    assert e.value.status == nplib.NP_ERR_UNSUPPORTED
+    if kv_heads % 4 == 0 and head_dim % 32 == 0:
+        _full_parity(nplib, w, num_splits=0)
+        _full_parity(nplib, w, num_splits=0, fused=False)
+    _full_parity(nplib, w, num_splits=1)
+    _full_parity(nplib, w, num_splits=3, fused=False)
 
 
 @pytest.mark.parametrize("kv_heads", [1, 3, 5, 12, 16])
@@ -397,15 +395,18 @@ def test_multi_query_tokens_fp32(nplib, group, query_len, head_dim):
     _full_parity(nplib, w, num_splits=0, fused=False)
 
 
-def test_multi_query_fp32_needs_the_balanced_read(nplib):
-    w = _custom([40, 70], 16, 8, 128, 16, "f32", seed=210, query_len=2)
-    inp = wl.make_inputs(w)
-    d = [t.to(DEV) for t in (inp.q, inp.k_pool, inp.v_pool)]
-    bt, cl = inp.block_tables.to(DEV), inp.context_lens.to(DEV)
-    with pytest.raises(nplib.NPError) as e:
-        nplib.np_paged_decode(torch.empty_like(d[0]), d[0], d[1], d[2], bt, cl, 0.1,
-                              num_splits=1)
-    assert e.value.status == nplib.NP_ERR_UNSUPPORTED
+@pytest.mark.parametrize("group,kv_heads,query_len,head_dim", [
+    (2, 8, 2, 128), (1, 2, 5, 64), (4, 2, 2, 128), (2, 3, 3, 32), (1, 1, 8, 16)])
+def test_multi_query_fp32_split_grid(nplib, group, kv_heads, query_len, head_dim):
+    """Several query tokens per row on fp32 pools through the split grid (any
+    kv head count, head_dim 16 included), one split and several, the append
+    fused or separate."""
+    ctx = [1, query_len, query_len + 1, 63, 64, 65, 700, 1500, 0]
+    w = _custom(ctx, kv_heads * group, kv_heads, head_dim, 16, "f32",
+                seed=210 + group * 7 + kv_heads + query_len, query_len=query_len)
+    _full_parity(nplib, w, num_splits=1)
+    _full_parity(nplib, w, num_splits=4)
+    _full_parity(nplib, w, num_splits=4, fused=False)
 
 
 @pytest.mark.parametrize("head_dim,block_size", [(64, 8), (256, 32), (32, 16)])

@@ -115,6 +115,12 @@ WORKLOADS: dict[str, Workload] = {
                  ctx=("loguniform", 16, 16384), pool=("spare", 256), seed=4,
                  description="bf16 ragged batch, contexts log-uniform "
                              "[16, 16384], block 32, append then read"),
+        Workload("llama-fp32-kv16", rows=8, q_heads=64, kv_heads=16, head_dim=128,
+                 block_size=16, dtype="f32", ctx=("uniform", 512, 2048),
+                 pool=("exact",), seed=5,
+                 description="fp32 decode with 16 kv heads (two 8-head groups per "
+                             "row, so one bulk copy per token row), contexts "
+                             "U[512, 2048]"),
         Workload("bf16-gqa4-q4", rows=64, q_heads=32, kv_heads=8, head_dim=128,
                  block_size=16, dtype="bf16", ctx=("uniform", 1024, 8192),
                  pool=("factor", 1.25), seed=2, query_len=4,
