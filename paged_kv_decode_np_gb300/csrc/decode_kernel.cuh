@@ -70,7 +70,7 @@ struct DecodeParams {
   const void* v_new;
   const int64_t* slot_mapping;  // [R, Q]
   // Balanced streamed read (num_splits == 0; decode_stream.cuh): partials
-  // go to ws_o, each CTA's two merge descriptors to st_desc ([P][2][4]).
+  // go to ws_o, each CTA's merge descriptor to st_desc ([P][4]).
   int32_t rows;
   int32_t* st_desc;
 };

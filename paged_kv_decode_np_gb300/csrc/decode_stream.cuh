@@ -24,9 +24,10 @@
 // m in log2 units, sum l, accumulator O) in the CTA's slot 0 (its first row)
 // or slot 1 (its last row), and the CTA that owns a cut row (the one where
 // the row begins) leaves a descriptor of it.  A second, small kernel then
-// merges each cut row -- one warp per (kv head, mma row) -- over the covering
-// CTAs in CTA order (the split read's max-and-weights combine), so results
-// are deterministic and no thread block ever waits for another.
+// merges each cut row -- in tasks of a few mma rows of one kv head, dealt
+// over all its blocks -- over the covering CTAs in CTA order (the split
+// read's max-and-weights combine), so results are deterministic and no
+// thread block ever waits for another.
 #pragma once
 
 #include "decode_fma.cuh"
@@ -75,7 +76,7 @@ constexpr int kMergeRpb = NPK_MERGE_RPB;
 // Workspace of the streamed read (host and device agree on this):
 //   parts  [kStreamMaxCtas][2 slots][8 kv heads] entries of
 //          m[16] l[16] o[16][D] fp32 (16 = mma rows)
-//   desc   [kStreamMaxCtas] int4: CTA b's merge descriptor {v, c, bl, slot}
+//   desc   [kStreamMaxCtas] int4: CTA b's merge descriptor {v, b, bl, slot}
 //          for the cut row it owns (v = -1: none)
 // Nothing in it needs to start zeroed.
 struct StreamWs {
@@ -85,8 +86,8 @@ struct StreamWs {
   __host__ __device__ static constexpr size_t parts_bytes(int d) {
     return (size_t)kStreamMaxCtas * 2 * 8 * entry_floats(d) * sizeof(float);
   }
-  __host__ __device__ static constexpr size_t bytes(int d) {  // + two int4 descriptors per CTA
-    return parts_bytes(d) + (size_t)kStreamMaxCtas * 8 * sizeof(int32_t);
+  __host__ __device__ static constexpr size_t bytes(int d) {  // + one int4 descriptor per CTA
+    return parts_bytes(d) + (size_t)kStreamMaxCtas * 4 * sizeof(int32_t);
   }
 };
 
@@ -284,8 +285,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   if (K::kTmap && (L.BT < 1 || L.BT > C::CT || C::CT % L.BT != 0)) {
     if (threadIdx.x == 0) {  // no partials: the merge finds no cut rows
       set_flag(p.err, NP_FLAG_CONFIG);
-      reinterpret_cast<int4*>(p.st_desc)[2 * b] = make_int4(-1, 0, 0, 0);
-      reinterpret_cast<int4*>(p.st_desc)[2 * b + 1] = make_int4(-1, 0, 0, 0);
+      reinterpret_cast<int4*>(p.st_desc)[b] = make_int4(-1, 0, 0, 0);
     }
     return;
   }
@@ -314,20 +314,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
     asm volatile("bar.arrive %0, %1;" ::"r"(kAppendBar), "r"(blockDim.x) : "memory");
     if (threadIdx.x == 0) {
-      // Merge descriptors {v, b0, bl, slot}: a cut row v, its covering CTAs
-      // b0 .. bl, and the slot of b0's partial.  The covering CTAs of v are
-      // b0, the CTA whose range holds (v, 0), through bl, the last whose
-      // stream position floor(bb*W/Pe) lies before the row's end pre[v+1];
-      // CTAs after b0 hold v as their first row (slot 0), b0 holds it in
-      // slot 0 if it is b0's first row, else in slot 1.  Descriptor 0: the
-      // row this CTA's range ends inside, if it began here ((vb, tb) <= (v,
-      // 0)).  Descriptor 1: the row this range starts inside (tb > 0), begun
-      // by an earlier CTA b0 = ceil((pre[v] + 1)*Pe/W) - 1 -- the first CTA
-      // whose end point lies past (v, 0) -- and b0's slot 0 exactly when
-      // floor(b0*W/Pe) >= pre[v].  Written here, after the partition, so the
-      // 64-bit divisions stay off the producer's start; the merge reads
-      // them only once the read has finished.
-      int4 d = make_int4(-1, 0, 0, 0), e = make_int4(-1, 0, 0, 0);
+      // Merge descriptor {v, b, bl, slot} of the row this CTA's range ends
+      // inside, if it began here ((vb, tb) <= (v, 0)) and so cuts it: its
+      // covering CTAs are b through bl, the last CTA whose stream position
+      // floor(bb*W/Pe) lies before the row's end pre[v+1]; CTAs after b hold
+      // v as their first row (slot 0), b holds it in slot 0 if it is b's
+      // first row, else in slot 1.  v = -1: no such row.  Written here,
+      // after the partition, so the 64-bit division stays off the
+      // producer's start; the merge reads it only once the read has
+      // finished.
+      int4 d = make_int4(-1, 0, 0, 0);
       if (te > 0 && ve < V && (vb < ve || tb == 0)) {
         const int64_t x = pre[ve + 1];
         d.x = ve;
@@ -335,18 +331,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         d.z = (int)min((int64_t)Pe - 1, (x * Pe - 1) / total);
         d.w = vb == ve ? 0 : 1;
       }
-      if (tb > 0 && vb < V) {
-        const int64_t x0 = pre[vb], x1 = pre[vb + 1];
-        const int64_t X = min(x1, x0 + 1);
-        const int b0 = (int)((X * Pe + total - 1) / total) - 1;
-        e.x = vb;
-        e.y = b0;
-        e.z = (int)min((int64_t)Pe - 1, (x1 * Pe - 1) / total);
-        e.w = (int64_t)b0 * total / Pe >= x0 ? 0 : 1;
-      }
       const PartialStore keep = PartialStore::make();  // read back by the merge
-      keep.i4(reinterpret_cast<int4*>(p.st_desc) + 2 * b, d);
-      keep.i4(reinterpret_cast<int4*>(p.st_desc) + 2 * b + 1, e);
+      keep.i4(reinterpret_cast<int4*>(p.st_desc) + b, d);
     }
     if (warp >= HG) return;
   }
@@ -691,51 +677,59 @@ __device__ __forceinline__ void merge_task(const DecodeParams& p, int v, int b0,
   }
 }
 
-// Merge of the cut rows.  One block per CTA of the read (one wave: every
-// block's work runs at once).  A cut row cut n ways (covering CTAs b0 ..
-// bl, n = bl - b0 + 1) is merged in tasks of RPW mma rows of one kv head
-// (and one of DH head_dim parts), numbered t = (group * head_group + head)
-// * DH + part and dealt out over the covering CTAs: the block of CTA b0 +
-// (t mod n) runs task t, so the row is merged on n SMs rather than on its
-// first CTA's.  The read left CTA c's two descriptors: the row it began and
-// cut (c = b0) and the row it continued (c > b0); the block's warps take
-// its tasks of both in turn.
+// Merge of the cut rows.  One block per CTA of the read (one wave).  The
+// read left, for each CTA b whose range ends inside a row it began (and so
+// cuts it), the descriptor {v, b, bl, slot}: the row, its covering CTAs b ..
+// bl and the slot of b's partial.  Every block loads all P descriptors (one
+// coalesced round), lists the cut rows in CTA order, and the cut rows' tasks
+// -- RPW mma rows of one kv head, one of DH head_dim parts, NT per row, all
+// numbered in that order -- are dealt round-robin over the blocks (block c
+// takes tasks c, c + P, c + 2P, ..., its warps one each in turn), so every
+// SM merges about the same number of tasks whatever the cut rows' lengths
+// and however many of them a CTA touches, and a few tasks still spread over
+// many SMs.
 template <typename T, int D, int G, int RPW, int DH>
 __global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_kernel(
     const __grid_constant__ DecodeParams p) {
   const int HG = p.head_group;  // kv heads per row group: 8 or 4
   const int c = blockIdx.x;
+  const int P = gridDim.x;  // <= kStreamMaxCtas
   const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int lane = threadIdx.x & 31;
+  __shared__ int4 s_desc[kStreamMaxCtas];
+  __shared__ int s_list[kStreamMaxCtas];  // CTAs that own a cut row, in order
+  __shared__ int s_rows;
 #if NPK_STREAM_PDL
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the read is complete
 #endif
-  const int4* desc = reinterpret_cast<const int4*>(p.st_desc) + 2 * c;
-  int4 d = desc[0], e = desc[1];
-  // a descriptor names a row and CTAs of this launch, or nothing
   const int nv = p.rows * (p.kv_heads / HG);
-  auto valid = [&](const int4& x) {
-    return x.x >= 0 && x.x < nv && x.y >= 0 && x.y <= c && x.z >= c && x.z < (int)gridDim.x &&
-           (x.w == 0 || x.w == 1);
-  };
-  if (!valid(d)) d.x = -1;
-  if (!valid(e)) e.x = -1;
+  const int4* desc = reinterpret_cast<const int4*>(p.st_desc);
+  for (int b = threadIdx.x; b < P; b += blockDim.x) {
+    int4 x = desc[b];
+    // a descriptor names a row begun by CTA b and CTAs of this launch, or nothing
+    if (!(x.x >= 0 && x.x < nv && x.y == b && x.z >= b && x.z < P && (x.w == 0 || x.w == 1)))
+      x.x = -1;
+    s_desc[b] = x;
+  }
+  __syncthreads();
+  if (w == 0) {  // list the owners in CTA order (ballots over 32 CTAs at a time)
+    int n = 0;
+    for (int b0 = 0; b0 < P; b0 += 32) {
+      const int b = b0 + lane;
+      const bool own = b < P && s_desc[b].x >= 0;
+      const unsigned m = __ballot_sync(0xffffffffu, own);
+      if (own) s_list[n + __popc(m & ((1u << lane) - 1u))] = b;
+      n += __popc(m);
+    }
+    if (lane == 0) s_rows = n;
+  }
+  __syncthreads();
   const int Gr = G > 0 ? G : p.q_heads / p.kv_heads;
   const int NT = (Gr * p.query_len + RPW - 1) / RPW * HG * DH;  // tasks per cut row
-  int kd = 0, nd = 1, ke = 0, ne = 1, oe = 0;
-  if (d.x >= 0) {  // tasks 0, n, 2n, ... of the row begun here
-    nd = max(1, d.z - d.y + 1);
-    kd = (NT + nd - 1) / nd;
-  }
-  if (e.x >= 0) {  // tasks o, o + n, ... of the row continued here (o = c - b0)
-    ne = max(1, e.z - e.y + 1);
-    oe = c - e.y;
-    ke = oe >= 0 && oe < NT ? (NT - oe + ne - 1) / ne : 0;
-  }
-  for (int k = w; k < kd + ke; k += nw) {
-    const bool own = k < kd;
-    const int t = own ? k * nd : oe + (k - kd) * ne;
-    const int4 x = own ? d : e;
+  const int total = s_rows * NT;
+  for (int g = c + w * P; g < total; g += nw * P) {
+    const int4 x = s_desc[s_list[g / NT]];
+    const int t = g % NT;
     const int hd = t / DH;  // t = hd * DH + part, hd = group * head_group + head
     merge_task<T, D, G, RPW, DH>(p, x.x, x.y, x.z, x.w, (hd / HG) * RPW, hd % HG, t % DH, lane);
   }
