@@ -90,57 +90,44 @@ __device__ __forceinline__ void fused_append(const DecodeParams& p, int r, int h
                                              int tid = threadIdx.x, int nthreads = blockDim.x) {
   if (p.slot_mapping == nullptr) return;
   const int Q = p.query_len;
-  const int64_t pos0 = c - Q;  // position of new token 0
-  // the new tokens j whose positions lie in [t0, t1) (and are >= 0)
-  const int jlo = (int)max((int64_t)0, t0 - pos0);
-  const int jhi = (int)min((int64_t)Q, t1 - pos0);
-  if (jlo >= jhi) return;
-  const int nvec = HG * D * ES / 16;  // 16-byte vectors of a token's slice
-  const int items = (jhi - jlo) * nvec;
-  const uint4* kn = static_cast<const uint4*>(p.k_new);
-  const uint4* vn = static_cast<const uint4*>(p.v_new);
-  uint4* kd = static_cast<uint4*>(const_cast<void*>(p.k_pool));
-  uint4* vd = static_cast<uint4*>(const_cast<void*>(p.v_pool));
-  const int64_t bs = p.block_size;
   bool wrote = false;
-  // Items (token j, vector i) in rounds of kAhead per thread: a round's
-  // loads -- the vectors, the slots, the table entries -- all go out before
-  // any is used (one round trip for up to kAhead * nthreads items, however
-  // many tokens), then the checked stores.
-  constexpr int kAhead = 4;
-  for (int base = tid; base < items; base += kAhead * nthreads) {
-    uint4 kv[kAhead], vv[kAhead];
-    int64_t sl[kAhead], bk[kAhead];
-#pragma unroll
-    for (int u = 0; u < kAhead; ++u) {
-      const int it = base + u * nthreads;
-      sl[u] = -1;
-      bk[u] = -1;
-      if (it < items) {
-        const int j = jlo + it / nvec, i = it - (it / nvec) * nvec;
-        const int64_t rq = (int64_t)r * Q + j;
-        const int64_t src = (rq * p.kv_heads + (int64_t)hgi * HG) * D * ES / 16 + i;
-        kv[u] = kn[src];
-        vv[u] = vn[src];
-        sl[u] = p.slot_mapping[rq];
-        bk[u] = p.block_tables[(int64_t)r * p.max_blocks_per_row + (pos0 + j) / bs];
-      }
+  for (int j = 0; j < Q; ++j) {
+    const int64_t pos = c - Q + j;
+    if (pos < 0 || pos < t0 || pos >= t1) continue;
+    const int64_t rq = (int64_t)r * Q + j;
+    const int64_t nvec = (int64_t)HG * D * ES / 16;  // 16-byte vectors of the slice
+    const int64_t src0 = (rq * p.kv_heads + (int64_t)hgi * HG) * D * ES / 16;
+    const uint4* kn = static_cast<const uint4*>(p.k_new);
+    const uint4* vn = static_cast<const uint4*>(p.v_new);
+    // the slot, its table entry and this thread's first vectors are loaded
+    // together (one round trip, not three in a chain): at the kernel's start
+    // the read's own copies load the memory system
+    const bool first = tid < nvec;
+    uint4 k0 = make_uint4(0, 0, 0, 0), v0 = k0;
+    if (first) {
+      k0 = kn[src0 + tid];
+      v0 = vn[src0 + tid];
     }
-#pragma unroll
-    for (int u = 0; u < kAhead; ++u) {
-      const int it = base + u * nthreads;
-      if (it >= items || sl[u] < 0) continue;  // a negative slot: no new token
-      const int j = jlo + it / nvec, i = it - (it / nvec) * nvec;
-      const int64_t pos = pos0 + j;
-      if (bk[u] < 0 || bk[u] >= p.num_blocks || sl[u] != bk[u] * bs + pos % bs) {
-        if (i == 0) set_flag(p.err, NP_FLAG_SLOT);
-        continue;
-      }
-      const int64_t dst = (sl[u] * p.kv_heads + (int64_t)hgi * HG) * D * ES / 16 + i;
-      kd[dst] = kv[u];
-      vd[dst] = vv[u];
-      wrote = true;
+    const int64_t bs = p.block_size;
+    const int64_t s = p.slot_mapping[rq];
+    const int64_t b = p.block_tables[(int64_t)r * p.max_blocks_per_row + pos / bs];
+    if (s < 0) continue;
+    if (b < 0 || b >= p.num_blocks || s != b * bs + pos % bs) {
+      if (tid == 0) set_flag(p.err, NP_FLAG_SLOT);
+      continue;
     }
+    const int64_t dst0 = (s * p.kv_heads + (int64_t)hgi * HG) * D * ES / 16;
+    uint4* kd = static_cast<uint4*>(const_cast<void*>(p.k_pool));
+    uint4* vd = static_cast<uint4*>(const_cast<void*>(p.v_pool));
+    if (first) {
+      kd[dst0 + tid] = k0;
+      vd[dst0 + tid] = v0;
+    }
+    for (int64_t i = tid + nthreads; i < nvec; i += nthreads) {
+      kd[dst0 + i] = kn[src0 + i];
+      vd[dst0 + i] = vn[src0 + i];
+    }
+    wrote = true;
   }
   if (wrote) asm volatile("fence.proxy.async.global;" ::: "memory");
 }
