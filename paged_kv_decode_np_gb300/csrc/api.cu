@@ -86,23 +86,53 @@ np_status device_info(int* sms, int* smem) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// kv heads per CTA of the balanced streamed read: 8, or 4 when the count is
-// a multiple of 4 but not of 8 (0: not a multiple of 4).
-int stream_head_group(int32_t kv_heads) {
-  return kv_heads % 8 == 0 ? 8 : (kv_heads % 4 == 0 ? 4 : 0);
+// Consumer warps per kv head of the balanced streamed read (TW): up to
+// 8 / HG, each taking ct0 tokens of every stage (ct0: the consumer warp's
+// chunk, 1024 / head_dim fp32 rows or the mma chunk), so that a stage holds
+// TW * ct0 tokens and the per-stage costs of the producer (barriers, table
+// lookups, copy issue) are paid once per TW * ct0 tokens.  A stage must not
+// straddle two 32-block windows of the block table: TW * ct0 divides
+// 32 * block_size.  HG = 4 keeps one warp per head when built with
+// NPK_STREAM_TW4=0.
+#ifndef NPK_STREAM_TW4
+#define NPK_STREAM_TW4 0
+#endif
+#ifndef NPK_STREAM_TWMAX
+#define NPK_STREAM_TWMAX 8
+#endif
+int stream_chunk_tokens(np_dtype dtype, int32_t head_dim) {
+  return dtype == NP_BF16 ? npk::mma_chunk_tokens(head_dim) : 1024 / head_dim;
+}
+int stream_token_warps(np_dtype dtype, int32_t head_dim, int hg, int32_t block_size) {
+  if (hg == 4 && !NPK_STREAM_TW4) return 1;
+  const int ct0 = stream_chunk_tokens(dtype, head_dim);
+  int tw = npk::kMaxConsumerWarps / hg;
+  if (tw > NPK_STREAM_TWMAX) tw = NPK_STREAM_TWMAX;
+  while (tw > 1 && ((int64_t)32 * block_size) % ((int64_t)ct0 * tw) != 0) --tw;
+  return tw;
+}
+
+// Tokens per tiled TMA box of the bf16 read: the largest power of two that
+// divides the block size, at most a stage's tokens.
+int box_tokens_for(int32_t block_size, int32_t head_dim) {
+  const int ct = npk::mma_chunk_tokens(head_dim);
+  int bt = 1;
+  while (bt < ct && block_size % (bt * 2) == 0) bt *= 2;
+  return bt;
 }
 
 // Shapes the balanced streamed read (num_splits == 0) handles: bf16 pools
-// with head_dim a multiple of 64 or fp32 pools with head_dim a multiple of
-// 32, kv heads in groups of 8 or 4 (bf16 with 4: an even block size, so the
-// TMA boxes keep the swizzle alignment), at most kStreamMaxVRows (row, head
-// group) pairs, contexts that fit int32.
+// with head_dim a multiple of 64 (tiled TMA boxes of box_tokens x HG heads
+// starting on 1024-byte swizzle boundaries: box_tokens * HG a multiple of 8)
+// or fp32 pools with head_dim a multiple of 32, at most kStreamMaxVRows
+// (row, head group) pairs, contexts that fit int32.  HG is the largest
+// divisor of kv_heads up to 8.
 bool stream_ok(np_dtype dtype, int32_t head_dim, int32_t kv_heads, int32_t rows,
                int32_t max_blocks_per_row, int32_t block_size) {
-  const int hg = stream_head_group(kv_heads);
+  const int hg = head_group_of(kv_heads);
   const bool dim_ok = dtype == NP_BF16 ? head_dim % 64 == 0 : head_dim % 32 == 0;
-  return hg > 0 && dim_ok && head_dim <= 256 &&
-         (dtype != NP_BF16 || hg == 8 || block_size % 2 == 0) &&
+  return dim_ok && head_dim <= 256 &&
+         (dtype != NP_BF16 || (box_tokens_for(block_size, head_dim) * hg) % 8 == 0) &&
          (int64_t)rows * (kv_heads / hg) <= npk::kStreamMaxVRows &&
          (int64_t)max_blocks_per_row * block_size <= INT32_MAX;
 }
@@ -123,20 +153,23 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return fn;
 }
 
-// Map of one pool as a 3-D tensor (dim, slot, kv head) -- the kv-head
-// dimension is listed last although its stride (head_dim*2 bytes) is the
-// smaller one, so that a box {64, box_tokens, head_group} lands in shared
-// memory as [head][token][64 dims] (each head's tokens in consecutive
-// 128-byte rows, 128-byte swizzle).  Returns false if the driver refuses.
+// Map of one pool as a 4-D tensor (64 dims, slot, kv head, 64-dim slab):
+// the dimensions are listed in the order a box lands in shared memory, not
+// by stride, so that one box {64, box_tokens, head_group, head_dim/64}
+// arrives as [slab][head][token][64 dims] -- each head's tokens in
+// consecutive 128-byte rows (128-byte swizzle) -- and one copy per box
+// brings every slab of its tokens.  Returns false if the driver refuses.
 bool encode_pool_map(CUtensorMap* m, const void* pool, int64_t slots, int32_t kv_heads,
                      int32_t head_dim, int box_tokens, int head_group) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
   if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)slots, (cuuint64_t)kv_heads};
-  cuuint64_t strides[2] = {(cuuint64_t)kv_heads * head_dim * 2, (cuuint64_t)head_dim * 2};
-  cuuint32_t box[3] = {64u, (cuuint32_t)box_tokens, (cuuint32_t)head_group};
-  cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult rc = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides,
+  cuuint64_t dims[4] = {64u, (cuuint64_t)slots, (cuuint64_t)kv_heads,
+                        (cuuint64_t)(head_dim / 64)};
+  cuuint64_t strides[3] = {(cuuint64_t)kv_heads * head_dim * 2, (cuuint64_t)head_dim * 2, 128u};
+  cuuint32_t box[4] = {64u, (cuuint32_t)box_tokens, (cuuint32_t)head_group,
+                       (cuuint32_t)(head_dim / 64)};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult rc = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return rc == CUDA_SUCCESS;
@@ -378,7 +411,7 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
   np_status st = device_info(&sms, &smem_optin);
   if (st != NP_OK) return st;
 
-  const int hg = streamed ? stream_head_group(kv_heads) : head_group_of(kv_heads);
+  const int hg = head_group_of(kv_heads);
   DecodeParams p{};
   p.out = out;
   p.ws_o = ws_o;
@@ -395,7 +428,8 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
   p.block_size = block_size;
   p.kv_heads = kv_heads;
   p.head_group = hg;
-  p.token_warps = npk::kMaxConsumerWarps / hg;
+  p.token_warps =
+      streamed ? stream_token_warps(dtype, head_dim, hg, block_size) : npk::kMaxConsumerWarps / hg;
   p.max_blocks_per_row = max_blocks_per_row;
   p.q_heads = q_heads;
   p.num_splits = num_splits;
@@ -415,9 +449,7 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
   p.use_tmap = 0;
   p.box_tokens = 1;
   if (dtype == NP_BF16 && head_dim % 64 == 0 && slots <= INT32_MAX) {
-    const int ct = npk::mma_chunk_tokens(head_dim);  // a box never exceeds a stage
-    int bt = 1;
-    while (bt < ct && block_size % (bt * 2) == 0) bt *= 2;
+    const int bt = box_tokens_for(block_size, head_dim);  // a box never exceeds a stage
     if ((bt * hg) % 8 == 0 &&
         pool_maps(p, k_pool, v_pool, slots, kv_heads, head_dim, bt, hg)) {
       p.use_tmap = 1;

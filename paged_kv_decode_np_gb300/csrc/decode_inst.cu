@@ -87,14 +87,27 @@ np_status launch_variant(DecodeLaunch& L, DecodeParams& p) {
 template <int G, bool TWO>
 np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
   using SS = StreamSmem<StorageT, NPK_D, G, TWO>;
-  const int hg = p.head_group;  // 8 or 4
+  const int hg = p.head_group;  // kv heads per CTA
   const int vrows = p.rows * (p.kv_heads / hg);
   // static shared memory of the kernel (scan scratch) comes off the budget
   const size_t budget = L.smem_budget - 4096;
-  size_t stages = 8;
-  while (stages >= 2 && SS::total(hg, (int)stages, vrows) > budget) --stages;
+  // a ring of up to 192 KB in flight (fewer, larger stages with more heads);
+  // when TW > 1 consumer warps per head leave no room for two stages next to
+  // their row-boundary states, half as many warps per head read (a stage of
+  // fewer tokens still divides the block table's 32-block windows)
+  size_t stages = 0;
+  int tw = p.token_warps;
+  for (;;) {
+    const size_t sb = SS::stage_bytes(hg, tw);
+    stages = (196608 / sb) < 2 ? 2 : (196608 / sb) > 32 ? 32 : 196608 / sb;
+    while (stages >= 2 && SS::total(hg, tw, (int)stages, vrows) > budget) --stages;
+    if (stages >= 2 || tw == 1) break;
+    tw = tw % 2 == 0 ? tw / 2 : 1;
+  }
   if (stages < 2) return NP_ERR_UNSUPPORTED;
-  const size_t smem = SS::total(hg, (int)stages, vrows);
+  p.token_warps = tw;
+  L.token_warps = tw;
+  const size_t smem = SS::total(hg, tw, (int)stages, vrows);
   p.stages = (int)stages;
   L.stages = (int)stages;
   L.smem_bytes = smem;

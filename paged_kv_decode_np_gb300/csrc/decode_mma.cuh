@@ -138,8 +138,8 @@ __device__ __forceinline__ float softmax_row(float (&sc)[4], float& m_run, float
 template <int D, bool TMAP>
 struct StageLayout {
   int BT;               // tokens per TMA box
-  uint32_t half_bytes;  // one 64-dim slab of a chunk (TMAP)
-  uint32_t box_bytes;   // one box within a slab (TMAP)
+  uint32_t slab_bytes;  // one 64-dim slab of a box: HG heads x BT rows of 128 bytes (TMAP)
+  uint32_t box_bytes;   // one box: D/64 slabs (TMAP)
   uint32_t RS;          // token-row stride (per-token copies)
   int hl;               // kv head within the CTA's group
 
@@ -157,7 +157,7 @@ struct StageLayout {
                                             int ld_c) const {
     if constexpr (TMAP) {
       const uint32_t cidx = ((2 * ks) & 7) + ld_c;  // chunk within the 128-byte row
-      return base + (ks >> 2) * half_bytes + off + ((cidx ^ swz) << 4);
+      return base + (ks >> 2) * slab_bytes + off + ((cidx ^ swz) << 4);
     } else {
       return base + off + ks * 32 + ld_c * 16;
     }
@@ -185,29 +185,28 @@ __device__ __forceinline__ void produce_chunk(const DecodeParams& p, const Stage
     my_id = jj < nblk ? p.block_tables[r * p.max_blocks_per_row + jj] : 0;
   }
   if constexpr (TMAP) {
-    // boxes of BT tokens; each lies inside one block (BT divides the block
-    // size and the chunk start) and is copied whole (rows past the history
-    // are masked by the consumers)
+    // boxes of BT tokens x HG heads x all D/64 slabs; each lies inside one
+    // block (BT divides the block size and the chunk start) and is copied
+    // whole (rows past the history are masked by the consumers)
     const int nbox = (n + L.BT - 1) / L.BT;
-    if (lane == 0) mbar_arrive_expect_tx(fb, 2u * (D / 64) * nbox * L.box_bytes);
-    const int items = nbox * (D / 64) * 2;  // (box, slab, K|V)
+    if (lane == 0) mbar_arrive_expect_tx(fb, 2u * nbox * L.box_bytes);
+    const int items = nbox * 2;  // (box, K|V)
     const int rounds = (items + 31) / 32;
     for (int rd = 0; rd < rounds; ++rd) {
       const int it = rd * 32 + lane;
-      const int bx = (it < items ? it : 0) / ((D / 64) * 2);
+      const int bx = (it < items ? it : 0) >> 1;
       const int64_t t = cb + (int64_t)bx * L.BT;
       const int64_t j = t / bs;
       int64_t b = __shfl_sync(FULL, my_id, (int)(j - win));
       if (it < items) {
-        const int slab = (it >> 1) % (D / 64);
         const bool isv = (it & 1) != 0;
         if (b < 0 || b >= p.num_blocks) {
           set_flag(p.err, NP_FLAG_BLOCK_ID);
           b = 0;
         }
         const int64_t slot = b * bs + (t - j * bs);
-        const uint32_t dst = (isv ? vdst : kdst) + slab * L.half_bytes + bx * L.box_bytes;
-        tma_load_3d(dst, isv ? &p.tm_v : &p.tm_k, slab * 64, (int32_t)slot, hgi * HG, fb, pol);
+        const uint32_t dst = (isv ? vdst : kdst) + bx * L.box_bytes;
+        tma_load_4d(dst, isv ? &p.tm_v : &p.tm_k, 0, (int32_t)slot, hgi * HG, 0, fb, pol);
       }
     }
   } else {
@@ -602,12 +601,12 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
   __syncthreads();
 
   const int64_t nch = (t1 - t0 + C::CT - 1) / C::CT;
-  // TMAP layout of a stage: [K | V] x [D/64 slabs of 64 dims] x [CT/B boxes]
+  // TMAP layout of a stage: [K | V] x [CT/B boxes] x [D/64 slabs of 64 dims]
   //                         x [HG heads] x [B token rows of 128 bytes]
   StageLayout<D, TMAP> L;
   L.BT = TMAP ? p.box_tokens : 1;
-  L.half_bytes = (uint32_t)C::CT * HG * 128;
-  L.box_bytes = (uint32_t)L.BT * HG * 128;
+  L.slab_bytes = (uint32_t)L.BT * HG * 128;
+  L.box_bytes = (uint32_t)(D / 64) * L.slab_bytes;
   L.RS = (uint32_t)S::row_stride(HG);
   L.hl = warp % HG;
   if (TMAP && (L.BT < 1 || L.BT > C::CT || C::CT % L.BT != 0)) {

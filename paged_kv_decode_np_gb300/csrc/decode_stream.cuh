@@ -123,21 +123,86 @@ struct StreamKind<float, D, G, MQ> {  // FMA pipes, 1-D bulk copies of token row
 
 // Shared memory: ring (1024-aligned) | full, empty barriers | abort |
 // virtual rows' chunk prefix (int64, V + 1) | their lengths (int32, V) |
-// consumer tiles (16-aligned).  hg = kv
-// heads per CTA (8 or 4).
+// consumer tiles (16-aligned) | the token warps' states (tw > 1).  hg = kv
+// heads per CTA, tw = consumer warps per kv head: a stage holds tw * K::CT
+// tokens, K::CT for each of a head's warps.
 template <typename T, int D, int G, bool TWO>
 struct StreamSmem {
   using K = StreamKind<T, D, G, TWO>;
-  __host__ __device__ static constexpr size_t lens_offset(int hg, int stages, int vrows) {
-    return K::stage_bytes(hg) * stages + 16ull * stages + 16 + (size_t)(vrows + 1) * 8;
+  __host__ __device__ static constexpr size_t stage_bytes(int hg, int tw) {
+    return K::stage_bytes(hg) * tw;
   }
-  __host__ __device__ static constexpr size_t tiles_offset(int hg, int stages, int vrows) {
-    return (lens_offset(hg, stages, vrows) + (size_t)vrows * 4 + 15) / 16 * 16;
+  __host__ __device__ static constexpr size_t lens_offset(int hg, int tw, int stages, int vrows) {
+    return stage_bytes(hg, tw) * stages + 16ull * stages + 16 + (size_t)(vrows + 1) * 8;
   }
-  __host__ __device__ static constexpr size_t total(int hg, int stages, int vrows) {
-    return 1024 + tiles_offset(hg, stages, vrows) + 8 * K::tile_floats() * sizeof(float);
+  __host__ __device__ static constexpr size_t tiles_offset(int hg, int tw, int stages, int vrows) {
+    return (lens_offset(hg, tw, stages, vrows) + (size_t)vrows * 4 + 15) / 16 * 16;
+  }
+  // several consumer warps per kv head (tw > 1): their (m, l, O) rows at a
+  // row boundary, one entry per warp
+  __host__ __device__ static constexpr size_t merge_offset(int hg, int tw, int stages, int vrows) {
+    return (tiles_offset(hg, tw, stages, vrows) + 8 * K::tile_floats() * sizeof(float) + 15) /
+           16 * 16;
+  }
+  __host__ __device__ static constexpr size_t total(int hg, int tw, int stages, int vrows) {
+    return 1024 + merge_offset(hg, tw, stages, vrows) +
+           (tw > 1 ? (size_t)kMaxConsumerWarps * StreamWs::entry_floats(D) * sizeof(float) : 0) +
+           (tw > 1 ? 16 : 0);  // + the merge's two mbarriers
   }
 };
+
+// The TW consumer warps of kv head hl (warps hl, hl + HG, ...) left their
+// unnormalised states (m in log2 units, l, O rows) side by side in `ws`;
+// warp tw merges rows tw, tw + TW, ... of them in warp order (max and
+// weights) and stores each row: normalised to `out` when the whole row is
+// this CTA's, else unnormalised to the cut row's partial entry `ent` for the
+// merge kernel.
+template <typename T, int D, typename St>
+__device__ __forceinline__ void merge_warp_states(const DecodeParams& p, const float* ws, int hl,
+                                                  int HG, int TW, int tw, int MR, int Gr,
+                                                  int64_t r, int kvh, bool whole, float* ent,
+                                                  St keep, int lane) {
+  constexpr int RW = kMmaRows;
+  constexpr int DL = D >= 32 ? D / 32 : 1;  // dims per lane
+  const int64_t stride = (int64_t)StreamWs::entry_floats(D);
+  const int Q = p.query_len;
+  const int d0 = lane * DL;
+  for (int row = tw; row < MR; row += TW) {
+    float mm = -INFINITY;
+    for (int w2 = 0; w2 < TW; ++w2) mm = fmaxf(mm, ws[(hl + w2 * HG) * stride + row]);
+    const float msub = mm == -INFINITY ? 0.f : mm;
+    float ll = 0.f, acc[DL];
+#pragma unroll
+    for (int e = 0; e < DL; ++e) acc[e] = 0.f;
+    for (int w2 = 0; w2 < TW; ++w2) {
+      const float* w = ws + (hl + w2 * HG) * stride;
+      const float a = ex2(w[row] - msub);  // a state with nothing in it: m = -inf, a = 0
+      ll = fmaf(w[RW + row], a, ll);
+      if (d0 < D) {
+#pragma unroll
+        for (int e = 0; e < DL; ++e) acc[e] = fmaf(w[2 * RW + row * D + d0 + e], a, acc[e]);
+      }
+    }
+    if (whole) {
+      const float inv = ll > 0.f ? 1.f / ll : 0.f;
+      float ov[DL];
+#pragma unroll
+      for (int e = 0; e < DL; ++e) ov[e] = acc[e] * inv;
+      const int qi = row / Gr, h = row - qi * Gr;
+      T* o = static_cast<T*>(p.out) + ((r * Q + qi) * p.q_heads + (int64_t)kvh * Gr + h) * D;
+      if (d0 < D) Storage<T>::template store<DL>(o + d0, ov);
+    } else {
+      if (lane == 0) {
+        keep(&ent[row], mm);
+        keep(&ent[RW + row], ll);
+      }
+      if (d0 < D) {
+#pragma unroll
+        for (int e = 0; e < DL; ++e) keep(&ent[2 * RW + row * D + d0 + e], acc[e]);
+      }
+    }
+  }
+}
 
 template <typename T, int D, int G, bool TWO>
 __global__ void __launch_bounds__(kMaxThreads, 1)
@@ -145,7 +210,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   using K = StreamKind<T, D, G, TWO>;
   using C = K;  // chunk geometry (CT, ST)
   constexpr unsigned FULL = 0xffffffffu;
-  const int HG = p.head_group;  // kv heads per CTA: 8, or 4 (consumer warps 0 .. HG-1)
+  const int HG = p.head_group;   // kv heads per CTA (the largest divisor of kv_heads <= 8)
+  const int TW = p.token_warps;  // consumer warps per kv head (HG * TW <= 8)
+  const int NCW = HG * TW;       // consumer warps 0 .. NCW-1: warp w reads kv head w % HG
   constexpr int kProducer = kMaxConsumerWarps;  // warp 8
 
   const int b = blockIdx.x;
@@ -166,16 +233,22 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int stages = p.stages;
-  const size_t stage_bytes = K::stage_bytes(HG);
+  // a stage: CT = K::CT tokens for each of a head's TW consumer warps
+  const int CT = C::CT * TW;
+  const size_t stage_bytes = StreamSmem<T, D, G, TWO>::stage_bytes(HG, TW);
   const size_t ring = stage_bytes * stages;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + ring);
   uint64_t* empty_bar = full_bar + stages;
   volatile int* abort = reinterpret_cast<volatile int*>(empty_bar + stages);
   int64_t* pre = reinterpret_cast<int64_t*>(smem + ring + 16ull * stages + 16);
   int32_t* lens =
-      reinterpret_cast<int32_t*>(smem + StreamSmem<T, D, G, TWO>::lens_offset(HG, stages, V));
+      reinterpret_cast<int32_t*>(smem + StreamSmem<T, D, G, TWO>::lens_offset(HG, TW, stages, V));
   float* tiles =
-      reinterpret_cast<float*>(smem + StreamSmem<T, D, G, TWO>::tiles_offset(HG, stages, V));
+      reinterpret_cast<float*>(smem + StreamSmem<T, D, G, TWO>::tiles_offset(HG, TW, stages, V));
+  float* wstate =  // TW > 1: the consumer warps' states at a row boundary
+      reinterpret_cast<float*>(smem + StreamSmem<T, D, G, TWO>::merge_offset(HG, TW, stages, V));
+  uint64_t* seg_bar = reinterpret_cast<uint64_t*>(wstate + kMaxConsumerWarps *
+                                                             StreamWs::entry_floats(D));
   __shared__ int64_t wsum[32];
   __shared__ int64_t range[4];  // vb, tb, ve, te
 
@@ -187,7 +260,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   if (threadIdx.x == 0) {  // the ring's barriers (ordered by the scan's barriers)
     for (int i = 0; i < stages; ++i) {
       mbar_init(smem_u32(&full_bar[i]), 1);
-      mbar_init(smem_u32(&empty_bar[i]), HG);  // one arrive per consumer warp
+      mbar_init(smem_u32(&empty_bar[i]), NCW);  // one arrive per consumer warp
+    }
+    if (TW > 1) {  // row boundaries: states written, then merged (all consumer warps)
+      mbar_init(smem_u32(&seg_bar[0]), NCW);
+      mbar_init(smem_u32(&seg_bar[1]), NCW);
     }
     *abort = 0;
     fence_mbar_init();
@@ -204,7 +281,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     for (int v = v0; v < v1; ++v) {
       const int64_t len = row_len(v);
       lens[v] = (int32_t)len;
-      sum += (len + C::CT - 1) / C::CT;
+      sum += (len + CT - 1) / CT;
       if (b == 0 && v < R && (p.context_lens[v] < 0 || p.context_lens[v] > cap))
         set_flag(p.err, NP_FLAG_CONTEXT);  // clamped above
     }
@@ -231,7 +308,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     int64_t run = x - sum + (warp > 0 ? wsum[warp - 1] : 0);
     for (int v = v0; v < v1; ++v) {
       pre[v] = run;
-      run += ((int64_t)lens[v] + C::CT - 1) / C::CT;
+      run += ((int64_t)lens[v] + CT - 1) / CT;
     }
   }
   __syncthreads();
@@ -253,7 +330,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       else hi = mid - 1;
     }
     pv = lo;
-    pt = lo < V ? (u - pre[lo]) * C::CT : 0;
+    pt = lo < V ? (u - pre[lo]) * CT : 0;
   };
   if (threadIdx.x == 0 || threadIdx.x == 32) {  // the two ends, found in parallel
     const int k = threadIdx.x >> 5;
@@ -278,11 +355,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
   StageLayout<D, true> L;
   L.BT = p.box_tokens;
-  L.half_bytes = (uint32_t)C::CT * HG * 128;
-  L.box_bytes = (uint32_t)L.BT * HG * 128;
+  L.slab_bytes = (uint32_t)L.BT * HG * 128;
+  L.box_bytes = (uint32_t)(D / 64) * L.slab_bytes;
   L.RS = 0;
   L.hl = warp % HG;
-  if (K::kTmap && (L.BT < 1 || L.BT > C::CT || C::CT % L.BT != 0)) {
+  if (K::kTmap && (L.BT < 1 || L.BT > C::CT || C::CT % L.BT != 0)) {  // boxes tile a slice
     if (threadIdx.x == 0) {  // no partials: the merge finds no cut rows
       set_flag(p.err, NP_FLAG_CONFIG);
       reinterpret_cast<int4*>(p.st_desc)[b] = make_int4(-1, 0, 0, 0);
@@ -334,7 +411,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       const PartialStore keep = PartialStore::make();  // read back by the merge
       keep.i4(reinterpret_cast<int4*>(p.st_desc) + b, d);
     }
-    if (warp >= HG) return;
+    if (warp >= NCW) return;
   }
 
   if (warp == kProducer) {
@@ -393,7 +470,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         nxt = load_window(nv, nw);
       };
       set_next();
-      for (int32_t cb = ts; cb < tend; cb += C::CT, ++gch) {
+      for (int32_t cb = ts; cb < tend; cb += CT, ++gch) {
         if (gch >= stages) {
           bool ok = mbar_wait(smem_u32(&empty_bar[st]), ph, abort);
           if (!__all_sync(FULL, ok)) {
@@ -407,7 +484,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           cur = (nv == v && nw == w) ? nxt : load_window(v, w);
           set_next();
         }
-        const int n = min(C::CT, tend - cb);
+        const int n = min(CT, tend - cb);
         if (fused && !appended && cb + n > first_new) {
           asm volatile("bar.sync %0, %1;" ::"r"(kAppendBar), "r"(blockDim.x) : "memory");
           appended = true;
@@ -417,11 +494,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         const uint32_t fb = smem_u32(&full_bar[st]);
         if constexpr (K::kTmap) {
           const int nbox = (n + L.BT - 1) / L.BT;
-          if (lane == 0) mbar_arrive_expect_tx(fb, 2u * (D / 64) * nbox * L.box_bytes);
-          const int items = nbox * (D / 64) * 2;  // (box, slab, K|V)
+          if (lane == 0) mbar_arrive_expect_tx(fb, 2u * nbox * L.box_bytes);
+          const int items = nbox * 2;  // (box, K|V)
           for (int it0 = 0; it0 < items; it0 += 32) {
             const int it = it0 + lane;
-            const int bx = (it < items ? it : 0) / ((D / 64) * 2);
+            const int bx = (it < items ? it : 0) >> 1;
             const int32_t t = cb + bx * L.BT;
             const int32_t j = t / bs;
             int32_t blk = __shfl_sync(FULL, cur, j - ww);
@@ -430,18 +507,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 set_flag(p.err, NP_FLAG_BLOCK_ID);
                 blk = 0;
               }
-              const int slab = (it >> 1) % (D / 64);
               const bool isv = (it & 1) != 0;
               const int32_t slot = blk * bs + (t - j * bs);
-              tma_load_3d((isv ? vdst : kdst) + slab * L.half_bytes + bx * L.box_bytes,
-                          isv ? &p.tm_v : &p.tm_k, slab * 64, slot, hgi * HG, fb, pol);
+              tma_load_4d((isv ? vdst : kdst) + bx * L.box_bytes, isv ? &p.tm_v : &p.tm_k, 0, slot,
+                          hgi * HG, 0, fb, pol);
             }
           }
         } else {
           // stage rows [token][HG kv heads][D]: when the pool has just HG kv
           // heads a run of tokens inside one block is one contiguous copy
           // (lane k: the chunk's k-th block); else one copy per token (lane =
-          // token).  A chunk holds at most 32 tokens and lies in window ww.
+          // token, 32 tokens a round).  A chunk lies in window ww.
           const uint32_t row_b = (uint32_t)HG * D * (uint32_t)sizeof(T);
           const int64_t pool_row = (int64_t)p.kv_heads * D * (int64_t)sizeof(T);
           const char* kp = static_cast<const char*>(p.k_pool) + (int64_t)hgi * row_b;
@@ -449,25 +525,28 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           if (lane == 0) mbar_arrive_expect_tx(fb, 2u * (uint32_t)n * row_b);
           const int32_t jf = cb / bs;
           const bool whole = p.kv_heads == HG;
-          const int32_t j = whole ? jf + lane : (cb + min(lane, n - 1)) / bs;
-          int32_t blk = __shfl_sync(FULL, cur, (j - ww) & 31);
-          int64_t ta, tz;  // this lane's tokens [ta, tz)
-          if (whole) {
-            ta = max((int64_t)cb, (int64_t)j * bs);
-            tz = min((int64_t)cb + n, ((int64_t)j + 1) * bs);
-          } else {
-            ta = cb + lane;
-            tz = lane < n ? ta + 1 : ta;
-          }
-          if (ta < tz) {
-            if (blk < 0 || blk >= p.num_blocks) {
-              set_flag(p.err, NP_FLAG_BLOCK_ID);
-              blk = 0;
+          for (int g0 = 0; g0 < (whole ? 1 : n); g0 += 32) {
+            const int32_t j = whole ? jf + lane : (cb + min(g0 + lane, n - 1)) / bs;
+            int32_t blk = __shfl_sync(FULL, cur, (j - ww) & 31);
+            int64_t ta, tz;  // this lane's tokens [ta, tz)
+            if (whole) {
+              ta = max((int64_t)cb, (int64_t)j * bs);
+              tz = min((int64_t)cb + n, ((int64_t)j + 1) * bs);
+            } else {
+              ta = cb + g0 + lane;
+              tz = g0 + lane < n ? ta + 1 : ta;
             }
-            const int64_t slot = (int64_t)blk * bs + (ta - j * bs);
-            const uint32_t off = (uint32_t)(ta - cb) * row_b, bytes = (uint32_t)(tz - ta) * row_b;
-            bulk_g2s(kdst + off, kp + slot * pool_row, bytes, fb, pol);
-            bulk_g2s(vdst + off, vp + slot * pool_row, bytes, fb, pol);
+            if (ta < tz) {
+              if (blk < 0 || blk >= p.num_blocks) {
+                set_flag(p.err, NP_FLAG_BLOCK_ID);
+                blk = 0;
+              }
+              const int64_t slot = (int64_t)blk * bs + (ta - j * bs);
+              const uint32_t off = (uint32_t)(ta - cb) * row_b;
+              const uint32_t bytes = (uint32_t)(tz - ta) * row_b;
+              bulk_g2s(kdst + off, kp + slot * pool_row, bytes, fb, pol);
+              bulk_g2s(vdst + off, vp + slot * pool_row, bytes, fb, pol);
+            }
           }
         }
         if (++st == stages) {
@@ -495,10 +574,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     return;
   }
 
-  // ======================= consumer warp hl: its kv head of every segment
-  const int hl = warp;
+  // ======================= consumer warp (hl, tw): kv head hl of every
+  // segment; with TW > 1 warps per head, warp tw takes tokens
+  // [tw*K::CT, (tw+1)*K::CT) of every stage, and the head's warps merge
+  // their states at the end of every segment
+  const int hl = warp % HG, tw = warp / HG;
   const PartialStore keep = PartialStore::make();  // cut-row partials: read by the merge
-  if (vb == ve && tb == te && vb < V) {
+  if (vb == ve && tb == te && vb < V && tw == 0) {
     // an empty range inside row vb: an empty partial (m = -inf, l = 0, o = 0)
     // in slot 0 for the merge of that row
     float* ent = p.ws_o + ((int64_t)b * 2 * HG + hl) * (int64_t)StreamWs::entry_floats(D);
@@ -509,9 +591,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     for (int i = lane; i < kMmaRows * D; i += 32) keep(&ent[2 * kMmaRows + i], 0.f);
   }
   typename K::Warp W;
-  float* tile = tiles + (size_t)hl * K::tile_floats();  // fp32 consumers' scratch
+  float* tile = tiles + (size_t)warp * K::tile_floats();  // fp32 consumers' scratch
   int64_t gch = 0;
   bool first = true;
+  uint32_t seg_phase = 0;  // parity of the row-boundary barriers (TW > 1)
   for (int v = vb; v <= ve && v < V; ++v) {
     int64_t ts, tend;
     seg_bounds(v, ts, tend);
@@ -521,7 +604,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     const int64_t c = len_of(v);
     W.begin(p, r, kvh, c, lane);
     bool ok = true;
-    for (int64_t cb = ts; cb < tend; cb += C::CT, ++gch) {
+    for (int64_t cb = ts; cb < tend; cb += CT, ++gch) {
       const int st = (int)(gch % stages);
       ok = mbar_wait(smem_u32(&full_bar[st]), (uint32_t)((gch / stages) & 1), abort);
       if (!__all_sync(FULL, ok)) {
@@ -529,34 +612,49 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         ok = false;
         break;
       }
-      const int nvalid = (int)min((int64_t)C::CT, tend - cb);
+      // this warp's slice of the stage: tokens [s0, s1)
+      const int nvalid = (int)min((int64_t)CT, tend - cb);
+      const int s0 = tw * C::CT, s1 = min(nvalid, s0 + C::CT);
       if constexpr (K::kTmap) {
         const uint32_t kst = smem_u32(smem + st * stage_bytes);
-        for (int sb = 0; sb < nvalid; sb += C::ST)
-          W.template tile<true>(L, kst, kst + (uint32_t)(stage_bytes / 2), sb, nvalid, cb,
-                                p.qscale, lane);
-      } else {
-        const float* ks = reinterpret_cast<const float*>(smem + st * stage_bytes);
-        W.consume(ks, ks + stage_bytes / 8, hl, HG, nvalid, cb, tile, lane);
+        for (int sb = s0; sb < s1; sb += C::ST)
+          W.template tile<true>(L, kst, kst + (uint32_t)(stage_bytes / 2), sb, s1, cb, p.qscale,
+                                lane);
+      } else if (s0 < s1) {
+        const float* ks = reinterpret_cast<const float*>(smem + st * stage_bytes) +
+                          (size_t)s0 * HG * D;
+        W.consume(ks, ks + stage_bytes / 8, hl, HG, s1 - s0, cb + s0, tile, lane);
       }
       __syncwarp();  // every lane's reads of this stage are done
       if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
     }
     if (!ok) return;
     W.finish();
-
-    if (ts == 0 && tend == c) {  // the whole row is here: normalise and store
-      W.store_out(p, r, kvh, lane);
-      first = false;
-      continue;
-    }
-
-    // ---- a cut row: store the partial for the merge kernel
+    const bool whole = ts == 0 && tend == c;
     const int slot = first ? 0 : 1;
     first = false;
-    const int64_t entry = ((int64_t)b * 2 + slot) * HG + hl;
-    float* ent = p.ws_o + entry * (int64_t)StreamWs::entry_floats(D);
-    W.store_rows(ent, ent + kMmaRows, ent + 2 * kMmaRows, MR, lane, keep);
+    float* ent = p.ws_o + (((int64_t)b * 2 + slot) * HG + hl) * (int64_t)StreamWs::entry_floats(D);
+
+    if (TW == 1) {
+      if (whole) W.store_out(p, r, kvh, lane);  // the whole row is here: normalise and store
+      else W.store_rows(ent, ent + kMmaRows, ent + 2 * kMmaRows, MR, lane, keep);  // cut row
+      continue;
+    }
+    // ---- TW > 1: the head's warps put their states side by side, then each
+    // merges a share of the rows (in tw order) and stores them or their
+    // partials.
+    // Bounded waits: a timed-out pipeline returns instead of waiting here.
+    float* my = wstate + (size_t)warp * StreamWs::entry_floats(D);
+    W.store_rows(my, my + kMmaRows, my + 2 * kMmaRows, MR, lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&seg_bar[0]));
+    if (!__all_sync(FULL, mbar_wait(smem_u32(&seg_bar[0]), seg_phase, abort))) return;
+    merge_warp_states<T, D>(p, wstate, hl, HG, TW, tw, MR, Gr, r, kvh, whole, ent, keep, lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&seg_bar[1]));
+    // the next boundary's states go to the same place: wait until merged
+    if (!__all_sync(FULL, mbar_wait(smem_u32(&seg_bar[1]), seg_phase, abort))) return;
+    seg_phase ^= 1u;
   }
 }
 

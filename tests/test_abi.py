@@ -81,8 +81,9 @@ def test_decode_validation(lib):
     assert _decode(lib, dtype=7, **ok_ptrs) == 2       # dtype
     assert _decode(lib, scale=float("nan"), **ok_ptrs) == 1
     assert _decode(lib, splits=-1, **ok_ptrs) == 1
-    assert _decode(lib, splits=0, **ok_ptrs) == 2            # balanced read: kv heads % 4
-    assert _decode(lib, splits=0, dtype=1, hk=6, hq=12, **ok_ptrs) == 2  # kv heads % 4
+    assert _decode(lib, splits=0, **ok_ptrs) == 3            # balanced read: needs workspace
+    assert _decode(lib, splits=0, dtype=1, hk=6, hq=12, **ok_ptrs) == 3  # any kv heads
+    assert _decode(lib, splits=0, dtype=1, hk=1, hq=8, bs=4, **ok_ptrs) == 2  # box x heads % 8
     assert _decode(lib, splits=0, dtype=1, hk=4, hq=8, bs=3, **ok_ptrs) == 2  # bf16 4 heads: odd bs
     assert _decode(lib, splits=0, dtype=1, hk=4, hq=8, nb=16, **ok_ptrs) == 3  # no workspace
     assert _decode(lib, splits=0, dtype=1, hk=8, hq=16, nb=16, **ok_ptrs) == 3  # no workspace
@@ -186,14 +187,18 @@ def test_plan_is_static_and_sane(lib):
         s = npg.np_paged_decode_plan(w.rows, w.q_heads, w.kv_heads, w.head_dim, w.block_size,
                                      w.max_blocks_per_row, w.torch_dtype, num_sms=152)
         cap = w.max_blocks_per_row * w.block_size
-        if s == 0:  # the balanced read: kv heads % 4, head_dim % 64 (bf16) or % 32 (fp32)
-            assert w.kv_heads % 4 == 0 and w.head_dim <= 256
+        if s == 0:  # the balanced read: head_dim % 64 (bf16) or % 32 (fp32), <= 256
+            assert w.head_dim <= 256
             assert w.head_dim % (64 if w.dtype == "bf16" else 32) == 0
             continue
         sl = npg.np_paged_decode_split_len(w.block_size, w.max_blocks_per_row, s)
         assert s >= 1 and sl * s >= cap
         if s > 1:  # each split reads at least 64 tokens' worth of every head group
             assert sl >= 64
+    for name in ("bf16-mqa", "bf16-kv2", "llama-fp32-kv16"):  # any kv head count
+        w = wl.WORKLOADS[name]
+        assert npg.np_paged_decode_plan(w.rows, w.q_heads, w.kv_heads, w.head_dim, w.block_size,
+                                        w.max_blocks_per_row, w.torch_dtype, num_sms=152) == 0
     # same shapes, same plan (no hidden state)
     a = npg.np_paged_decode_plan(16, 64, 8, 128, 32, 4096, "bf16", num_sms=152)
     assert a == npg.np_paged_decode_plan(16, 64, 8, 128, 32, 4096, "bf16", num_sms=152)

@@ -28,8 +28,12 @@ def _draw(i: int):
     block_size = rnd.choice([1, 3, 8, 16, 24, 32, 64])
     rows = rnd.randint(1, 12)
     # several query tokens: (query token, head) rows g*Q <= 16 on bf16, <= 8 on fp32
-    balanced_ok = (kv_heads % 4 == 0 and head_dim % (64 if dtype == "bf16" else 32) == 0
-                   and (dtype == "f32" or kv_heads % 8 == 0 or block_size % 2 == 0))
+    hg = max(d for d in range(1, 9) if kv_heads % d == 0)  # kv heads per CTA
+    bt = 1  # bf16 TMA box tokens: the largest power of two dividing the block, <= 16
+    while bt < (8 if head_dim >= 256 else 16) and block_size % (2 * bt) == 0:
+        bt *= 2
+    balanced_ok = (head_dim % (64 if dtype == "bf16" else 32) == 0
+                   and (dtype == "f32" or (bt * hg) % 8 == 0))
     q_max = (16 if dtype == "bf16" else 8) // group
     query_len = rnd.choice([1, 1, 1, max(1, min(q_max, rnd.randint(2, 5)))])
     budget = 60_000 // (kv_heads * max(head_dim, 32))  # keeps the oracle fast

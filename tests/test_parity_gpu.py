@@ -260,8 +260,7 @@ def test_any_group_on_bf16(nplib, group, kv_heads, query_len):
     ctx = [max(c, query_len) if c else 0 for c in ctx]
     w = _custom(ctx, kv_heads * group, kv_heads, 128, 16, "bf16",
                 seed=300 + group * 7 + kv_heads + query_len, query_len=query_len)
-    if kv_heads % 4 == 0:
-        _full_parity(nplib, w, num_splits=0)
+    _full_parity(nplib, w, num_splits=0)
     _full_parity(nplib, w, num_splits=1)
     _full_parity(nplib, w, num_splits=3, fused=False)
 
@@ -278,7 +277,7 @@ def test_other_groups_on_fp32(nplib, group, kv_heads, query_len, head_dim):
     ctx = [max(c, query_len) if c else 0 for c in ctx]
     w = _custom(ctx, kv_heads * group, kv_heads, head_dim, 16, "f32",
                 seed=400 + group * 7 + kv_heads + query_len, query_len=query_len)
-    if kv_heads % 4 == 0 and head_dim % 32 == 0:
+    if head_dim % 32 == 0:
         _full_parity(nplib, w, num_splits=0)
         _full_parity(nplib, w, num_splits=0, fused=False)
     _full_parity(nplib, w, num_splits=1)
@@ -428,11 +427,17 @@ def test_head_dim_256_with_eight_kv_heads(nplib):
     (8, 4, 128, 16, 1), (8, 8, 128, 32, 1), (8, 5, 128, 8, 1), (16, 1, 64, 16, 1),
     (8, 2, 256, 32, 1), (8, 4, 128, 16, 3), (8, 8, 64, 64, 2), (16, 4, 128, 4, 1),
     (4, 4, 128, 16, 1), (4, 8, 128, 32, 2), (12, 2, 64, 8, 1), (4, 5, 256, 2, 1),
-    (20, 1, 128, 16, 4)])
+    (20, 1, 128, 16, 4), (1, 8, 128, 16, 1), (1, 16, 128, 32, 1), (2, 8, 128, 16, 2),
+    (3, 4, 128, 8, 1), (6, 3, 64, 16, 1), (5, 2, 256, 16, 1), (7, 1, 128, 32, 3),
+    (2, 4, 64, 8, 1), (10, 2, 128, 16, 1), (11, 2, 128, 16, 1), (9, 2, 128, 8, 1),
+    (1, 8, 256, 16, 1), (2, 8, 64, 16, 1), (1, 4, 128, 8, 2)])
 def test_balanced_read(nplib, kv_heads, group, head_dim, block_size, query_len):
     """num_splits = 0: one CTA per SM, equal token shares; rows cut between
     CTAs are merged by the second kernel.  Small totals spread over 152
-    CTAs cut most rows, so the merge path is exercised heavily."""
+    CTAs cut most rows, so the merge path is exercised heavily.  Any kv head
+    count: with fewer than 8 heads per CTA several warps read each head,
+    each taking its slice of every stage's tokens, and merge their states at
+    every row end."""
     ctx = [0, 1, 5, 16, 17, 300, 2049, 64, 0, 4000, 31, 7]
     ctx = [max(c, query_len if c else 0) for c in ctx]
     w = _custom(ctx, kv_heads * group, kv_heads, head_dim, block_size, "bf16",
@@ -445,11 +450,13 @@ def test_balanced_read(nplib, kv_heads, group, head_dim, block_size, query_len):
 @pytest.mark.parametrize("kv_heads,group,head_dim,block_size", [
     (8, 4, 128, 16), (8, 1, 128, 32), (8, 2, 64, 8), (8, 8, 32, 3), (8, 5, 256, 16),
     (16, 4, 128, 16), (16, 2, 256, 1), (8, 8, 128, 24), (8, 4, 32, 64),
-    (4, 4, 128, 16), (12, 1, 256, 3), (4, 8, 64, 1)])
+    (4, 4, 128, 16), (12, 1, 256, 3), (4, 8, 64, 1), (1, 8, 128, 16), (2, 4, 128, 3),
+    (3, 2, 64, 16), (6, 1, 256, 8), (5, 8, 32, 1), (11, 2, 128, 16), (13, 1, 32, 16),
+    (1, 8, 256, 16), (2, 4, 64, 1)])
 def test_balanced_read_fp32(nplib, kv_heads, group, head_dim, block_size):
     """fp32 pools on the balanced read (FMA consumers, 1-D bulk copies:
-    whole block runs when the pool has just the CTA's 8 or 4 kv heads, one
-    copy per token otherwise)."""
+    whole block runs when the pool has just the CTA's kv heads, one copy per
+    token otherwise, in rounds of 32 tokens when a stage holds more)."""
     ctx = [0, 1, 5, 16, 17, 300, 2049, 64, 0, 4000, 31, 7]
     w = _custom(ctx, kv_heads * group, kv_heads, head_dim, block_size, "f32",
                 seed=180 + kv_heads + group + head_dim + block_size)

@@ -121,6 +121,24 @@ WORKLOADS: dict[str, Workload] = {
                  description="fp32 decode with 16 kv heads (two 8-head groups per "
                              "row, so one bulk copy per token row), contexts "
                              "U[512, 2048]"),
+        Workload("bf16-mqa", rows=64, q_heads=8, kv_heads=1, head_dim=128,
+                 block_size=16, dtype="bf16", ctx=("uniform", 1024, 8192),
+                 pool=("factor", 1.25), seed=6,
+                 description="bf16 decode with one kv head (a GQA-8 model's per-GPU "
+                             "slice under 8-way tensor parallelism), contexts "
+                             "U[1024, 8192]"),
+        Workload("bf16-kv2", rows=64, q_heads=16, kv_heads=2, head_dim=128,
+                 block_size=16, dtype="bf16", ctx=("uniform", 1024, 8192),
+                 pool=("factor", 1.25), seed=7,
+                 description="bf16 decode with two kv heads (a GQA-8 model's per-GPU "
+                             "slice under 4-way tensor parallelism), contexts "
+                             "U[1024, 8192]"),
+        Workload("bf16-kv4", rows=64, q_heads=32, kv_heads=4, head_dim=128,
+                 block_size=16, dtype="bf16", ctx=("uniform", 1024, 8192),
+                 pool=("factor", 1.25), seed=8,
+                 description="bf16 decode with four kv heads (a GQA-8 model's per-GPU "
+                             "slice under 2-way tensor parallelism), contexts "
+                             "U[1024, 8192]"),
         Workload("bf16-gqa4-q4", rows=64, q_heads=32, kv_heads=8, head_dim=128,
                  block_size=16, dtype="bf16", ctx=("uniform", 1024, 8192),
                  pool=("factor", 1.25), seed=2, query_len=4,
