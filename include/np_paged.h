@@ -195,11 +195,14 @@ size_t np_paged_decode_workspace_bytes(int32_t rows, int32_t q_heads,
  *                  (results are deterministic).  out is written; no reduce
  *                  call.
  *                  Needs head_dim a multiple of 64 (bf16) or 32 (fp32, up
- *                  to 256), kv_heads a multiple of 4 (taken 8 at a time when
- *                  a multiple of 8, else 4; bf16 with groups of 4 also needs
- *                  an even block_size), rows * kv_heads / group <= 4096,
- *                  tables of at most 2^31 - 1 tokens and a workspace (else
- *                  NP_ERR_UNSUPPORTED / NP_ERR_WORKSPACE).
+ *                  to 256); any kv_heads, taken HG at a time (HG = the
+ *                  largest divisor of kv_heads up to 8); for bf16,
+ *                  box_tokens * HG a multiple of 8, where box_tokens is the
+ *                  largest power of two dividing block_size, at most 16 (8
+ *                  at head_dim 256) -- e.g. block_size a multiple of 8 when
+ *                  HG = 1; rows * kv_heads / HG <= 4096, tables of at most
+ *                  2^31 - 1 tokens and a workspace (else NP_ERR_UNSUPPORTED
+ *                  / NP_ERR_WORKSPACE).
  *                  Results equal the split read's up to fp32 rounding order.
  *   workspace      device buffer of >= np_paged_decode_workspace_bytes(...)
  *                  bytes, 256-byte aligned (may be NULL when num_splits == 1)

@@ -1,8 +1,8 @@
-// decode_stream.cuh -- the balanced streamed read (kv heads in groups of 8,
-// or of 4 when the count is not a multiple of 8;
-// bf16 pools with head_dim a multiple of 64 on the tensor cores, through
-// tiled TMA boxes, or fp32 pools with head_dim a multiple of 32 on the FMA
-// pipes, through 1-D bulk copies): the same arithmetic as the split read,
+// decode_stream.cuh -- the balanced streamed read (kv heads in groups of HG,
+// the largest divisor of the count up to 8; bf16 pools with head_dim a
+// multiple of 64 on the tensor cores, through tiled TMA boxes, or fp32 pools
+// with head_dim a multiple of 32 on the FMA pipes, through 1-D bulk
+// copies): the same arithmetic as the split read,
 // with the work laid out so that every SM gets the same number of history
 // tokens and no thread block is launched for nothing.
 //
@@ -35,7 +35,7 @@
 
 namespace npk {
 
-constexpr int kStreamMaxVRows = 4096;  // virtual rows (row, 8-head group) per launch
+constexpr int kStreamMaxVRows = 4096;  // virtual rows (row, kv-head group) per launch
 constexpr int kStreamMaxCtas = 160;    // grid cap, >= the GB300's 152 SMs (the
                                        // workspace is sized for it)
 
@@ -789,7 +789,7 @@ __device__ __forceinline__ void merge_task(const DecodeParams& p, int v, int b0,
 template <typename T, int D, int G, int RPW, int DH>
 __global__ void __launch_bounds__(256 * kMergeRpb) paged_decode_stream_merge_kernel(
     const __grid_constant__ DecodeParams p) {
-  const int HG = p.head_group;  // kv heads per row group: 8 or 4
+  const int HG = p.head_group;  // kv heads per row group
   const int c = blockIdx.x;
   const int P = gridDim.x;  // <= kStreamMaxCtas
   const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
