@@ -132,6 +132,54 @@ __device__ __forceinline__ void fused_append(const DecodeParams& p, int r, int h
   if (wrote) asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// One new token of the fused append, written by a group of `tpt` threads
+// (thread t of the group): row r's token j (position pos), the HG heads of
+// group hgi.  Same rule as fused_append.  The slot, its table entry and the
+// thread's vectors of K and of V (at most kAppendVpl of each: the caller
+// sizes the group so) are loaded together -- one round trip -- so the
+// groups of a CTA append their tokens side by side in about the time of
+// one.  Returns whether the thread stored anything (the caller fences
+// before the barrier that precedes its TMA reads).
+constexpr int kAppendVpl = 4;
+template <int D, int ES>
+__device__ __forceinline__ bool append_token_group(const DecodeParams& p, int r, int hgi, int HG,
+                                                   int64_t pos, int j, int t, int tpt) {
+  const int64_t rq = (int64_t)r * p.query_len + j;
+  const int nvec = HG * D * ES / 16;  // 16-byte vectors of the slice
+  const int64_t src0 = (rq * p.kv_heads + (int64_t)hgi * HG) * D * ES / 16;
+  const uint4* kn = static_cast<const uint4*>(p.k_new);
+  const uint4* vn = static_cast<const uint4*>(p.v_new);
+  uint4 kr[kAppendVpl], vr[kAppendVpl];
+#pragma unroll
+  for (int e = 0; e < kAppendVpl; ++e) {
+    const int i = t + tpt * e;
+    if (i < nvec) {
+      kr[e] = kn[src0 + i];
+      vr[e] = vn[src0 + i];
+    }
+  }
+  const int64_t bs = p.block_size;
+  const int64_t s = p.slot_mapping[rq];
+  const int64_t b = p.block_tables[(int64_t)r * p.max_blocks_per_row + pos / bs];
+  if (s < 0) return false;
+  if (b < 0 || b >= p.num_blocks || s != b * bs + pos % bs) {
+    if (t == 0) set_flag(p.err, NP_FLAG_SLOT);
+    return false;
+  }
+  const int64_t dst0 = (s * p.kv_heads + (int64_t)hgi * HG) * D * ES / 16;
+  uint4* kd = static_cast<uint4*>(const_cast<void*>(p.k_pool));
+  uint4* vd = static_cast<uint4*>(const_cast<void*>(p.v_pool));
+#pragma unroll
+  for (int e = 0; e < kAppendVpl; ++e) {
+    const int i = t + tpt * e;
+    if (i < nvec) {
+      kd[dst0 + i] = kr[e];
+      vd[dst0 + i] = vr[e];
+    }
+  }
+  return t < nvec;
+}
+
 #ifndef NPK_MMA_CT
 #define NPK_MMA_CT 16  // tokens per pipeline stage for 64 <= head_dim < 256
 #endif

@@ -367,11 +367,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     return;
   }
 
-  // Warps 0..7 write the zero rows and the fused append while the producer
-  // starts on the history; they signal named barrier 1 (after
-  // fence.proxy.async, so the appended rows are visible to TMA) and the
-  // producer waits on it before the first chunk that holds a new token.
-  // Warps HG..7 (when HG = 4) have no kv head and leave after that.
+  // Warps 0..7 write the zero rows and the fused append (new tokens side by
+  // side, one per group of warps) while the producer starts on the history;
+  // they signal
+  // named barrier 1 (after fence.proxy.async, so the appended rows are
+  // visible to TMA) and the producer waits on it before the first chunk that
+  // holds a new token.  Warps NCW..7 (HG * TW < 8) have no kv head and leave
+  // after that.
   constexpr int kAppendBar = 1;
   if (warp < kProducer) {
     const int tid = threadIdx.x, nthr = 32 * kProducer;
@@ -383,11 +385,30 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         for (int i = tid; i < HG * Gr * D; i += nthr) o[i] = T(0.f);
       }
     }
-    for (int v = vb; v <= ve && v < V; ++v) {  // the new tokens of this CTA's segments
-      int64_t ts, tend;
-      seg_bounds(v, ts, tend);
-      if (ts < tend)
-        fused_append<D, (int)sizeof(T)>(p, v % R, v / R, HG, len_of(v), ts, tend, tid, nthr);
+    if (p.slot_mapping != nullptr) {
+      // the new tokens whose positions lie in this CTA's segments, one per
+      // group of GW warps in turn (token k of the walk goes to group k % NG;
+      // GW: enough warps that no thread copies more than kAppendVpl vectors)
+      const int nvec = HG * D * (int)sizeof(T) / 16;
+      const int GW = nvec <= 32 * kAppendVpl ? 1 : nvec <= 64 * kAppendVpl ? 2
+                   : nvec <= 128 * kAppendVpl ? 4 : 8;
+      const int NG = kProducer / GW;
+      const int grp = warp / GW, t = (warp % GW) * 32 + lane;
+      bool wrote = false;
+      int k = 0;
+      for (int v = vb; v <= ve && v < V; ++v) {
+        int64_t ts, tend;
+        seg_bounds(v, ts, tend);
+        const int64_t c = len_of(v);
+        for (int j = 0; j < Q; ++j) {
+          const int64_t pos = c - Q + j;
+          if (pos < 0 || pos < ts || pos >= tend) continue;
+          if (k++ % NG == grp)
+            wrote |= append_token_group<D, (int)sizeof(T)>(p, v % R, v / R, HG, pos, j, t,
+                                                           32 * GW);
+        }
+      }
+      if (wrote) asm volatile("fence.proxy.async.global;" ::: "memory");
     }
     asm volatile("bar.arrive %0, %1;" ::"r"(kAppendBar), "r"(blockDim.x) : "memory");
     if (threadIdx.x == 0) {
