@@ -153,6 +153,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return fn;
 }
 
+// L2 promotion of the pool maps' requests (CUtensorMapL2promotion).
+#ifndef NPK_TMAP_L2_PROMO
+#define NPK_TMAP_L2_PROMO CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+#endif
+
 // Map of one pool as a 4-D tensor (64 dims, slot, kv head, 64-dim slab):
 // the dimensions are listed in the order a box lands in shared memory, not
 // by stride, so that one box {64, box_tokens, head_group, head_dim/64}
@@ -171,7 +176,7 @@ bool encode_pool_map(CUtensorMap* m, const void* pool, int64_t slots, int32_t kv
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   CUresult rc = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    NPK_TMAP_L2_PROMO, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return rc == CUDA_SUCCESS;
 }
 
