@@ -394,6 +394,19 @@ def test_multi_query_tokens_fp32(nplib, group, query_len, head_dim):
     _full_parity(nplib, w, num_splits=0, fused=False)
 
 
+@pytest.mark.parametrize("kv_heads,group,query_len,head_dim", [
+    (1, 2, 3, 128), (2, 1, 5, 64), (3, 2, 4, 32), (11, 1, 3, 128)])
+def test_multi_query_tokens_fp32_small_head_groups(nplib, kv_heads, group, query_len, head_dim):
+    """fp32, several query tokens, head groups under 8 on the balanced read:
+    several FMA warps per kv head, each on its slice of every stage (one
+    head of 11: one copy per token, in rounds of 32 tokens)."""
+    ctx = [1, query_len, query_len + 1, 63, 64, 65, 700, 1500, 0]
+    w = _custom(ctx, kv_heads * group, kv_heads, head_dim, 16, "f32",
+                seed=240 + kv_heads * 5 + group + query_len, query_len=query_len)
+    _full_parity(nplib, w, num_splits=0)
+    _full_parity(nplib, w, num_splits=0, fused=False)
+
+
 @pytest.mark.parametrize("group,kv_heads,query_len,head_dim", [
     (2, 8, 2, 128), (1, 2, 5, 64), (4, 2, 2, 128), (2, 3, 3, 32), (1, 1, 8, 16)])
 def test_multi_query_fp32_split_grid(nplib, group, kv_heads, query_len, head_dim):
