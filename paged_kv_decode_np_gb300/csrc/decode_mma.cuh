@@ -240,7 +240,9 @@ struct MmaWarp {
   // 2*(lane%4) (+1) in oA, 8 + 2*(lane%4) (+1) in oB
   float oA[KS][4];
   float oB[TWO ? KS : 1][4];
-  int64_t limA, limB;  // last position each row may see (-1: a padding row)
+  // last position each row may see (-1: a padding row); positions fit int32
+  // (context_lens are int32)
+  int32_t limA, limB;
   int gr;              // query heads per kv head (G, or q_heads/kv_heads when G = 0)
 
   // q of row r, kv head kvh: mma row qi*G + h is query token qi, head
@@ -256,8 +258,8 @@ struct MmaWarp {
              ((r * Q + qi) * p.q_heads + kvh * gr + h) * D;
     };
     const bool liveA = g4 < MR, liveB = g4 + 8 < MR;
-    limA = liveA ? c - Q + g4 / gr : -1;
-    limB = liveB ? c - Q + (g4 + 8) / gr : -1;
+    limA = liveA ? (int32_t)(c - Q + g4 / gr) : -1;
+    limB = liveB ? (int32_t)(c - Q + (g4 + 8) / gr) : -1;
     const __nv_bfloat16* qa = liveA ? qrow(g4) : nullptr;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
@@ -316,14 +318,16 @@ struct MmaWarp {
     }
     // ---- masks: token (tile-local) 2*c4 + {0, 1, 8, 9} must be a valid
     // token of the chunk and at or before the row's own position
+    // (limits relative to the chunk's first position: no overflow, as
+    // 0 <= tch <= INT32_MAX and lim >= -1)
     const int lt = sb + 2 * c4;
-    const int64_t pos = tch + lt;
+    const int32_t relA = limA - (int32_t)tch;
     const bool v0 = lt < nvalid, v1 = lt + 1 < nvalid, v8 = lt + 8 < nvalid, v9 = lt + 9 < nvalid;
     float sa[4] = {s0[0] * qscale, s0[1] * qscale, s1[0] * qscale, s1[1] * qscale};
-    if (!(v0 && pos <= limA)) sa[0] = -INFINITY;
-    if (!(v1 && pos + 1 <= limA)) sa[1] = -INFINITY;
-    if (!(v8 && pos + 8 <= limA)) sa[2] = -INFINITY;
-    if (!(v9 && pos + 9 <= limA)) sa[3] = -INFINITY;
+    if (!(v0 && lt <= relA)) sa[0] = -INFINITY;
+    if (!(v1 && lt + 1 <= relA)) sa[1] = -INFINITY;
+    if (!(v8 && lt + 8 <= relA)) sa[2] = -INFINITY;
+    if (!(v9 && lt + 9 <= relA)) sa[3] = -INFINITY;
     const float alphaA = softmax_row(sa, mA, lA);
     const uint32_t pa0 = pack_bf16(sa[0], sa[1]);
     const uint32_t pa1 = pack_bf16(sa[2], sa[3]);
@@ -331,10 +335,11 @@ struct MmaWarp {
     uint32_t pb0 = 0u, pb1 = 0u;
     if constexpr (TWO) {
       float sbv[4] = {s0[2] * qscale, s0[3] * qscale, s1[2] * qscale, s1[3] * qscale};
-      if (!(v0 && pos <= limB)) sbv[0] = -INFINITY;
-      if (!(v1 && pos + 1 <= limB)) sbv[1] = -INFINITY;
-      if (!(v8 && pos + 8 <= limB)) sbv[2] = -INFINITY;
-      if (!(v9 && pos + 9 <= limB)) sbv[3] = -INFINITY;
+      const int32_t relB = limB - (int32_t)tch;
+      if (!(v0 && lt <= relB)) sbv[0] = -INFINITY;
+      if (!(v1 && lt + 1 <= relB)) sbv[1] = -INFINITY;
+      if (!(v8 && lt + 8 <= relB)) sbv[2] = -INFINITY;
+      if (!(v9 && lt + 9 <= relB)) sbv[3] = -INFINITY;
       alphaB = softmax_row(sbv, mB, lB);
       pb0 = pack_bf16(sbv[0], sbv[1]);
       pb1 = pack_bf16(sbv[2], sbv[3]);
@@ -648,9 +653,10 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
     // ======================= consumer warp: kv head hl, chunks tw, tw+TW, ...
     const int tw = warp / HG;
     W.begin(p, r, hgi * HG + L.hl, c, lane);
+    int st = tw % stages;                 // stage of chunk ch, and the parity of
+    uint32_t fph = (tw / stages) & 1u;    // its full barrier's phase, kept incrementally
     for (int64_t ch = tw; ch < nch; ch += TW) {
-      const int st = (int)(ch % stages);
-      bool ok = mbar_wait(smem_u32(&full_bar[st]), (uint32_t)((ch / stages) & 1), abort);
+      bool ok = mbar_wait(smem_u32(&full_bar[st]), fph, abort);
       if (!__all_sync(FULL, ok)) {
         set_flag(p.err, NP_FLAG_TIMEOUT);
         break;
@@ -663,6 +669,7 @@ __global__ void __launch_bounds__(kMaxThreads, NPK_MMA_MIN_BLOCKS)
                               p.qscale, lane);
       __syncwarp();  // every lane's reads of this stage are done
       if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
+      for (st += TW; st >= stages; st -= stages) fph ^= 1u;
     }
     W.finish();
   }

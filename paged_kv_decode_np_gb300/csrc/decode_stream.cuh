@@ -613,7 +613,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   }
   typename K::Warp W;
   float* tile = tiles + (size_t)warp * K::tile_floats();  // fp32 consumers' scratch
-  int64_t gch = 0;
+  int st = 0;          // the next stage, and
+  uint32_t fph = 0;    // the parity of its full barrier's phase (flips at every wrap)
   bool first = true;
   uint32_t seg_phase = 0;  // parity of the row-boundary barriers (TW > 1)
   for (int v = vb; v <= ve && v < V; ++v) {
@@ -625,9 +626,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     const int64_t c = len_of(v);
     W.begin(p, r, kvh, c, lane);
     bool ok = true;
-    for (int64_t cb = ts; cb < tend; cb += CT, ++gch) {
-      const int st = (int)(gch % stages);
-      ok = mbar_wait(smem_u32(&full_bar[st]), (uint32_t)((gch / stages) & 1), abort);
+    for (int64_t cb = ts; cb < tend; cb += CT) {
+      ok = mbar_wait(smem_u32(&full_bar[st]), fph, abort);
       if (!__all_sync(FULL, ok)) {
         set_flag(p.err, NP_FLAG_TIMEOUT);
         ok = false;
@@ -648,6 +648,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       }
       __syncwarp();  // every lane's reads of this stage are done
       if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
+      if (++st == stages) {
+        st = 0;
+        fph ^= 1u;
+      }
     }
     if (!ok) return;
     W.finish();
