@@ -82,6 +82,10 @@ np_status launch_variant(DecodeLaunch& L, DecodeParams& p) {
 
 #if (NPK_BF16 && NPK_D % 64 == 0) || (!NPK_BF16 && NPK_D % 32 == 0)
 #define NPK_HAS_STREAM 1
+#ifndef NPK_MERGE_RPW4
+#define NPK_MERGE_RPW4 1
+#endif
+
 // The balanced streamed read: grid = L.splits CTAs (one per SM), 8 kv heads
 // per CTA, the virtual-row prefix in shared memory after the ring.
 template <int G, bool TWO>
@@ -133,13 +137,26 @@ np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
   attr[0].val.programmaticStreamSerializationAllowed = NPK_STREAM_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // Merge tasks: two mma rows each when a row group has 16; half the
-  // head_dim each when the rows are likely cut into more than 16 pieces
-  // (more CTAs than 16 per virtual row), so that one round of loads covers
-  // a row's partials.
+  // Merge tasks: two mma rows each when a row group has 16 (four when the
+  // cut rows' tasks would otherwise outnumber the merge's warps and a row is
+  // cut into at most ~4 pieces, one batch of 4 partials); half the head_dim
+  // each when the rows are likely cut into more than 16 pieces (more CTAs
+  // than 16 per virtual row), so that one round of loads covers a row's
+  // partials.
   const int mr = L.group * p.query_len;
   cudaError_t rc = cudaErrorInvalidValue;
   bool done = false;
+#if NPK_MERGE_RPW4
+  if (mr >= 16) {
+    const int64_t cut_rows = vrows < L.splits ? vrows : L.splits;
+    const int64_t tasks2 = cut_rows * (mr / 2) * hg;
+    const int64_t warps = (int64_t)L.splits * (256 * kMergeRpb / 32);
+    if (tasks2 > warps && L.splits <= 3 * vrows) {
+      rc = cudaLaunchKernelEx(&cfg, paged_decode_stream_merge_kernel<StorageT, NPK_D, G, 4, 1>, p);
+      done = true;
+    }
+  }
+#endif
   if constexpr (NPK_D >= 64 && NPK_MERGE_DH2) {
     if (mr < 16 && 16 * vrows < L.splits) {
       rc = cudaLaunchKernelEx(&cfg, paged_decode_stream_merge_kernel<StorageT, NPK_D, G, 1, 2>, p);
