@@ -50,13 +50,11 @@
  *   - Pools: k_pool and v_pool are separate arrays, each
  *     [num_blocks, block_size, kv_heads, head_dim] of `dtype`.
  *   - Supported: dtype NP_F32 or NP_BF16; head_dim in {16, 32, 64, 128, 256};
- *     group g = q_heads/kv_heads in {1, 2, 4, 5, 8} on fp32 pools (any g up
- *     to 8 through the balanced read, num_splits == 0), any g from 1 to 16
- *     on bf16 pools; any block_size >= 1;
- *     any kv_heads >= 1; query_len 1, or any query_len with g * query_len
- *     <= 16 on bf16 pools, or <= 8 on fp32 pools through the balanced read
- *     (num_splits == 0).  Arithmetic is fp32 in every case (bf16 is widened
- *     exactly); q and out have the pool dtype.
+ *     group g = q_heads/kv_heads from 1 to 8 on fp32 pools, from 1 to 16 on
+ *     bf16 pools; any block_size >= 1; any kv_heads >= 1; query_len 1, or
+ *     any query_len with g * query_len <= 16 on bf16 pools, <= 8 on fp32
+ *     pools, on every schedule.  Arithmetic is fp32 in every case (bf16 is
+ *     widened exactly); q and out have the pool dtype.
  *   - Several query tokens per row (query_len Q > 1, speculative or chunked
  *     decode): the row's Q query tokens are its last Q positions
  *     c - Q .. c - 1 (c = context_lens[r], counting them); query token i
