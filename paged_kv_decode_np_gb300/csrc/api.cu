@@ -112,6 +112,23 @@ int stream_token_warps(np_dtype dtype, int32_t head_dim, int hg, int32_t block_s
   return tw;
 }
 
+// K::CT-token pieces each consumer warp takes per stage (SL): with fewer than
+// 8 consumer warps (HG * TW < 8, e.g. four kv heads with one warp each) a
+// stage holds 8 / (HG * TW) pieces per warp, so that it still moves about
+// 64 KB per producer iteration; SL * TW * ct0 divides 32 * block_size.
+// Built with NPK_STREAM_SLICES=0: one piece.
+#ifndef NPK_STREAM_SLICES
+#define NPK_STREAM_SLICES 1
+#endif
+int stream_stage_slices(np_dtype dtype, int32_t head_dim, int hg, int tw, int32_t block_size) {
+  if (!NPK_STREAM_SLICES) return 1;
+  const int ct0 = stream_chunk_tokens(dtype, head_dim);
+  int sl = npk::kMaxConsumerWarps / (hg * tw);
+  if (sl < 1) sl = 1;
+  while (sl > 1 && ((int64_t)32 * block_size) % ((int64_t)ct0 * tw * sl) != 0) --sl;
+  return sl;
+}
+
 // Tokens per tiled TMA box of the bf16 read: the largest power of two that
 // divides the block size, at most a stage's tokens.
 int box_tokens_for(int32_t block_size, int32_t head_dim) {
@@ -435,6 +452,8 @@ np_status decode_impl(void* out, const void* q, const void* k_pool, const void* 
   p.head_group = hg;
   p.token_warps =
       streamed ? stream_token_warps(dtype, head_dim, hg, block_size) : npk::kMaxConsumerWarps / hg;
+  p.stage_slices =
+      streamed ? stream_stage_slices(dtype, head_dim, hg, p.token_warps, block_size) : 1;
   p.max_blocks_per_row = max_blocks_per_row;
   p.q_heads = q_heads;
   p.num_splits = num_splits;

@@ -101,17 +101,18 @@ np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
   // fewer tokens still divides the block table's 32-block windows)
   size_t stages = 0;
   int tw = p.token_warps;
+  const int sl = p.stage_slices;  // K::CT-token pieces per warp and stage
   for (;;) {
-    const size_t sb = SS::stage_bytes(hg, tw);
+    const size_t sb = SS::stage_bytes(hg, tw * sl);
     stages = (196608 / sb) < 2 ? 2 : (196608 / sb) > 32 ? 32 : 196608 / sb;
-    while (stages >= 2 && SS::total(hg, tw, (int)stages, vrows) > budget) --stages;
+    while (stages >= 2 && SS::total(hg, tw * sl, (int)stages, vrows, tw) > budget) --stages;
     if (stages >= 2 || tw == 1) break;
     tw = tw % 2 == 0 ? tw / 2 : 1;
   }
   if (stages < 2) return NP_ERR_UNSUPPORTED;
   p.token_warps = tw;
   L.token_warps = tw;
-  const size_t smem = SS::total(hg, tw, (int)stages, vrows);
+  const size_t smem = SS::total(hg, tw * sl, (int)stages, vrows, tw);
   p.stages = (int)stages;
   L.stages = (int)stages;
   L.smem_bytes = smem;

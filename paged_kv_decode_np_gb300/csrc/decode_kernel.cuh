@@ -54,6 +54,7 @@ struct DecodeParams {
   int32_t kv_heads;
   int32_t head_group;    // HG: kv heads per CTA (divides kv_heads)
   int32_t token_warps;   // TW: consumer warps per kv head
+  int32_t stage_slices;  // balanced read: K::CT-token pieces per warp and stage (SL)
   int32_t max_blocks_per_row;
   int32_t q_heads;
   int32_t num_splits;

@@ -124,28 +124,31 @@ struct StreamKind<float, D, G, MQ> {  // FMA pipes, 1-D bulk copies of token row
 // Shared memory: ring (1024-aligned) | full, empty barriers | abort |
 // virtual rows' chunk prefix (int64, V + 1) | their lengths (int32, V) |
 // consumer tiles (16-aligned) | the token warps' states (tw > 1).  hg = kv
-// heads per CTA, tw = consumer warps per kv head: a stage holds tw * K::CT
-// tokens, K::CT for each of a head's warps.
+// heads per CTA, tw = consumer warps per kv head times the pieces of K::CT
+// tokens each of them takes per stage: a stage holds tw * K::CT tokens.
 template <typename T, int D, int G, bool TWO>
 struct StreamSmem {
   using K = StreamKind<T, D, G, TWO>;
-  __host__ __device__ static constexpr size_t stage_bytes(int hg, int tw) {
-    return K::stage_bytes(hg) * tw;
+  // sm: K::CT-token pieces per kv head in a stage (consumer warps per head
+  // times the pieces each takes)
+  __host__ __device__ static constexpr size_t stage_bytes(int hg, int sm) {
+    return K::stage_bytes(hg) * sm;
   }
-  __host__ __device__ static constexpr size_t lens_offset(int hg, int tw, int stages, int vrows) {
-    return stage_bytes(hg, tw) * stages + 16ull * stages + 16 + (size_t)(vrows + 1) * 8;
+  __host__ __device__ static constexpr size_t lens_offset(int hg, int sm, int stages, int vrows) {
+    return stage_bytes(hg, sm) * stages + 16ull * stages + 16 + (size_t)(vrows + 1) * 8;
   }
-  __host__ __device__ static constexpr size_t tiles_offset(int hg, int tw, int stages, int vrows) {
-    return (lens_offset(hg, tw, stages, vrows) + (size_t)vrows * 4 + 15) / 16 * 16;
+  __host__ __device__ static constexpr size_t tiles_offset(int hg, int sm, int stages, int vrows) {
+    return (lens_offset(hg, sm, stages, vrows) + (size_t)vrows * 4 + 15) / 16 * 16;
   }
   // several consumer warps per kv head (tw > 1): their (m, l, O) rows at a
   // row boundary, one entry per warp
-  __host__ __device__ static constexpr size_t merge_offset(int hg, int tw, int stages, int vrows) {
-    return (tiles_offset(hg, tw, stages, vrows) + 8 * K::tile_floats() * sizeof(float) + 15) /
+  __host__ __device__ static constexpr size_t merge_offset(int hg, int sm, int stages, int vrows) {
+    return (tiles_offset(hg, sm, stages, vrows) + 8 * K::tile_floats() * sizeof(float) + 15) /
            16 * 16;
   }
-  __host__ __device__ static constexpr size_t total(int hg, int tw, int stages, int vrows) {
-    return 1024 + merge_offset(hg, tw, stages, vrows) +
+  __host__ __device__ static constexpr size_t total(int hg, int sm, int stages, int vrows,
+                                                    int tw) {
+    return 1024 + merge_offset(hg, sm, stages, vrows) +
            (tw > 1 ? (size_t)kMaxConsumerWarps * StreamWs::entry_floats(D) * sizeof(float) : 0) +
            (tw > 1 ? 16 : 0);  // + the merge's two mbarriers
   }
@@ -233,20 +236,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int stages = p.stages;
-  // a stage: CT = K::CT tokens for each of a head's TW consumer warps
-  const int CT = C::CT * TW;
-  const size_t stage_bytes = StreamSmem<T, D, G, TWO>::stage_bytes(HG, TW);
+  // a stage: WS = SL * K::CT tokens for each of a head's TW consumer warps
+  const int WS = C::CT * p.stage_slices;
+  const int CT = WS * TW;
+  using SS = StreamSmem<T, D, G, TWO>;
+  const int SM = TW * p.stage_slices;  // K::CT-token pieces per kv head in a stage
+  const size_t stage_bytes = SS::stage_bytes(HG, SM);
   const size_t ring = stage_bytes * stages;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + ring);
   uint64_t* empty_bar = full_bar + stages;
   volatile int* abort = reinterpret_cast<volatile int*>(empty_bar + stages);
   int64_t* pre = reinterpret_cast<int64_t*>(smem + ring + 16ull * stages + 16);
-  int32_t* lens =
-      reinterpret_cast<int32_t*>(smem + StreamSmem<T, D, G, TWO>::lens_offset(HG, TW, stages, V));
-  float* tiles =
-      reinterpret_cast<float*>(smem + StreamSmem<T, D, G, TWO>::tiles_offset(HG, TW, stages, V));
+  int32_t* lens = reinterpret_cast<int32_t*>(smem + SS::lens_offset(HG, SM, stages, V));
+  float* tiles = reinterpret_cast<float*>(smem + SS::tiles_offset(HG, SM, stages, V));
   float* wstate =  // TW > 1: the consumer warps' states at a row boundary
-      reinterpret_cast<float*>(smem + StreamSmem<T, D, G, TWO>::merge_offset(HG, TW, stages, V));
+      reinterpret_cast<float*>(smem + SS::merge_offset(HG, SM, stages, V));
   uint64_t* seg_bar = reinterpret_cast<uint64_t*>(wstate + kMaxConsumerWarps *
                                                              StreamWs::entry_floats(D));
   __shared__ int64_t wsum[32];
@@ -596,9 +600,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   }
 
   // ======================= consumer warp (hl, tw): kv head hl of every
-  // segment; with TW > 1 warps per head, warp tw takes tokens
-  // [tw*K::CT, (tw+1)*K::CT) of every stage, and the head's warps merge
-  // their states at the end of every segment
+  // segment; warp tw takes tokens [tw*WS, (tw+1)*WS) of every stage (WS =
+  // SL pieces of K::CT tokens), and with TW > 1 warps per head the head's
+  // warps merge their states at the end of every segment
   const int hl = warp % HG, tw = warp / HG;
   const PartialStore keep = PartialStore::make();  // cut-row partials: read by the merge
   if (vb == ve && tb == te && vb < V && tw == 0) {
@@ -635,16 +639,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       }
       // this warp's slice of the stage: tokens [s0, s1)
       const int nvalid = (int)min((int64_t)CT, tend - cb);
-      const int s0 = tw * C::CT, s1 = min(nvalid, s0 + C::CT);
+      const int s0 = tw * WS, s1 = min(nvalid, s0 + WS);
       if constexpr (K::kTmap) {
         const uint32_t kst = smem_u32(smem + st * stage_bytes);
         for (int sb = s0; sb < s1; sb += C::ST)
           W.template tile<true>(L, kst, kst + (uint32_t)(stage_bytes / 2), sb, s1, cb, p.qscale,
                                 lane);
-      } else if (s0 < s1) {
-        const float* ks = reinterpret_cast<const float*>(smem + st * stage_bytes) +
-                          (size_t)s0 * HG * D;
-        W.consume(ks, ks + stage_bytes / 8, hl, HG, s1 - s0, cb + s0, tile, lane);
+      } else {
+        const float* ks = reinterpret_cast<const float*>(smem + st * stage_bytes);
+        for (int k0 = s0; k0 < s1; k0 += C::CT)
+          W.consume(ks + (size_t)k0 * HG * D, ks + stage_bytes / 8 + (size_t)k0 * HG * D, hl, HG,
+                    min(s1 - k0, C::CT), cb + k0, tile, lane);
       }
       __syncwarp();  // every lane's reads of this stage are done
       if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
