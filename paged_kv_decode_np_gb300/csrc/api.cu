@@ -100,13 +100,18 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 #ifndef NPK_STREAM_TWMAX
 #define NPK_STREAM_TWMAX 8
 #endif
+// One- and two-head groups: four consumer warps (two pieces of each stage
+// apiece), so that their row-end states leave room for three 64 KB stages.
+#ifndef NPK_STREAM_NCW4
+#define NPK_STREAM_NCW4 1
+#endif
 int stream_chunk_tokens(np_dtype dtype, int32_t head_dim) {
   return dtype == NP_BF16 ? npk::mma_chunk_tokens(head_dim) : 1024 / head_dim;
 }
 int stream_token_warps(np_dtype dtype, int32_t head_dim, int hg, int32_t block_size) {
   if (hg == 4 && !NPK_STREAM_TW4) return 1;
   const int ct0 = stream_chunk_tokens(dtype, head_dim);
-  int tw = npk::kMaxConsumerWarps / hg;
+  int tw = (NPK_STREAM_NCW4 && hg <= 2 ? 4 : npk::kMaxConsumerWarps) / hg;
   if (tw > NPK_STREAM_TWMAX) tw = NPK_STREAM_TWMAX;
   while (tw > 1 && ((int64_t)32 * block_size) % ((int64_t)ct0 * tw) != 0) --tw;
   return tw;

@@ -102,29 +102,35 @@ np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
   size_t stages = 0;
   int tw = p.token_warps;
   const int sl = p.stage_slices;  // K::CT-token pieces per warp and stage
+  const int mr = L.group * p.query_len;  // (query token, head) rows per kv head
   for (;;) {
     const size_t sb = SS::stage_bytes(hg, tw * sl);
     stages = (196608 / sb) < 2 ? 2 : (196608 / sb) > 32 ? 32 : 196608 / sb;
-    while (stages >= 2 && SS::total(hg, tw * sl, (int)stages, vrows, tw) > budget) --stages;
+    while (stages >= 2 && SS::total(hg, tw * sl, (int)stages, vrows, tw, hg * tw, mr) > budget)
+      --stages;
     if (stages >= 2 || tw == 1) break;
     tw = tw % 2 == 0 ? tw / 2 : 1;
   }
   if (stages < 2) return NP_ERR_UNSUPPORTED;
   p.token_warps = tw;
   L.token_warps = tw;
-  const size_t smem = SS::total(hg, tw * sl, (int)stages, vrows, tw);
+  const size_t smem = SS::total(hg, tw * sl, (int)stages, vrows, tw, hg * tw, mr);
   p.stages = (int)stages;
   L.stages = (int)stages;
   L.smem_bytes = smem;
-  auto kern = paged_decode_stream_kernel<StorageT, NPK_D, G, TWO>;
-  static unsigned long long configured = 0;  // bit d: attribute set on device d
+  // several warps per kv head: the build with their row-end merges
+  const int multi = tw > 1 ? 1 : 0;
+  auto kern = multi ? paged_decode_stream_kernel<StorageT, NPK_D, G, TWO, true>
+                    : paged_decode_stream_kernel<StorageT, NPK_D, G, TWO, false>;
+  static unsigned long long configured[2] = {0, 0};  // bit d: attribute set on device d
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return NP_ERR_CUDA;
-  if (dev >= 64 || !((__atomic_load_n(&configured, __ATOMIC_ACQUIRE) >> dev) & 1ull)) {
+  if (dev >= 64 ||
+      !((__atomic_load_n(&configured[multi], __ATOMIC_ACQUIRE) >> dev) & 1ull)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget) !=
         cudaSuccess)
       return NP_ERR_CUDA;
-    if (dev < 64) __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
+    if (dev < 64) __atomic_fetch_or(&configured[multi], 1ull << dev, __ATOMIC_ACQ_REL);
   }
   kern<<<L.splits, 32 * (8 + 1), smem, L.stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return NP_ERR_CUDA;
@@ -144,7 +150,6 @@ np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {
   // each when the rows are likely cut into more than 16 pieces (more CTAs
   // than 16 per virtual row), so that one round of loads covers a row's
   // partials.
-  const int mr = L.group * p.query_len;
   cudaError_t rc = cudaErrorInvalidValue;
   bool done = false;
 #if NPK_MERGE_RPW4

@@ -121,6 +121,15 @@ struct StreamKind<float, D, G, MQ> {  // FMA pipes, 1-D bulk copies of token row
   __host__ __device__ static constexpr size_t tile_floats() { return FmaCfg<D, G, MQ>::TILE; }
 };
 
+// A consumer warp's row-end state in shared memory: m[MRP] (log2 units),
+// l[MRP], O[MR][D] floats, MRP = MR rounded up to 4 so that every part and
+// every entry starts on a 16-byte boundary (the fp32 warp stores O rows as
+// 16-byte vectors; D is a multiple of 32).
+__host__ __device__ constexpr int wstate_mrp(int mr) { return (mr + 3) & ~3; }
+__host__ __device__ constexpr size_t wstate_entry_floats(int mr, int d) {
+  return 2 * (size_t)wstate_mrp(mr) + (size_t)mr * d;
+}
+
 // Shared memory: ring (1024-aligned) | full, empty barriers | abort |
 // virtual rows' chunk prefix (int64, V + 1) | their lengths (int32, V) |
 // consumer tiles (16-aligned) | the token warps' states (tw > 1).  hg = kv
@@ -146,20 +155,22 @@ struct StreamSmem {
     return (tiles_offset(hg, sm, stages, vrows) + 8 * K::tile_floats() * sizeof(float) + 15) /
            16 * 16;
   }
+  // tw > 1: ncw consumer warps' row-end states of mr rows each
   __host__ __device__ static constexpr size_t total(int hg, int sm, int stages, int vrows,
-                                                    int tw) {
+                                                    int tw, int ncw, int mr) {
     return 1024 + merge_offset(hg, sm, stages, vrows) +
-           (tw > 1 ? (size_t)kMaxConsumerWarps * StreamWs::entry_floats(D) * sizeof(float) : 0) +
+           (tw > 1 ? (size_t)ncw * wstate_entry_floats(mr, D) * sizeof(float) : 0) +
            (tw > 1 ? 16 : 0);  // + the merge's two mbarriers
   }
 };
 
 // The TW consumer warps of kv head hl (warps hl, hl + HG, ...) left their
-// unnormalised states (m in log2 units, l, O rows) side by side in `ws`;
-// warp tw merges rows tw, tw + TW, ... of them in warp order (max and
-// weights) and stores each row: normalised to `out` when the whole row is
-// this CTA's, else unnormalised to the cut row's partial entry `ent` for the
-// merge kernel.
+// unnormalised states side by side in `ws`, one entry per warp (the layout
+// of wstate_entry_floats); warp tw merges
+// rows tw, tw + TW, ... of them in warp order (max and weights) and stores
+// each row: normalised to `out` when the whole row is this CTA's, else
+// unnormalised to the cut row's partial entry `ent` (the workspace layout:
+// m[16], l[16], O[16][D]) for the merge kernel.
 template <typename T, int D, typename St>
 __device__ __forceinline__ void merge_warp_states(const DecodeParams& p, const float* ws, int hl,
                                                   int HG, int TW, int tw, int MR, int Gr,
@@ -167,7 +178,8 @@ __device__ __forceinline__ void merge_warp_states(const DecodeParams& p, const f
                                                   St keep, int lane) {
   constexpr int RW = kMmaRows;
   constexpr int DL = D >= 32 ? D / 32 : 1;  // dims per lane
-  const int64_t stride = (int64_t)StreamWs::entry_floats(D);
+  const int64_t stride = (int64_t)wstate_entry_floats(MR, D);
+  const int MRP = wstate_mrp(MR);
   const int Q = p.query_len;
   const int d0 = lane * DL;
   for (int row = tw; row < MR; row += TW) {
@@ -180,10 +192,10 @@ __device__ __forceinline__ void merge_warp_states(const DecodeParams& p, const f
     for (int w2 = 0; w2 < TW; ++w2) {
       const float* w = ws + (hl + w2 * HG) * stride;
       const float a = ex2(w[row] - msub);  // a state with nothing in it: m = -inf, a = 0
-      ll = fmaf(w[RW + row], a, ll);
+      ll = fmaf(w[MRP + row], a, ll);
       if (d0 < D) {
 #pragma unroll
-        for (int e = 0; e < DL; ++e) acc[e] = fmaf(w[2 * RW + row * D + d0 + e], a, acc[e]);
+        for (int e = 0; e < DL; ++e) acc[e] = fmaf(w[2 * MRP + row * D + d0 + e], a, acc[e]);
       }
     }
     if (whole) {
@@ -207,14 +219,17 @@ __device__ __forceinline__ void merge_warp_states(const DecodeParams& p, const f
   }
 }
 
-template <typename T, int D, int G, bool TWO>
+// MULTI: built for several consumer warps per kv head (p.token_warps > 1,
+// row-end merges of their states); without it the kernel holds none of
+// that code and reads one warp per head.
+template <typename T, int D, int G, bool TWO, bool MULTI>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     paged_decode_stream_kernel(const __grid_constant__ DecodeParams p) {
   using K = StreamKind<T, D, G, TWO>;
   using C = K;  // chunk geometry (CT, ST)
   constexpr unsigned FULL = 0xffffffffu;
   const int HG = p.head_group;   // kv heads per CTA (the largest divisor of kv_heads <= 8)
-  const int TW = p.token_warps;  // consumer warps per kv head (HG * TW <= 8)
+  const int TW = MULTI ? p.token_warps : 1;  // consumer warps per kv head (HG * TW <= 8)
   const int NCW = HG * TW;       // consumer warps 0 .. NCW-1: warp w reads kv head w % HG
   constexpr int kProducer = kMaxConsumerWarps;  // warp 8
 
@@ -251,8 +266,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   float* tiles = reinterpret_cast<float*>(smem + SS::tiles_offset(HG, SM, stages, V));
   float* wstate =  // TW > 1: the consumer warps' states at a row boundary
       reinterpret_cast<float*>(smem + SS::merge_offset(HG, SM, stages, V));
-  uint64_t* seg_bar = reinterpret_cast<uint64_t*>(wstate + kMaxConsumerWarps *
-                                                             StreamWs::entry_floats(D));
+  // (one 16-byte aligned entry per consumer warp)
+  uint64_t* seg_bar = reinterpret_cast<uint64_t*>(wstate + (size_t)NCW * wstate_entry_floats(MR, D));
   __shared__ int64_t wsum[32];
   __shared__ int64_t range[4];  // vb, tb, ve, te
 
@@ -674,8 +689,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     // merges a share of the rows (in tw order) and stores them or their
     // partials.
     // Bounded waits: a timed-out pipeline returns instead of waiting here.
-    float* my = wstate + (size_t)warp * StreamWs::entry_floats(D);
-    W.store_rows(my, my + kMmaRows, my + 2 * kMmaRows, MR, lane);
+    float* my = wstate + (size_t)warp * wstate_entry_floats(MR, D);
+    W.store_rows(my, my + wstate_mrp(MR), my + 2 * wstate_mrp(MR), MR, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&seg_bar[0]));
     if (!__all_sync(FULL, mbar_wait(smem_u32(&seg_bar[0]), seg_phase, abort))) return;
