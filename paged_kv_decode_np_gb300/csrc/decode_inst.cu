@@ -86,7 +86,7 @@ np_status launch_variant(DecodeLaunch& L, DecodeParams& p) {
 #define NPK_MERGE_RPW4 1
 #endif
 
-// The balanced streamed read: grid = L.splits CTAs (one per SM), 8 kv heads
+// The balanced streamed read: grid = L.splits CTAs (one per SM), HG kv heads
 // per CTA, the virtual-row prefix in shared memory after the ring.
 template <int G, bool TWO>
 np_status launch_stream(DecodeLaunch& L, DecodeParams& p) {

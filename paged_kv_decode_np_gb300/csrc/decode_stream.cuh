@@ -8,22 +8,23 @@
 //
 // Partition (computed on the device from context_lens; no host sync, so the
 // step stays graph-capturable).  Virtual rows v = hgi*rows + r (row r, kv
-// head group hgi) are laid end to end, v's length being the row's context.
-// With W their total and P = gridDim.x (one CTA per SM), the first Pe =
-// min(P, ceil(W / kMinCtaTokens)) CTAs share the stream -- a small step
-// gives each working CTA a few chunks instead of spreading a short row over
-// every SM -- and CTA b < Pe owns the tokens from point(b*W/Pe) up to
-// point((b+1)*W/Pe), where point(u) is the (virtual row, token) holding
-// stream position u, the token rounded down to a whole chunk so that TMA
-// boxes stay block-aligned; CTAs b >= Pe own nothing.  A CTA walks its rows
-// back to back with one producer/consumer pipeline: no drain between rows.
+// head group hgi) are laid end to end, each as ceil(context / CT) chunks of
+// CT tokens (a stage: its last chunk may be short).  With W chunks in all
+// and P = gridDim.x (one CTA per SM), the first Pe = min(P, ceil(W /
+// kMinCtaChunks)) CTAs share the stream -- a small step gives each working
+// CTA a few chunks instead of spreading a short row over every SM -- and CTA
+// b < Pe owns chunks [floor(b*W/Pe), floor((b+1)*W/Pe)); chunk starts are
+// whole chunks of their row, so TMA boxes stay block-aligned; CTAs b >= Pe
+// own nothing.  A CTA walks its rows back to back with one producer/consumer
+// pipeline: no drain between rows.
 //
 // Results.  A row that lies wholly inside one CTA is written straight to
 // `out`.  Only the first and the last row of a CTA can be cut; for those the
-// consumer warp of each kv head stores its unnormalised partial (running max
-// m in log2 units, sum l, accumulator O) in the CTA's slot 0 (its first row)
-// or slot 1 (its last row), and the CTA that owns a cut row (the one where
-// the row begins) leaves a descriptor of it.  A second, small kernel then
+// consumer warps of each kv head store its unnormalised partial (running max
+// m in log2 units, sum l, accumulator O; merged first across the head's
+// warps when several read it) in the CTA's slot 0 (its first row) or slot 1
+// (its last row), and the CTA that owns a cut row (the one where the row
+// begins) leaves a descriptor of it.  A second, small kernel then
 // merges each cut row -- in tasks of a few mma rows of one kv head, dealt
 // over all its blocks -- over the covering CTAs in CTA order (the split
 // read's max-and-weights combine), so results are deterministic and no
