@@ -443,7 +443,8 @@ def test_head_dim_256_with_eight_kv_heads(nplib):
     (20, 1, 128, 16, 4), (1, 8, 128, 16, 1), (1, 16, 128, 32, 1), (2, 8, 128, 16, 2),
     (3, 4, 128, 8, 1), (6, 3, 64, 16, 1), (5, 2, 256, 16, 1), (7, 1, 128, 32, 3),
     (2, 4, 64, 8, 1), (10, 2, 128, 16, 1), (11, 2, 128, 16, 1), (9, 2, 128, 8, 1),
-    (1, 8, 256, 16, 1), (2, 8, 64, 16, 1), (1, 4, 128, 8, 2)])
+    (1, 8, 256, 16, 1), (2, 8, 64, 16, 1), (1, 4, 128, 8, 2),
+    (1, 3, 128, 16, 1), (2, 5, 64, 16, 1), (1, 5, 128, 8, 3)])
 def test_balanced_read(nplib, kv_heads, group, head_dim, block_size, query_len):
     """num_splits = 0: one CTA per SM, equal token shares; rows cut between
     CTAs are merged by the second kernel.  Small totals spread over 152
@@ -465,11 +466,13 @@ def test_balanced_read(nplib, kv_heads, group, head_dim, block_size, query_len):
     (16, 4, 128, 16), (16, 2, 256, 1), (8, 8, 128, 24), (8, 4, 32, 64),
     (4, 4, 128, 16), (12, 1, 256, 3), (4, 8, 64, 1), (1, 8, 128, 16), (2, 4, 128, 3),
     (3, 2, 64, 16), (6, 1, 256, 8), (5, 8, 32, 1), (11, 2, 128, 16), (13, 1, 32, 16),
-    (1, 8, 256, 16), (2, 4, 64, 1)])
+    (1, 8, 256, 16), (2, 4, 64, 1), (1, 3, 64, 16), (2, 5, 128, 16), (1, 7, 32, 8)])
 def test_balanced_read_fp32(nplib, kv_heads, group, head_dim, block_size):
     """fp32 pools on the balanced read (FMA consumers, 1-D bulk copies:
     whole block runs when the pool has just the CTA's kv heads, one copy per
-    token otherwise, in rounds of 32 tokens when a stage holds more)."""
+    token otherwise, in rounds of 32 tokens when a stage holds more).  Odd
+    groups with one or two kv heads: several warps per head whose row-end
+    states hold an odd number of rows (16-byte vector stores)."""
     ctx = [0, 1, 5, 16, 17, 300, 2049, 64, 0, 4000, 31, 7]
     w = _custom(ctx, kv_heads * group, kv_heads, head_dim, block_size, "f32",
                 seed=180 + kv_heads + group + head_dim + block_size)
